@@ -1,0 +1,409 @@
+#!/usr/bin/env python3
+"""Benchmark of the int4 block-quantized MatMulNBits decode GEMV on GB300.
+
+One step = one pass of the hot path over one input batch: the GEMV of the
+chosen workload once per output dtype the workload names (the 4096x4096
+attention projection runs an fp16-output and a bf16-output launch per step).
+
+  value      algorithmic HBM bytes of the step's GEMV calls / device time per
+             step, with inputs resident in HBM.  Weight copies rotate over more
+             than 4x the L2 size so every launch streams its weights from HBM.
+             The K timed steps run as replays of a CUDA graph of captured
+             library launches (the kernel launches are the library's own).
+  e2e        the same metric through the public API with host buffers: each step
+             copies x, qweight, scales and zero-points from pinned host memory,
+             runs the GEMV(s) and copies y back.
+  roofline   the GEMV kernel's achieved bandwidth against the measured HBM peak.
+  cpu_baseline  the CPU oracle timed on a bounded sample on this host's cores.
+
+``--impl reference`` times the CPU oracle alone (the reference arm).  With
+torchrun and N > 1 every rank runs an independent replica (the path has no
+exchange step) and rank 0 prints the line; value sums all ranks' bytes over the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import shutil
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode GEMV µs/call and achieved HBM GB/s (% of GB300 peak) at M=1"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "attn-proj-m1-k4096-n4096"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["mnb", "reference"], default="mnb")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--split-k", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU seconds for the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("int4_block_quantized_mnb_gb300/csrc/mnb_gemv.cu", "include/mnb.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "gemv_dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return d.get("bytes_per_launch", {}).get(workload)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.reader = None
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if exe is None:
+            return
+        self.proc = subprocess.Popen(
+            [exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+             "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def oracle_sample(w, inp, seconds, threads):
+    """Times the CPU oracle on about `seconds` of work: a sample of output
+    columns of the workload.  Returns (GB/s, description, threads used)."""
+    from oracle import Oracle
+    o = Oracle()
+    n_calls = len(w.out_dtypes)      # one oracle pass yields every output dtype
+    rng = np.random.default_rng(0)
+    probe = rng.choice(w.N, size=min(w.N, max(threads, 16)), replace=False).astype(np.int64)
+    t0 = time.perf_counter()
+    o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=probe, threads=threads)
+    rate = probe.size / max(time.perf_counter() - t0, 1e-6)          # columns per second
+    ncols = int(max(threads, min(w.N, rate * seconds)))
+    cols = rng.choice(w.N, size=ncols, replace=False).astype(np.int64)
+    t0 = time.perf_counter()
+    o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=cols, threads=threads)
+    dt = time.perf_counter() - t0
+    gbs = w.algorithmic_bytes() * n_calls * (ncols / w.N) / dt / 1e9
+    desc = (f"{ncols} of {w.N} output columns (all {w.M} rows, full K={w.K}), one pass producing "
+            f"the fp16 and bf16 results, {dt:.1f} s on {threads} threads")
+    return gbs, desc, dt
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    from int4_block_quantized_mnb_gb300.synth import make_inputs
+    from oracle import Oracle
+    inp = make_inputs(w.M, w.N, w.K, seed=0)
+    o = Oracle()
+    threads = os.cpu_count() or 1
+    n_calls = len(w.out_dtypes)
+    rng = np.random.default_rng(0)
+    # calibrate: columns per second on all host threads
+    probe = rng.choice(w.N, size=min(w.N, max(threads, 16)), replace=False).astype(np.int64)
+    t0 = time.perf_counter()
+    o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=probe, threads=threads)
+    rate = probe.size / max(time.perf_counter() - t0, 1e-6)
+    budget = 120.0
+    per_step = int(max(1, min(w.N, rate * budget / max(1, args.steps + args.warmup))))
+    cols = [rng.choice(w.N, size=per_step, replace=False).astype(np.int64)
+            for _ in range(min(args.steps + args.warmup, 64))]
+    for i in range(args.warmup):
+        o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=cols[i % len(cols)],
+               threads=threads)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=cols[i % len(cols)],
+               threads=threads)
+    dt = time.perf_counter() - t0
+    step_bytes = w.algorithmic_bytes() * n_calls * per_step / w.N
+    value = step_bytes * args.steps / dt / 1e9
+    sample = (f"each step: {per_step} of {w.N} output columns (all {w.M} rows, full K={w.K}) of "
+              f"{w.name}, one oracle pass producing the fp16 and bf16 results")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N,
+                   "out_dtypes": list(w.out_dtypes)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- GPU arm --
+
+def main():
+    args = parse()
+    from int4_block_quantized_mnb_gb300.synth import WORKLOADS, make_inputs
+    if args.workload not in WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {list(WORKLOADS)}")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    rank, local_rank, world = dist_env()
+    # The CPU oracle's thread pool is created before the first GPU call.
+    inp = make_inputs(w.M, w.N, w.K, seed=0)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        gbs, desc, _ = oracle_sample(w, inp, args.cpu_seconds, threads)
+        cpu = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+
+    import torch
+    import int4_block_quantized_mnb_gb300 as mnb
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    mnb.load()
+
+    def to_dev(a, dtype):
+        return torch.from_numpy(a.view(np.int16).copy() if a.dtype == np.uint16 else a).view(dtype).to(dev)
+
+    x = to_dev(inp.x, torch.float16)
+    q0 = to_dev(inp.qweight, torch.uint8)
+    s0 = to_dev(inp.scales, torch.float16)
+    z0 = to_dev(inp.zp, torch.uint8)
+    outs = list(w.out_dtypes)
+    L = len(outs)
+    ys = {o: torch.empty((w.M, w.N), dtype=torch.float16 if o == "f16" else torch.bfloat16,
+                         device=dev) for o in outs}
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    wbytes = q0.numel() + 2 * s0.numel() + z0.numel()
+    R = max(L, math.ceil(4 * l2 / wbytes))
+    R = int(math.ceil(R / L) * L)
+    copies = [(q0, s0, z0)] + [(q0.clone(), s0.clone(), z0.clone()) for _ in range(R - 1)]
+    split_k = args.split_k if args.split_k else mnb.split_k_auto(w.M, w.N, w.K)
+    stream = torch.cuda.Stream(dev)
+
+    def step(j):
+        # one step: every output dtype of the workload, each on its own weight copy
+        for i, o in enumerate(outs):
+            q, s, z = copies[(j * L + i) % R]
+            mnb.gemv(x, q, s, z, out_dtype=o, split_k=split_k, y=ys[o], stream=stream)
+
+    # Warm-up: W eager steps.
+    with torch.cuda.stream(stream):
+        for j in range(args.warmup):
+            step(j)
+    torch.cuda.synchronize(dev)
+
+    # Graph of G steps, G * L a multiple of R so copies rotate without reuse.
+    base = R // L
+    G = min(base * max(1, 4000 // (base * L)), args.steps)
+    graphs = []
+    full, rem = divmod(args.steps, G)
+
+    def capture(nsteps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(nsteps):
+                    step(j)
+        return g
+
+    g_main = capture(G) if full else None
+    g_rem = capture(rem) if rem else None
+    for g in (g_main, g_rem):
+        if g is not None:
+            g.replay()       # uploads the graph; not timed
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(full):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([t_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_ms = float(t.item())
+
+    bytes_call = w.algorithmic_bytes()
+    launches = args.steps * L
+    per_launch_s = t_ms / 1e3 / launches
+    value = bytes_call * launches * world / (t_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_call / per_launch_s / 1e9
+
+    # End to end through the public API with pinned host buffers.
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.from_numpy(inp.x.view(np.int16).copy()).view(torch.float16).pin_memory()
+        hq = torch.from_numpy(inp.qweight).pin_memory()
+        hs = torch.from_numpy(inp.scales.view(np.int16).copy()).view(torch.float16).pin_memory()
+        hz = torch.from_numpy(inp.zp).pin_memory()
+        hy = {o: torch.empty(ys[o].shape, dtype=ys[o].dtype).pin_memory() for o in outs}
+        dq, ds, dz, dx = torch.empty_like(q0), torch.empty_like(s0), torch.empty_like(z0), torch.empty_like(x)
+        h2d = hx.numel() * 2 + hq.numel() + hs.numel() * 2 + hz.numel()
+        d2h = sum(hy[o].numel() * 2 for o in outs)
+        E = max(3, min(args.steps, int(4e9 / h2d)))
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            ds.copy_(hs, non_blocking=True)
+            dz.copy_(hz, non_blocking=True)
+            for o in outs:
+                mnb.gemv(dx, dq, ds, dz, out_dtype=o, split_k=split_k, y=ys[o], stream=stream)
+                hy[o].copy_(ys[o], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                e2e_step()
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(E):
+                e2e_step()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        te = e0.elapsed_time(e1) / 1e3
+        e2e = {"value": bytes_call * L * E / te / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": E}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "us_per_call": per_launch_s * 1e6,
+        "pct_of_hbm_peak": 100.0 * achieved / peak,
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "out_dtypes": outs,
+                   "split_k": split_k, "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": f"inputs larger than L2: {R} rotating weight copies, "
+                         f"{R * wbytes / 2**20:.0f} MiB vs L2 {l2 / 2**20:.0f} MiB",
+                   "timing": f"CUDA events around {full} replays of a {G}-step graph"
+                             + (f" + 1 replay of a {rem}-step graph" if rem else "")
+                             + "; warm-up: W eager steps, then one untimed replay per graph"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": recorded_traffic(w.name),
+                     "algorithmic_bytes_per_launch": bytes_call},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,151 @@
+/*
+ * mnb.h -- C ABI of the GB300 (sm_103a) int4 block-quantized MatMulNBits
+ * decode GEMV library (libmnb.so).
+ *
+ * The operation (one launch computes every output element):
+ *
+ *     y[m,n] = round( sum_k x[m,k] * (q[n,k] - zp[n, k/32]) * scale[n, k/32] )
+ *
+ * with 4-bit weight codes q and 4-bit asymmetric zero-points zp at block size
+ * 32, fp16 activations x and fp16 scales, fp32 accumulation, and a result
+ * rounded to fp16; on request the fp16 result is narrowed to bf16 in the same
+ * epilogue (fp32 -> fp16 -> bf16, two round-to-nearest-even steps).
+ *
+ *   - "perf(cuda): let the split-K decode GEMV store bf16 directly"
+ *     (onnx-genai PR 1550), paragraphs 1-2: the block-32 split-K decode GEMV,
+ *     its fp16 epilogue on one lane per output column, and the launch-uniform
+ *     bf16 narrowing store that is bit-identical to casting the fp16 result.
+ *     Paragraph 4 (the small-batch row loop): a launch must write every
+ *     element of its output; here one call always writes all M*N elements.
+ *   - "PORT-1 (offline bias+interleave) -- measured NO-GO on the multicol
+ *     asymmetric-zp GEMV" (onnx-genai PR 1002), "Why the premise fails
+ *     here" point 1: 4-bit weights with a per-block asymmetric zero-point.
+ *
+ * Conventions shared by every entry point:
+ *   - Memory: all array arguments are device pointers owned by the caller
+ *     (the library allocates nothing).  Calls are asynchronous on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream); a kernel-side fault
+ *     surfaces at the caller's next synchronisation.
+ *   - Errors: every entry point returns an mnb_status.  Nothing is printed and
+ *     no exception crosses the ABI.  mnb_last_error_detail() returns a
+ *     thread-local text describing the calling thread's last failure.
+ *   - Thread safety: the entry points are re-entrant; the only shared state is
+ *     a set of atomic launch counters and a per-device error word.
+ */
+#ifndef MNB_H_
+#define MNB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MNB_ABI_VERSION 1
+
+/* Output element type of mnb_gemv. */
+typedef enum mnb_out_dtype {
+    MNB_OUT_F16 = 0,   /* y holds the fp16 result */
+    MNB_OUT_BF16 = 1   /* y holds bf16( fp16 result ), i.e. double-rounded */
+} mnb_out_dtype;
+
+typedef enum mnb_status {
+    MNB_OK = 0,
+    MNB_ERR_NULL = 1,    /* a required pointer is NULL */
+    MNB_ERR_SHAPE = 2,   /* M, N or K outside the supported range */
+    MNB_ERR_BLOCK = 3,   /* block size other than 32 */
+    MNB_ERR_DTYPE = 4,   /* out_dtype not an mnb_out_dtype */
+    MNB_ERR_SPLITK = 5,  /* split_k outside [0, mnb_max_split_k] or too small for K */
+    MNB_ERR_ALIGN = 6,   /* a pointer is misaligned for its element type (see mnb_gemv) */
+    MNB_ERR_ALIAS = 7,   /* y overlaps an input array */
+    MNB_ERR_CUDA = 8,    /* a CUDA runtime call failed; see mnb_last_error_detail */
+    MNB_ERR_DEVICE = 9   /* the current device is not an sm_103 GPU */
+} mnb_status;
+
+/* Limits of mnb_gemv. */
+#define MNB_MAX_M 8            /* decode batch rows per call */
+#define MNB_BLOCK 32           /* quantization block along K */
+#define MNB_MAX_SPLIT_K 8      /* K-partitions reduced inside one thread-block cluster */
+
+/*
+ * mnb_gemv -- the decode GEMV, all M rows in one launch.
+ *
+ *   x        [M][K] fp16, row-major, 2-byte aligned (16-byte alignment is
+ *            faster).
+ *   qweight  [N][K/2] uint8, row-major, 16-byte aligned.  Byte k/2 of row n
+ *            holds code q[n,k] in its low nibble for even k and in its high
+ *            nibble for odd k.
+ *   scales   [N][K/32] fp16, row-major, 2-byte aligned.
+ *   zp       [N][ceil(K/64)] uint8, row-major, any alignment.  Byte b/2 of
+ *            row n holds zero-point zp[n,b] in its low nibble for even block
+ *            index b and in its high nibble for odd b; when K/32 is odd the
+ *            last high nibble of each row is ignored.
+ *   y        [M][N] fp16 (out_dtype MNB_OUT_F16) or bf16 (MNB_OUT_BF16),
+ *            row-major, 2-byte aligned, must not overlap any input.  Every
+ *            one of its M*N elements is written by this call.
+ *   M        1..MNB_MAX_M.   N >= 1.   K >= 32 and a multiple of 32.
+ *   block    must be MNB_BLOCK (32).
+ *   out_dtype  an mnb_out_dtype.  It changes only the final store: for the
+ *            same inputs and split_k the bf16 result equals the
+ *            round-to-nearest-even bf16 narrowing of the fp16 result, bit
+ *            for bit.
+ *   split_k  number of contiguous K ranges (whole 32-blocks) each output is
+ *            split into; the ranges are reduced in a fixed order inside one
+ *            thread-block cluster.  0 = chosen by the library
+ *            (mnb_split_k_auto); otherwise 1..min(MNB_MAX_SPLIT_K, K/32) and
+ *            at least mnb_min_split_k(M, K).  Results meet the same error
+ *            bound for every split_k; the fp16 bits may differ between
+ *            split_k values.
+ *   stream   cudaStream_t to launch on (NULL = legacy default stream).
+ *
+ * Returns MNB_OK once the kernel is enqueued, or the first failing check.
+ * Nothing is launched on a non-OK return.
+ */
+int mnb_gemv(const void *x, const uint8_t *qweight, const void *scales, const uint8_t *zp,
+             void *y, int M, int N, int K, int block, int out_dtype, int split_k,
+             void *stream);
+
+/* split_k that mnb_gemv uses for split_k = 0 on the current device.
+ * Writes it to *split_k.  Same shape checks and statuses as mnb_gemv. */
+int mnb_split_k_auto(int M, int N, int K, int *split_k);
+
+/* Smallest split_k mnb_gemv accepts for this M and K (a CTA covers at most
+ * 8192 values of K when M >= 4 and 16384 otherwise).  Writes it to *min_split. */
+int mnb_min_split_k(int M, int K, int *min_split);
+
+/* Largest split_k mnb_gemv accepts for this K: min(MNB_MAX_SPLIT_K, K/32). */
+int mnb_max_split_k(int K, int *max_split);
+
+/* Static text for a status code (never NULL). */
+const char *mnb_status_string(int status);
+
+/* Thread-local text about the calling thread's last non-OK return (empty when
+ * none).  Valid until the thread's next call into the library. */
+const char *mnb_last_error_detail(void);
+
+/* Device-side error word of the current device: 0, or the first code a
+ * kernel recorded when one of its bounded waits gave up (1 = stage data never
+ * arrived, 2 = a stage was never released, 3 = copies still in flight at exit,
+ * 4 = a reduction slot was never filled or freed).  Enqueues a read on
+ * `stream`, synchronises that stream and writes the word to *code; clears it
+ * when `clear` is non-zero.  Returns MNB_ERR_CUDA if the read fails. */
+int mnb_device_error(void *stream, unsigned int *code, int clear);
+
+/* Launch counters, for tests that must prove the GPU kernel ran:
+ *   [0] launches, [1] fp16-output launches, [2] bf16-output launches,
+ *   [3] launches with split_k > 1 (cluster reduction), [4 + M - 1] launches
+ *   with M rows (M = 1..8).
+ * Copies min(n, MNB_NUM_COUNTERS) counters to out; returns how many. */
+#define MNB_NUM_COUNTERS 12
+int mnb_debug_counters(uint64_t *out, int n);
+void mnb_debug_counters_reset(void);
+
+/* MNB_ABI_VERSION of the loaded library. */
+int mnb_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MNB_H_ */

@@ -1,1 +1,112 @@
-"""int4 block-quantized MatMulNBits decode GEMV for GB300 (sm_103a)."""
+"""int4 block-quantized MatMulNBits decode GEMV for GB300 (sm_103a).
+
+``gemv`` computes y[m,n] = sum_k x[m,k] * (q[n,k] - zp[n,k/32]) * s[n,k/32]
+for M <= 8 decode rows in one launch of the library's CUDA kernel, rounds to
+fp16 and optionally narrows to bf16.  This module only marshals torch tensors
+into the C ABI of ``libmnb.so`` (include/mnb.h); every arithmetic step runs in
+the CUDA kernel.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._native import (BLOCK, MAX_M, MAX_SPLIT_K, OUT_BF16, OUT_F16, MnbError, check,
+                      load)
+
+__all__ = ["gemv", "gemv_ptr", "split_k_auto", "min_split_k", "max_split_k", "counters",
+           "reset_counters", "device_error", "MnbError", "OUT_F16", "OUT_BF16", "BLOCK",
+           "MAX_M", "MAX_SPLIT_K"]
+
+_DTYPES = {"f16": OUT_F16, "float16": OUT_F16, "bf16": OUT_BF16, "bfloat16": OUT_BF16}
+
+
+def _out_code(out_dtype) -> int:
+    import torch
+    if out_dtype in (torch.float16,):
+        return OUT_F16
+    if out_dtype in (torch.bfloat16,):
+        return OUT_BF16
+    if isinstance(out_dtype, str) and out_dtype in _DTYPES:
+        return _DTYPES[out_dtype]
+    if out_dtype in (OUT_F16, OUT_BF16):
+        return int(out_dtype)
+    raise ValueError(f"out_dtype must be f16 or bf16, got {out_dtype!r}")
+
+
+def gemv_ptr(x: int, qweight: int, scales: int, zp: int, y: int, M: int, N: int, K: int,
+             block: int = BLOCK, out_dtype: int = OUT_F16, split_k: int = 0,
+             stream: int = 0) -> None:
+    """Raw C-ABI call with integer device pointers; raises MnbError on failure."""
+    check(load().mnb_gemv(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, stream))
+
+
+def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stream=None):
+    """y = MatMulNBits(x, qweight, scales, zp) on the current CUDA device.
+
+    x [M][K] float16, qweight [N][K/2] uint8, scales [N][K/32] float16,
+    zp [N][ceil(K/64)] uint8, all contiguous CUDA tensors.  Returns y [M][N]
+    float16 or bfloat16 (or writes the given ``y``).
+    """
+    import torch
+    code = _out_code(out_dtype)
+    if x.dim() != 2 or qweight.dim() != 2 or scales.dim() != 2 or zp.dim() != 2:
+        raise ValueError("x, qweight, scales and zp must be 2-D")
+    M, K = x.shape
+    N = qweight.shape[0]
+    if qweight.shape[1] * 2 != K or scales.shape != (N, K // BLOCK) or \
+            zp.shape != (N, (K // BLOCK + 1) // 2):
+        raise ValueError("shapes do not match x [M][K], qweight [N][K/2], scales [N][K/32], "
+                         "zp [N][ceil(K/64)]")
+    if x.dtype != torch.float16 or scales.dtype != torch.float16 or \
+            qweight.dtype != torch.uint8 or zp.dtype != torch.uint8:
+        raise TypeError("x and scales must be float16; qweight and zp uint8")
+    for t in (x, qweight, scales, zp):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    ydt = torch.float16 if code == OUT_F16 else torch.bfloat16
+    if y is None:
+        y = torch.empty((M, N), dtype=ydt, device=x.device)
+    elif y.shape != (M, N) or y.dtype != ydt or not y.is_contiguous() or not y.is_cuda:
+        raise ValueError("y must be a contiguous [M][N] CUDA tensor of the output dtype")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        gemv_ptr(x.data_ptr(), qweight.data_ptr(), scales.data_ptr(), zp.data_ptr(),
+                 y.data_ptr(), M, N, K, BLOCK, code, int(split_k), stream.cuda_stream)
+    return y
+
+
+def split_k_auto(M: int, N: int, K: int) -> int:
+    out = ctypes.c_int(0)
+    check(load().mnb_split_k_auto(M, N, K, ctypes.byref(out)))
+    return out.value
+
+
+def min_split_k(M: int, K: int) -> int:
+    out = ctypes.c_int(0)
+    check(load().mnb_min_split_k(M, K, ctypes.byref(out)))
+    return out.value
+
+
+def max_split_k(K: int) -> int:
+    out = ctypes.c_int(0)
+    check(load().mnb_max_split_k(K, ctypes.byref(out)))
+    return out.value
+
+
+def counters() -> list:
+    buf = (ctypes.c_uint64 * 12)()
+    n = load().mnb_debug_counters(buf, 12)
+    return [int(buf[i]) for i in range(n)]
+
+
+def reset_counters() -> None:
+    load().mnb_debug_counters_reset()
+
+
+def device_error(stream=None, clear: bool = True) -> int:
+    import torch
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    code = ctypes.c_uint(0)
+    check(load().mnb_device_error(s, ctypes.byref(code), 1 if clear else 0))
+    return code.value

@@ -1,0 +1,85 @@
+"""The C-ABI library loads, exports every symbol include/mnb.h declares, and
+rejects bad arguments on the host before touching a device (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mnb.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mnb_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int4_block_quantized_mnb_gb300 import build, _native
+    build.build()
+    return _native.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mnb_gemv", "mnb_status_string", "mnb_last_error_detail", "mnb_split_k_auto",
+              "mnb_device_error", "mnb_debug_counters"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from int4_block_quantized_mnb_gb300 import _native
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in mnb.h but not exported"
+        assert name in _native.SIGNATURES, f"{name} has no ctypes declaration"
+
+
+def test_status_strings(lib):
+    for s in range(10):
+        assert lib.mnb_status_string(s)
+    assert lib.mnb_status_string(99) == b"unknown status"
+    assert lib.mnb_abi_version() == 1
+
+
+# Fake but 16-byte-aligned, non-overlapping addresses: validation fails before
+# anything is dereferenced or launched.
+X, Q, S, Z, Y = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000
+
+
+def call(lib, x=X, q=Q, s=S, z=Z, y=Y, M=1, N=64, K=256, block=32, out=0, split=1):
+    return lib.mnb_gemv(x, q, s, z, y, M, N, K, block, out, split, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=0), 1), (dict(q=0), 1), (dict(s=0), 1), (dict(z=0), 1), (dict(y=0), 1),
+    (dict(block=64), 3), (dict(block=16), 3),
+    (dict(M=0), 2), (dict(M=9), 2), (dict(N=0), 2), (dict(N=-3), 2),
+    (dict(K=0), 2), (dict(K=48), 2), (dict(K=31), 2),
+    (dict(out=2), 4), (dict(out=-1), 4),
+    (dict(q=Q + 8), 6), (dict(x=X + 1), 6), (dict(s=S + 1), 6), (dict(y=Y + 1), 6),
+    (dict(y=X), 7), (dict(y=Q + 16), 7), (dict(y=S), 7), (dict(y=Z), 7),
+    (dict(split=9), 5), (dict(split=-1), 5), (dict(K=64, split=3), 5),
+    (dict(M=8, K=16384, split=1), 5),
+])
+def test_host_validation(lib, kw, status):
+    assert call(lib, **kw) == status
+    assert lib.mnb_last_error_detail()
+
+
+def test_split_limits(lib):
+    out = ctypes.c_int(0)
+    assert lib.mnb_max_split_k(4096, ctypes.byref(out)) == 0 and out.value == 8
+    assert lib.mnb_max_split_k(64, ctypes.byref(out)) == 0 and out.value == 2
+    assert lib.mnb_min_split_k(8, 16384, ctypes.byref(out)) == 0 and out.value == 2
+    assert lib.mnb_min_split_k(1, 16384, ctypes.byref(out)) == 0 and out.value == 1
+    assert lib.mnb_min_split_k(9, 4096, ctypes.byref(out)) == 2
+    assert lib.mnb_max_split_k(4096, None) == 1
+
+
+def test_no_fallback_when_library_missing(tmp_path):
+    from int4_block_quantized_mnb_gb300 import _native
+    with pytest.raises(RuntimeError, match="not found"):
+        _native.load(str(tmp_path / "libmnb.so"))

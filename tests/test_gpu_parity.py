@@ -1,0 +1,160 @@
+"""Parity of the sm_103a GEMV (through the C ABI) with the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+import int4_block_quantized_mnb_gb300 as mnb
+from int4_block_quantized_mnb_gb300.synth import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from int4_block_quantized_mnb_gb300 import build
+    build.build()
+    mnb.load()
+
+
+SMALL = [(1, 32), (7, 64), (33, 96), (257, 1024), (130, 4096), (19, 8192)]
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("N,K", SMALL)
+@pytest.mark.parametrize("split", ["auto", 1, "max"])
+def test_small_shapes(M, N, K, split):
+    inp = make_inputs(M, N, K, seed=100 + M * 7 + N + K)
+    lo, hi = mnb.min_split_k(M, K), mnb.max_split_k(K)
+    sk = {"auto": 0, 1: lo, "max": hi}[split]
+    dev = _gpu.to_device(inp)
+    y16 = _gpu.bits(_gpu.run(dev, "f16", sk))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16", sk))
+    _gpu.compare(inp, y16, ybf)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_every_split_k(M):
+    N, K = 300, 512
+    inp = make_inputs(M, N, K, seed=5)
+    dev = _gpu.to_device(inp)
+    for sk in range(mnb.min_split_k(M, K), mnb.max_split_k(K) + 1):
+        y16 = _gpu.bits(_gpu.run(dev, "f16", sk))
+        ybf = _gpu.bits(_gpu.run(dev, "bf16", sk))
+        _gpu.compare(inp, y16, ybf)
+
+
+def sample_cols(N, rng, n=384):
+    edge = np.r_[np.arange(min(N, 64)), np.arange(max(0, N - 64), N)]
+    return np.unique(np.r_[edge, rng.choice(N, size=min(N, n), replace=False)]).astype(np.int64)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_full_size(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w.M, w.N, w.K, seed=0)
+    dev = _gpu.to_device(inp)
+    y16 = _gpu.bits(_gpu.run(dev, "f16"))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16"))
+    # every element written (the NaN sentinel is gone) in both arms
+    o = _gpu.oracle()
+    assert not np.isnan(o.f16_to_f64(y16)).any()
+    assert not np.isnan(o.bf16_to_f64(ybf)).any()
+    # the bf16 arm is the narrowed fp16 arm everywhere, not only where sampled
+    assert np.array_equal(ybf, o.f16_to_bf16(y16))
+    cols = None if w.N * w.K <= 1 << 20 else sample_cols(w.N, np.random.default_rng(1))
+    _gpu.compare(inp, y16, ybf, cols=cols)
+
+
+@pytest.mark.parametrize("M", [2, 4, 8])
+def test_small_batch_every_row_written(M):
+    """A launch owns all M*N outputs: no row is left at the sentinel."""
+    N, K = 8192, 8192
+    inp = make_inputs(M, N, K, seed=M)
+    dev = _gpu.to_device(inp)
+    y = _gpu.run(dev, "bf16")
+    ybits = _gpu.bits(y)
+    assert not np.isnan(_gpu.oracle().bf16_to_f64(ybits)).any()
+    rows = np.arange(M)
+    # rows are distinct computations: no row is a copy of row 0
+    for m in rows[1:]:
+        assert not np.array_equal(ybits[m], ybits[0])
+    cols = sample_cols(N, np.random.default_rng(M), n=128)
+    y16 = _gpu.bits(_gpu.run(dev, "f16"))
+    _gpu.compare(inp, y16, ybits, cols=cols)
+
+
+def test_counters_prove_the_kernel_ran():
+    inp = make_inputs(2, 64, 256, seed=3)
+    dev = _gpu.to_device(inp)
+    before = mnb.counters()
+    _gpu.run(dev, "f16", 1)
+    _gpu.run(dev, "bf16", 2)
+    after = mnb.counters()
+    d = [a - b for a, b in zip(after, before)]
+    assert d[0] == 2 and d[1] == 1 and d[2] == 1 and d[3] == 1 and d[4 + 2 - 1] == 2
+
+
+def test_misaligned_pointers():
+    """x, scales and zp need not be 16-byte aligned (qweight must be)."""
+    M, N, K = 2, 75, 96 * 3
+    inp = make_inputs(M, N, K, seed=9)
+    x, q, s, z = _gpu.to_device(inp)
+    xb = torch.empty(M * K + 3, dtype=torch.float16, device="cuda")
+    sb = torch.empty(s.numel() + 5, dtype=torch.float16, device="cuda")
+    zb = torch.empty(z.numel() + 7, dtype=torch.uint8, device="cuda")
+    xo = xb[1:1 + M * K].view(M, K); xo.copy_(x)
+    so = sb[3:3 + s.numel()].view(s.shape); so.copy_(s)
+    zo = zb[5:5 + z.numel()].view(z.shape); zo.copy_(z)
+    ref16 = _gpu.bits(_gpu.run((x, q, s, z), "f16", 1))
+    got16 = _gpu.bits(_gpu.run((xo, q, so, zo), "f16", 1))
+    assert np.array_equal(ref16, got16)
+    got_bf = _gpu.bits(_gpu.run((xo, q, so, zo), "bf16", 2))
+    _gpu.compare(inp, _gpu.bits(_gpu.run((xo, q, so, zo), "f16", 2)), got_bf)
+
+
+def test_zero_point_padding_nibble_ignored():
+    M, N, K = 1, 40, 96   # 3 blocks per row: the last high zp nibble is padding
+    inp = make_inputs(M, N, K, seed=4)
+    dev = list(_gpu.to_device(inp))
+    a = _gpu.bits(_gpu.run(tuple(dev), "f16"))
+    dev[3] = dev[3] ^ torch.tensor([0, 0xF0], dtype=torch.uint8, device="cuda")
+    b = _gpu.bits(_gpu.run(tuple(dev), "f16"))
+    assert np.array_equal(a, b)
+
+
+def test_cuda_graph_capture_matches_eager():
+    inp = make_inputs(1, 1000, 4096, seed=11)
+    x, q, s, z = _gpu.to_device(inp)
+    eager = mnb.gemv(x, q, s, z, "bf16")
+    torch.cuda.synchronize()
+    y = torch.empty_like(eager)
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            mnb.gemv(x, q, s, z, "bf16", y=y)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.view(torch.int16), y.view(torch.int16))
+
+
+def test_non_finite_inputs_follow_ieee():
+    M, N, K = 1, 16, 64
+    inp = make_inputs(M, N, K, seed=2)
+    xs = inp.x.copy()
+    xs[0, 3] = 0x7C00          # +inf
+    inp.x = xs
+    y16 = _gpu.bits(_gpu.run(_gpu.to_device(inp), "f16"))
+    ref = _gpu.oracle().gemv(inp.x, inp.qweight, inp.scales, inp.zp, M, N, K)
+    o = _gpu.oracle()
+    g, r = o.f16_to_f64(y16), o.f16_to_f64(ref["y_f16"])
+    assert np.array_equal(np.isnan(g), np.isnan(r))
+    assert np.array_equal(g[np.isinf(r)], r[np.isinf(r)])
+
+
+def test_no_device_error_recorded():
+    assert mnb.device_error() == 0

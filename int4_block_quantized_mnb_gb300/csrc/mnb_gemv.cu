@@ -58,11 +58,15 @@ namespace mnb {
 constexpr int kBlock = MNB_BLOCK;
 constexpr int kMaxM = MNB_MAX_M;
 constexpr int kMaxSplit = MNB_MAX_SPLIT_K;
-constexpr int kMaxWarpsPerGroup = 16;
-constexpr int kMaxThreads = 17 * 32;              // 16 consumer warps + 1 producer
+
+// Consumer warps per CTA: 12 for M <= 2 keeps at most 4 warps (14 with the
+// producer and epilogue warps) on an SM sub-partition, i.e. 128 registers per thread.
+constexpr int consumer_warp_budget(int M) { return M <= 2 ? 12 : 16; }
+constexpr int max_threads(int M) { return (consumer_warp_budget(M) + 2) * 32; }
 constexpr int kSmemBudget = 200 * 1024;           // stages + bookkeeping
 constexpr int kPartBudget = 32 * 1024;            // cluster partial sums per CTA
-constexpr int kMaxStages = 12;
+constexpr int kMaxStages = 16;
+constexpr int kSlotsPerGroup = 4;               // reduction slots a group may have pending
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 enum : unsigned {
@@ -88,6 +92,7 @@ struct Params {
   int groups;       // consumer groups per CTA
   int wpg;          // warps per group
   int stages;
+  int rows_stage;   // rows of the weight matrix per stage (a multiple of the chunk rows)
   int q_pitch;      // bytes per row inside a stage's weight area
   int q_bytes, sc_bytes, zp_bytes, stage_bytes;
   int bar_offset;   // shared-memory offset of the mbarrier array
@@ -190,6 +195,14 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank
   return v;
 }
 
+// (a & mask) | magic in one LOP3 (the compiler splits it in two when both
+// constants are immediates).
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(magic));
+  return d;
+}
+
 // (q - zp) for two codes: packed fp16 subtraction of magic-biased values.
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -274,9 +287,12 @@ __device__ __forceinline__ RegionCopy plan_region(unsigned char* dst_base, const
 // ------------------------------------------------------------------ kernel --
 
 template <int M, int KPL, int RC>
-__global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const Params p) {
+__global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p) {
   constexpr int kWords = KPL / 8;                   // 32-bit code words per lane segment
-  constexpr int kVals = RC * M;                     // (row, m) values per lane per tile
+  constexpr int kLaneBlocks = KPL >= 32 ? KPL / 32 : 1;   // 32-blocks a lane's segment touches
+  constexpr int kBlockWords = KPL >= 32 ? 4 : kWords;     // words of the segment in one block
+  static_assert(KPL == 16 || KPL == 32 || KPL == 64, "segment of 16, 32 or 64 codes");
+  constexpr int kVals = RC * M;                     // (row, m) values per lane per stage
   constexpr int kVP = Pow2Ceil<kVals>::value;
   constexpr int kOwnerShift = 5 - (kVP == 1 ? 0 : kVP == 2 ? 1 : kVP == 4 ? 2 : kVP == 8 ? 3 : kVP == 16 ? 4 : 5);
   static_assert(kVP <= 32, "too many values per lane");
@@ -285,14 +301,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const Params p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int consumer_warps = p.groups * p.wpg;
+  const int producer_warp = consumer_warps;
+  const int epilogue_warp = consumer_warps + 1;
+  const int nslots = p.groups * kSlotsPerGroup;
 
+  // mbarriers:
+  //   full[s]   (stage)  1 arrival + transaction bytes: the stage's data landed
+  //   empty[s]  (stage)  wpg arrivals: the group's K-slice warps hold the data
+  //                      in registers, the stage may be refilled
+  //   ready[j]  (slot)   wpg arrivals: every K-slice warp filed its partial sums
+  //   free[j]   (slot)   1 arrival: the epilogue has consumed the slot
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_offset);
-  // bars: full[stages], empty[stages], rfull[groups][2], rfree[groups][2]
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * p.stages;
-  const uint32_t rfull0 = empty0 + 8u * p.stages;
-  const uint32_t rfree0 = rfull0 + 16u * p.groups;
-  float* red = reinterpret_cast<float*>(smem + p.red_offset);     // [groups][2][wpg][kVP]
+  const uint32_t ready0 = empty0 + 8u * p.stages;
+  const uint32_t free0 = ready0 + 8u * nslots;
+  float* red = reinterpret_cast<float*>(smem + p.red_offset);     // [slots][wpg][RC * M]
   float* part = reinterpret_cast<float*>(smem + p.part_offset);   // [cluster rows][M]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.flag_offset);
 
@@ -304,9 +328,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const Params p) {
   const int row_begin = static_cast<int>((static_cast<long long>(unit) * p.N) / units);
   const int row_end = static_cast<int>((static_cast<long long>(unit + 1) * p.N) / units);
   const int nrows = row_end - row_begin;
-  const int ntiles = (nrows + RC - 1) / RC;
-  const int b_begin = static_cast<int>((static_cast<long long>(rank) * p.C) / split);
-  const int b_end = static_cast<int>((static_cast<long long>(rank + 1) * p.C) / split);
+  const int ntiles = (nrows + RC - 1) / RC;         // one stage holds RC rows
+  // K ranges are whole multiples of the lane segment's blocks (2 when KPL = 64).
+  const int seg_units = p.C / kLaneBlocks;
+  const int b_begin = kLaneBlocks * static_cast<int>((static_cast<long long>(rank) * seg_units) / split);
+  const int b_end = kLaneBlocks * static_cast<int>((static_cast<long long>(rank + 1) * seg_units) / split);
   const int k_begin = b_begin * kBlock;
   const int k_len = (b_end - b_begin) * kBlock;
 
@@ -315,18 +341,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const Params p) {
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, p.wpg);
     }
-    for (int g = 0; g < p.groups; ++g) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(rfull0 + 16u * g + 8u * b, p.wpg);
-        mbar_init(rfree0 + 16u * g + 8u * b, 1);
-      }
+    for (int j = 0; j < nslots; ++j) {
+      mbar_init(ready0 + 8u * j, p.wpg);
+      mbar_init(free0 + 8u * j, 1);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  if (warp == consumer_warps) {
+  if (warp == producer_warp) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       int issued = 0;
@@ -378,186 +402,193 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const Params p) {
       }
     }
     __syncwarp();
-    if (split > 1) {
-      cluster_sync();  // partial sums complete in every CTA of the cluster
-      cluster_sync();  // every CTA has finished reading its peers' partial sums
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers --
-  const int g = warp / p.wpg;
-  const int wg = warp % p.wpg;
-  const int seg = wg * 32 + lane;
-  const int kl = seg * KPL;                           // offset inside the CTA's K range
-  const bool active = kl < k_len;
-  const int bl = (k_begin + kl) / kBlock;             // global 32-block index of the segment
-  const int zshift = (bl & 1) * 4;
-
-  // Activations for this lane's k values, paired to match the nibble order
-  // produced by the dequant below: word i holds k = 8i..8i+7 of the segment
-  // and pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7).
-  uint32_t xr[M][kWords][4];
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-#pragma unroll
-    for (int i = 0; i < kWords; ++i) {
-      uint16_t h[8];
-      if (active) {
-        const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + k_begin + kl + 8 * i;
-        if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
-          h[0] = v.x & 0xFFFF; h[1] = v.x >> 16; h[2] = v.y & 0xFFFF; h[3] = v.y >> 16;
-          h[4] = v.z & 0xFFFF; h[5] = v.z >> 16; h[6] = v.w & 0xFFFF; h[7] = v.w >> 16;
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) h[j] = __ldg(src + j);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) h[j] = 0;
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        xr[m][i][j] = static_cast<uint32_t>(h[j]) | (static_cast<uint32_t>(h[j + 4]) << 16);
-    }
-  }
-
-  const uintptr_t sc_mis = reinterpret_cast<uintptr_t>(p.scales) & 15u;
-  const uintptr_t zp_mis = reinterpret_cast<uintptr_t>(p.zp) & 15u;
-  int t = 0;  // this group's local tile counter
-  bool ok = true;
-  for (int i = g; i < ntiles && ok; i += p.groups, ++t) {
-    const int s = i % p.stages;
-    if (!mbar_wait(full0 + 8u * s, (i / p.stages) & 1, abort_flag, kErrStageData)) {
-      ok = false;
-      break;
-    }
-    const int r0 = row_begin + i * RC;
-    const int nr = min(RC, row_end - r0);
-    const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-    // Misalignment offsets chosen by the producer's region copies.
-    const uint32_t sc_off =
-        static_cast<uint32_t>((sc_mis + static_cast<uintptr_t>(r0) * p.C * 2) & 15u);
-    const uint32_t zp_off = static_cast<uint32_t>((zp_mis + static_cast<uintptr_t>(r0) * p.Z) & 15u);
-    const uint16_t* st_sc = reinterpret_cast<const uint16_t*>(st + p.q_bytes + sc_off);
-    const unsigned char* st_zp = st + p.q_bytes + p.sc_bytes + zp_off;
-
-    uint32_t qw[RC][kWords];
-    uint32_t zb[RC];
-    uint16_t sb[RC];
-#pragma unroll
-    for (int r = 0; r < RC; ++r) {
-      if (active && r < nr) {
-        const unsigned char* qrow = st + static_cast<size_t>(r) * p.q_pitch + kl / 2;
-        if constexpr (kWords == 4) {
-          const uint4 v = *reinterpret_cast<const uint4*>(qrow);
-          qw[r][0] = v.x; qw[r][1] = v.y; qw[r][2] = v.z; qw[r][3] = v.w;
-        } else {
-          const uint2 v = *reinterpret_cast<const uint2*>(qrow);
-          qw[r][0] = v.x; qw[r][1] = v.y;
-        }
-        sb[r] = st_sc[r * p.C + bl];
-        zb[r] = st_zp[r * p.Z + (bl >> 1)];
-      } else {
-#pragma unroll
-        for (int w = 0; w < kWords; ++w) qw[r][w] = 0;
-        sb[r] = 0;
-        zb[r] = 0;
-      }
-    }
-    // The stage's bytes are in registers: hand it back to the producer.
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8u * s);
-
-    float v[kVP];
-#pragma unroll
-    for (int j = 0; j < kVP; ++j) v[j] = 0.f;
-#pragma unroll
-    for (int r = 0; r < RC; ++r) {
-      const uint32_t z = (zb[r] >> zshift) & 0xFu;
-      const uint32_t zl = (z * 0x00010001u) | 0x64006400u;          // 1024 + zp, twice
-      const uint32_t zh = ((z << 4) * 0x00010001u) | 0x54005400u;   // 64 + zp, twice
-      float acc[M];
-#pragma unroll
-      for (int m = 0; m < M; ++m) acc[m] = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWords; ++w) {
-        const uint32_t word = qw[r][w];
-        const uint32_t w8 = word >> 8;
-        const uint32_t d0 = hsub2((word & 0x000F000Fu) | 0x64006400u, zl);   // k0, k4
-        const uint32_t d1 = hsub2((word & 0x00F000F0u) | 0x54005400u, zh);   // k1, k5
-        const uint32_t d2 = hsub2((w8 & 0x000F000Fu) | 0x64006400u, zl);     // k2, k6
-        const uint32_t d3 = hsub2((w8 & 0x00F000F0u) | 0x54005400u, zh);     // k3, k7
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-          acc[m] = fma2_f16_f32(xr[m][w][0], d0, acc[m]);
-          acc[m] = fma2_f16_f32(xr[m][w][1], d1, acc[m]);
-          acc[m] = fma2_f16_f32(xr[m][w][2], d2, acc[m]);
-          acc[m] = fma2_f16_f32(xr[m][w][3], d3, acc[m]);
-        }
-      }
-      const float scale = __half2float(__ushort_as_half(sb[r]));
-#pragma unroll
-      for (int m = 0; m < M; ++m) v[r * M + m] = acc[m] * scale;
-    }
-
-    const float total = transpose_reduce<kVP>(v, lane);
-    const int idx = lane >> kOwnerShift;              // (row, m) value this lane now holds
-    const bool owner = (lane & ((1 << kOwnerShift) - 1)) == 0 && idx < kVals;
-
-    if (p.wpg == 1) {
-      if (owner) {
-        const int r = idx / M, m = idx % M;
-        if (r < nr) {
-          if (split == 1)
-            store_output(p.y, static_cast<size_t>(m) * p.N + r0 + r, total, p.out_bf16);
-          else
-            part[(r0 - row_begin + r) * M + m] = total;
-        }
-      }
-      continue;
-    }
-
-    // Cross-warp (K-slice) reduction through a double-buffered slot.
-    const int buf = t & 1;
-    const uint32_t rfull = rfull0 + 16u * g + 8u * buf;
-    const uint32_t rfree = rfree0 + 16u * g + 8u * buf;
-    float* slot = red + ((static_cast<size_t>(g) * 2 + buf) * p.wpg) * kVP;
-    if (t >= 2 && !mbar_wait(rfree, ((t >> 1) - 1) & 1, abort_flag, kErrReduceSlot)) {
-      ok = false;
-      break;
-    }
-    if (owner) slot[wg * kVP + idx] = total;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(rfull);
-    if (wg == 0) {
-      if (!mbar_wait(rfull, (t >> 1) & 1, abort_flag, kErrReduceSlot)) {
-        ok = false;
-        break;
-      }
-      if (lane < kVals) {
+  } else if (warp == epilogue_warp) {
+    // ------------------------------------------------------------ epilogue --
+    // Adds the K-slice partial sums of every row in slice order, rounds and
+    // stores (or keeps them for the cluster reduction), then frees the slot.
+    for (int i = 0; i < ntiles; ++i) {
+      const int g = i % p.groups, t = i / p.groups;
+      const int j = g * kSlotsPerGroup + t % kSlotsPerGroup;
+      if (!mbar_wait(ready0 + 8u * j, (t / kSlotsPerGroup) & 1, abort_flag, kErrReduceSlot)) break;
+      const int r0 = row_begin + i * RC;
+      const int vals = min(RC, row_end - r0) * M;
+      const float* slot = red + static_cast<size_t>(j) * p.wpg * kVals;
+      if (lane < vals) {
         float sum = 0.f;
-        for (int w = 0; w < p.wpg; ++w) sum += slot[w * kVP + lane];
+        for (int w = 0; w < p.wpg; ++w) sum += slot[w * kVals + lane];
         const int r = lane / M, m = lane % M;
-        if (r < nr) {
-          if (split == 1)
-            store_output(p.y, static_cast<size_t>(m) * p.N + r0 + r, sum, p.out_bf16);
-          else
-            part[(r0 - row_begin + r) * M + m] = sum;
-        }
+        if (split == 1)
+          store_output(p.y, static_cast<size_t>(m) * p.N + r0 + r, sum, p.out_bf16);
+        else
+          part[(r0 - row_begin + r) * M + m] = sum;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(rfree);
+      if (lane == 0) mbar_arrive(free0 + 8u * j);
+    }
+  } else {
+    // ----------------------------------------------------------- consumers --
+    const int g = warp / p.wpg;
+    const int wg = warp % p.wpg;
+    const int seg = wg * 32 + lane;
+    const int kl = seg * KPL;                           // offset inside the CTA's K range
+    const bool active = kl < k_len;
+    // Inactive lanes (past the end of the K range) alias the range's first
+    // segment so every shared-memory read stays inside the stage; their
+    // activations are zero, so they contribute exact zeros.
+    const int klc = active ? kl : 0;
+    const int bl = (k_begin + klc) / kBlock;            // global 32-block index
+    const int zshift = (bl & 1) * 4;
+
+    // Activations for this lane's k values, paired to match the nibble order
+    // produced by the dequant below: word i holds k = 8i..8i+7 of the segment
+    // and pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7).
+    uint32_t xr[M][kWords][4];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+#pragma unroll
+      for (int i = 0; i < kWords; ++i) {
+        uint16_t h[8];
+        if (active) {
+          const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + k_begin + kl + 8 * i;
+          if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+            h[0] = v.x & 0xFFFF; h[1] = v.x >> 16; h[2] = v.y & 0xFFFF; h[3] = v.y >> 16;
+            h[4] = v.z & 0xFFFF; h[5] = v.z >> 16; h[6] = v.w & 0xFFFF; h[7] = v.w >> 16;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) h[j] = __ldg(src + j);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) h[j] = 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          xr[m][i][j] = static_cast<uint32_t>(h[j]) | (static_cast<uint32_t>(h[j + 4]) << 16);
+      }
+    }
+
+    const uintptr_t sc_mis = reinterpret_cast<uintptr_t>(p.scales) & 15u;
+    const uintptr_t zp_mis = reinterpret_cast<uintptr_t>(p.zp) & 15u;
+    const int q_pitch = p.q_pitch, C = p.C, Z = p.Z;
+    int t = 0;                                          // this group's tile counter
+    for (int i = g; i < ntiles; i += p.groups, ++t) {
+      const int s = i % p.stages;
+      if (!mbar_wait(full0 + 8u * s, (i / p.stages) & 1, abort_flag, kErrStageData)) break;
+      const int r0 = row_begin + i * RC;
+      const int nr = min(RC, row_end - r0);
+      const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+      // Misalignment offsets chosen by the producer's region copies.
+      const uint32_t sc_off =
+          static_cast<uint32_t>((sc_mis + static_cast<uintptr_t>(r0) * C * 2) & 15u);
+      const uint32_t zp_off = static_cast<uint32_t>((zp_mis + static_cast<uintptr_t>(r0) * Z) & 15u);
+      const unsigned char* qp = st + klc / 2;
+      const uint16_t* sp = reinterpret_cast<const uint16_t*>(st + p.q_bytes + sc_off) + bl;
+      const unsigned char* zpp = st + p.q_bytes + p.sc_bytes + zp_off + (bl >> 1);
+
+      // Pull this lane's codes, zero-point bytes and scales of every row into
+      // registers and give the stage straight back to the producer.  Rows past
+      // the end of a ragged tile re-read its last row; they are never stored.
+      uint32_t words[RC][kWords];
+      uint32_t zbyte[RC];
+      uint32_t sbits[RC];
+#pragma unroll
+      for (int r = 0; r < RC; ++r) {
+        const int rr = (nr == RC) ? r : min(r, nr - 1);
+        const unsigned char* qrow = qp + rr * q_pitch;
+        if constexpr (kWords == 2) {
+          const uint2 a = *reinterpret_cast<const uint2*>(qrow);
+          words[r][0] = a.x; words[r][1] = a.y;
+        } else {
+#pragma unroll
+          for (int h = 0; h < kWords / 4; ++h) {
+            const uint4 a = *reinterpret_cast<const uint4*>(qrow + 16 * h);
+            words[r][4 * h] = a.x; words[r][4 * h + 1] = a.y;
+            words[r][4 * h + 2] = a.z; words[r][4 * h + 3] = a.w;
+          }
+        }
+        zbyte[r] = zpp[rr * Z];
+        if constexpr (kLaneBlocks == 2)
+          sbits[r] = *reinterpret_cast<const uint32_t*>(sp + rr * C);
+        else
+          sbits[r] = sp[rr * C];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8u * s);
+
+      float v[kVP];
+#pragma unroll
+      for (int j = 0; j < kVP; ++j) v[j] = 0.f;
+#pragma unroll
+      for (int r = 0; r < RC; ++r) {
+        uint32_t zl[kLaneBlocks], zh[kLaneBlocks];
+        float scale[kLaneBlocks];
+        if constexpr (kLaneBlocks == 2) {
+          // Blocks bl (even, low nibble) and bl + 1 (high nibble) share one byte.
+          const uint32_t tz = zbyte[r] * 0x00010001u;
+          zl[0] = and_or(tz, 0x000F000Fu, 0x64006400u);         // 1024 + zp, twice
+          zh[0] = and_or(tz << 4, 0x00F000F0u, 0x54005400u);    //   64 + zp, twice
+          zl[1] = and_or(tz >> 4, 0x000F000Fu, 0x64006400u);
+          zh[1] = and_or(tz, 0x00F000F0u, 0x54005400u);
+          scale[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sbits[r] & 0xFFFFu)));
+          scale[1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sbits[r] >> 16)));
+        } else {
+          const uint32_t tz = zbyte[r] >> zshift;
+          zl[0] = and_or(tz * 0x00010001u, 0x000F000Fu, 0x64006400u);
+          zh[0] = and_or(tz * 0x00100010u, 0x00F000F0u, 0x54005400u);
+          scale[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sbits[r])));
+        }
+        float res[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) res[m] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kLaneBlocks; ++j) {
+          float acc[M];
+#pragma unroll
+          for (int m = 0; m < M; ++m) acc[m] = 0.f;
+#pragma unroll
+          for (int w = j * kBlockWords; w < (j + 1) * kBlockWords; ++w) {
+            const uint32_t word = words[r][w];
+            const uint32_t w8 = word >> 8;
+            const uint32_t d0 = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl[j]);   // k0, k4
+            const uint32_t d1 = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh[j]);   // k1, k5
+            const uint32_t d2 = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl[j]);     // k2, k6
+            const uint32_t d3 = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh[j]);     // k3, k7
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+              acc[m] = fma2_f16_f32(xr[m][w][0], d0, acc[m]);
+              acc[m] = fma2_f16_f32(xr[m][w][1], d1, acc[m]);
+              acc[m] = fma2_f16_f32(xr[m][w][2], d2, acc[m]);
+              acc[m] = fma2_f16_f32(xr[m][w][3], d3, acc[m]);
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < M; ++m) res[m] = fmaf(acc[m], scale[j], res[m]);
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) v[r * M + m] = res[m];
+      }
+
+      // Warp sum of every (row, m) value; the owning lane files it in this K
+      // slice's part of a reduction slot, which the epilogue warp finishes.
+      const float total = transpose_reduce<kVP>(v, lane);
+      const int idx = lane >> kOwnerShift;
+      const int j = g * kSlotsPerGroup + t % kSlotsPerGroup;
+      if (t >= kSlotsPerGroup &&
+          !mbar_wait(free0 + 8u * j, ((t / kSlotsPerGroup) - 1) & 1, abort_flag, kErrReduceSlot))
+        break;
+      if ((lane & ((1 << kOwnerShift) - 1)) == 0 && idx < kVals)
+        red[(static_cast<size_t>(j) * p.wpg + wg) * kVals + idx] = total;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ready0 + 8u * j);
     }
   }
 
   if (split > 1) {
     cluster_sync();  // every CTA of the cluster has written its partial sums
     // Rank r finalises rows r, r + split, ...; peers are added in rank order.
-    const int consumers = consumer_warps * 32;
     const uint32_t part_addr = smem_u32(part);
-    for (int e = threadIdx.x; e < nrows * M; e += consumers) {
+    for (int e = threadIdx.x; e < nrows * M; e += blockDim.x) {
       const int r = e / M;
       if (r % split != static_cast<int>(rank)) continue;
       float sum = 0.f;
@@ -590,7 +621,11 @@ constexpr KernelFn kernel_for() {
   return &gemv_kernel<M, shape_for(M).kpl, shape_for(M).rc>;
 }
 
-KernelFn pick_kernel(int M) {
+// Codes per lane segment (the per-M default; the kernel also supports 64-code
+// segments, two blocks per lane, which measured slower on these shapes).
+int pick_kpl(int M, int, int, const void*) { return shape_for(M).kpl; }
+
+KernelFn pick_kernel(int M, int) {
   switch (M) {
     case 1: return kernel_for<1>();
     case 2: return kernel_for<2>();
@@ -603,7 +638,7 @@ KernelFn pick_kernel(int M) {
   }
 }
 
-int max_k_per_cta(int M) { return kMaxWarpsPerGroup * 32 * shape_for(M).kpl; }
+int max_k_per_cta(int M) { return consumer_warp_budget(M) * 32 * shape_for(M).kpl; }
 
 thread_local std::string t_detail;
 
@@ -690,8 +725,8 @@ struct Plan {
   size_t smem;
 };
 
-int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, Plan* plan) {
-  const KernelShape ks = shape_for(M);
+int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, int kpl, Plan* plan) {
+  const KernelShape ks{kpl, shape_for(M).rc};
   Params& p = plan->p;
   p.M = M;
   p.N = N;
@@ -699,17 +734,14 @@ int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, Plan* plan)
   p.C = K / kBlock;
   p.Z = (p.C + 1) / 2;
   p.split = split;
-  const int blocks_cta = (p.C + split - 1) / split;     // largest K range of a rank, in blocks
+  const int lane_blocks = ks.kpl >= 32 ? ks.kpl / 32 : 1;
+  const int seg_units = p.C / lane_blocks;
+  const int blocks_cta = lane_blocks * ((seg_units + split - 1) / split);   // largest rank K range
   const int k_cta = blocks_cta * kBlock;
   const int segs = k_cta / ks.kpl;
-  p.wpg = (segs + 31) / 32;
-  p.groups = std::max(1, std::min(4, kMaxWarpsPerGroup / p.wpg));
+  p.wpg = (segs + 31) / 32;                            // <= consumer_warp_budget(M) by check_shape
+  p.groups = std::max(1, std::min(4, consumer_warp_budget(M) / p.wpg));
   p.q_pitch = k_cta / 2;
-  p.q_bytes = ks.rc * p.q_pitch;
-  p.sc_bytes = (ks.rc * p.C * 2 + 16 + 15) & ~15;
-  p.zp_bytes = (ks.rc * p.Z + 16 + 15) & ~15;
-  p.stage_bytes = p.q_bytes + p.sc_bytes + p.zp_bytes;
-
   // Grid: one CTA per SM; with split > 1 the units are clusters, and enough
   // of them that each cluster's partial sums fit in shared memory.
   const long long tiles = (static_cast<long long>(N) + ks.rc - 1) / ks.rc;
@@ -723,29 +755,32 @@ int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, Plan* plan)
   const long long rows_per_unit = (N + units - 1) / units;
   const int part_bytes = split > 1 ? static_cast<int>(((rows_per_unit * M * 4) + 15) & ~15LL) : 0;
 
-  const int kvals = ks.rc * M;
-  int vp = 1;
-  while (vp < kvals) vp *= 2;
-  const int red_bytes = p.wpg > 1 ? p.groups * 2 * p.wpg * vp * 4 : 0;
-  const int bar_bytes = 8 * (2 * kMaxStages + 4 * p.groups);
-  const int fixed = bar_bytes + red_bytes + part_bytes + 16;
+  // Shared memory: a ring of stages (codes, scales and zero-points of RC rows),
+  // the groups' reduction slots, and the mbarriers.
+  p.rows_stage = ks.rc;
+  p.q_bytes = ks.rc * p.q_pitch;
+  p.sc_bytes = (ks.rc * p.C * 2 + 16 + 15) & ~15;
+  p.zp_bytes = (ks.rc * p.Z + 16 + 15) & ~15;
+  p.stage_bytes = p.q_bytes + p.sc_bytes + p.zp_bytes;
+  const int nslots = p.groups * kSlotsPerGroup;
+  const int red_bytes = ((nslots * p.wpg * ks.rc * M * 4) + 15) & ~15;
+  const int fixed = red_bytes + 8 * 2 * nslots + part_bytes + 16;
   const int budget = std::min<int>(kSmemBudget, static_cast<int>(dev.smem_optin)) - fixed;
-  int stages = budget / p.stage_bytes;
-  stages = std::min(stages, kMaxStages);
+  const int stages = std::min(budget / (p.stage_bytes + 16), kMaxStages);
   if (stages < 2) return fail(MNB_ERR_SHAPE, "shape needs more shared memory than one SM has");
   p.stages = stages;
   int off = stages * p.stage_bytes;
-  p.bar_offset = off;
-  off += 8 * (2 * stages + 4 * p.groups);
   p.red_offset = off;
   off += red_bytes;
+  p.bar_offset = off;
+  off += 8 * (2 * stages + 2 * nslots);
   p.part_offset = off;
   off += part_bytes;
   p.flag_offset = off;
   off += 16;
   plan->smem = static_cast<size_t>(off);
   plan->grid = dim3(static_cast<unsigned>(units * split));
-  plan->block = dim3(static_cast<unsigned>((p.groups * p.wpg + 1) * 32));
+  plan->block = dim3(static_cast<unsigned>((p.groups * p.wpg + 2) * 32));
   return MNB_OK;
 }
 
@@ -834,8 +869,9 @@ int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const ui
   if ((st = device_info(&dev)) != MNB_OK) return st;
   const int split = split_k == 0 ? auto_split(M, N, K, dev.sms) : split_k;
 
+  const int kpl = pick_kpl(M, K / kBlock, split, scales);
   Plan plan;
-  if ((st = make_plan(dev, M, N, K, split, &plan)) != MNB_OK) return st;
+  if ((st = make_plan(dev, M, N, K, split, kpl, &plan)) != MNB_OK) return st;
   Params& p = plan.p;
   p.x = static_cast<const uint16_t*>(x);
   p.q = qweight;
@@ -844,7 +880,7 @@ int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const ui
   p.y = y;
   p.out_bf16 = out_dtype == MNB_OUT_BF16;
 
-  KernelFn fn = pick_kernel(M);
+  KernelFn fn = pick_kernel(M, kpl);
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.smem));

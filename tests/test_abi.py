@@ -74,7 +74,8 @@ def test_split_limits(lib):
     assert lib.mnb_max_split_k(4096, ctypes.byref(out)) == 0 and out.value == 8
     assert lib.mnb_max_split_k(64, ctypes.byref(out)) == 0 and out.value == 2
     assert lib.mnb_min_split_k(8, 16384, ctypes.byref(out)) == 0 and out.value == 2
-    assert lib.mnb_min_split_k(1, 16384, ctypes.byref(out)) == 0 and out.value == 1
+    assert lib.mnb_min_split_k(1, 12288, ctypes.byref(out)) == 0 and out.value == 1
+    assert lib.mnb_min_split_k(1, 16384, ctypes.byref(out)) == 0 and out.value == 2
     assert lib.mnb_min_split_k(9, 4096, ctypes.byref(out)) == 2
     assert lib.mnb_max_split_k(4096, None) == 1
 

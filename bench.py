@@ -86,15 +86,18 @@ def kernel_source_hash():
 def recorded_traffic(workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "gemv_dram_traffic.json")
+    path = os.path.join(ROOT, "profiles", "gemv_dram_traffic.txt")
     try:
         with open(path) as f:
-            d = json.load(f)
-    except (OSError, ValueError):
+            entries = dict(line.split("=", 1) for line in f
+                           if "=" in line and not line.lstrip().startswith("#"))
+    except OSError:
         return None
-    if d.get("kernel_source_sha256") != kernel_source_hash():
+    entries = {k.strip(): v.strip() for k, v in entries.items()}
+    if entries.get("kernel_source_sha256") != kernel_source_hash():
         return None
-    return d.get("bytes_per_launch", {}).get(workload)
+    v = entries.get(workload)
+    return int(v) if v else None
 
 
 class ClockSampler:

@@ -67,6 +67,7 @@ constexpr int kSmemBudget = 200 * 1024;           // stages + bookkeeping
 constexpr int kPartBudget = 32 * 1024;            // cluster partial sums per CTA
 constexpr int kMaxStages = 16;
 constexpr int kSlotsPerGroup = 4;               // reduction slots a group may have pending
+constexpr int kStageCodeBytes = 32 * 1024;        // target size of a stage's code area
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 enum : unsigned {
@@ -307,8 +308,9 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
 
   // mbarriers:
   //   full[s]   (stage)  1 arrival + transaction bytes: the stage's data landed
-  //   empty[s]  (stage)  wpg arrivals: the group's K-slice warps hold the data
-  //                      in registers, the stage may be refilled
+  //   empty[s]  (stage)  wpg arrivals per tile of the stage: once every tile's
+  //                      K-slice warps hold their data in registers the stage
+  //                      may be refilled
   //   ready[j]  (slot)   wpg arrivals: every K-slice warp filed its partial sums
   //   free[j]   (slot)   1 arrival: the epilogue has consumed the slot
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_offset);
@@ -328,7 +330,10 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
   const int row_begin = static_cast<int>((static_cast<long long>(unit) * p.N) / units);
   const int row_end = static_cast<int>((static_cast<long long>(unit + 1) * p.N) / units);
   const int nrows = row_end - row_begin;
-  const int ntiles = (nrows + RC - 1) / RC;         // one stage holds RC rows
+  const int ntiles = (nrows + RC - 1) / RC;         // tiles of RC rows (one group each)
+  const int RS = p.rows_stage;                      // a stage holds RS / RC whole tiles
+  const int TPS = RS / RC;
+  const int nstages = (nrows + RS - 1) / RS;        // stage loads this CTA makes
   // K ranges are whole multiples of the lane segment's blocks (2 when KPL = 64).
   const int seg_units = p.C / kLaneBlocks;
   const int b_begin = kLaneBlocks * static_cast<int>((static_cast<long long>(rank) * seg_units) / split);
@@ -339,7 +344,7 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, p.wpg);
+      mbar_init(empty0 + 8u * s, p.wpg * TPS);
     }
     for (int j = 0; j < nslots; ++j) {
       mbar_init(ready0 + 8u * j, p.wpg);
@@ -354,13 +359,13 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       int issued = 0;
-      for (int i = 0; i < ntiles; ++i) {
-        const int s = i % p.stages;
-        if (i >= p.stages &&
-            !mbar_wait(empty0 + 8u * s, ((i / p.stages) - 1) & 1, abort_flag, kErrStageFree))
+      int s = 0;                                        // stage slot of load i
+      uint32_t ph = 0;                                  // completed uses of slot s, mod 2
+      for (int i = 0; i < nstages; ++i) {
+        if (i >= p.stages && !mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, kErrStageFree))
           break;
-        const int r0 = row_begin + i * RC;
-        const int nr = min(RC, row_end - r0);
+        const int r0 = row_begin + i * RS;
+        const int nr = min(RS, row_end - r0);
         unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
         const uint32_t bar = full0 + 8u * s;
         // Scales and zero-points of these rows are contiguous in global memory.
@@ -386,6 +391,10 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
         if (sc.body) bulk_copy_g2s(sc.dst, sc.src, sc.body, bar);
         if (zc.body) bulk_copy_g2s(zc.dst, zc.src, zc.body, bar);
         issued = i + 1;
+        if (++s == p.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       // Let every copy this thread issued land before the CTA may exit.
       for (int i = max(0, issued - p.stages); i < issued; ++i) {
@@ -406,8 +415,8 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
     // ------------------------------------------------------------ epilogue --
     // Adds the K-slice partial sums of every row in slice order, rounds and
     // stores (or keeps them for the cluster reduction), then frees the slot.
+    int g = 0, t = 0;                                   // tile i belongs to group g, its t-th
     for (int i = 0; i < ntiles; ++i) {
-      const int g = i % p.groups, t = i / p.groups;
       const int j = g * kSlotsPerGroup + t % kSlotsPerGroup;
       if (!mbar_wait(ready0 + 8u * j, (t / kSlotsPerGroup) & 1, abort_flag, kErrReduceSlot)) break;
       const int r0 = row_begin + i * RC;
@@ -424,6 +433,10 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(free0 + 8u * j);
+      if (++g == p.groups) {
+        g = 0;
+        ++t;
+      }
     }
   } else {
     // ----------------------------------------------------------- consumers --
@@ -471,20 +484,28 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
     const uintptr_t sc_mis = reinterpret_cast<uintptr_t>(p.scales) & 15u;
     const uintptr_t zp_mis = reinterpret_cast<uintptr_t>(p.zp) & 15u;
     const int q_pitch = p.q_pitch, C = p.C, Z = p.Z;
+    // Tile i sits in stage load si = i / TPS at row ti * RC; the load uses
+    // slot s = si % stages for the ph-th time (mod 2).  Kept incrementally:
+    // no division in the loop.
+    int si = g / TPS;
+    int ti = g - si * TPS;
+    int s = si % p.stages;
+    uint32_t ph = static_cast<uint32_t>(si / p.stages) & 1u;
     int t = 0;                                          // this group's tile counter
-    for (int i = g; i < ntiles; i += p.groups, ++t) {
-      const int s = i % p.stages;
-      if (!mbar_wait(full0 + 8u * s, (i / p.stages) & 1, abort_flag, kErrStageData)) break;
+    for (int i = g; i < ntiles; ++t) {
+      if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) break;
       const int r0 = row_begin + i * RC;
       const int nr = min(RC, row_end - r0);
+      const int rin = ti * RC;                          // tile's first row inside the stage
+      const int rs0 = r0 - rin;                         // first row of the stage
       const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
       // Misalignment offsets chosen by the producer's region copies.
       const uint32_t sc_off =
-          static_cast<uint32_t>((sc_mis + static_cast<uintptr_t>(r0) * C * 2) & 15u);
-      const uint32_t zp_off = static_cast<uint32_t>((zp_mis + static_cast<uintptr_t>(r0) * Z) & 15u);
-      const unsigned char* qp = st + klc / 2;
-      const uint16_t* sp = reinterpret_cast<const uint16_t*>(st + p.q_bytes + sc_off) + bl;
-      const unsigned char* zpp = st + p.q_bytes + p.sc_bytes + zp_off + (bl >> 1);
+          static_cast<uint32_t>((sc_mis + static_cast<uintptr_t>(rs0) * C * 2) & 15u);
+      const uint32_t zp_off = static_cast<uint32_t>((zp_mis + static_cast<uintptr_t>(rs0) * Z) & 15u);
+      const unsigned char* qp = st + rin * q_pitch + klc / 2;
+      const uint16_t* sp = reinterpret_cast<const uint16_t*>(st + p.q_bytes + sc_off) + rin * C + bl;
+      const unsigned char* zpp = st + p.q_bytes + p.sc_bytes + zp_off + rin * Z + (bl >> 1);
 
       // Pull this lane's codes, zero-point bytes and scales of every row into
       // registers and give the stage straight back to the producer.  Rows past
@@ -581,6 +602,13 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
         red[(static_cast<size_t>(j) * p.wpg + wg) * kVals + idx] = total;
       __syncwarp();
       if (lane == 0) mbar_arrive(ready0 + 8u * j);
+      i += p.groups;
+      for (ti += p.groups; ti >= TPS; ti -= TPS) {
+        if (++s == p.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
     }
   }
 
@@ -621,11 +649,12 @@ constexpr KernelFn kernel_for() {
   return &gemv_kernel<M, shape_for(M).kpl, shape_for(M).rc>;
 }
 
-// Codes per lane segment (the per-M default; the kernel also supports 64-code
-// segments, two blocks per lane, which measured slower on these shapes).
-int pick_kpl(int M, int, int, const void*) { return shape_for(M).kpl; }
+// Lane segment and rows per tile: the per-M default.  (The kernel template
+// also supports 64-code segments, two blocks per lane; on GB300 they measured
+// slower than 32-code segments for M = 1, so they are not instantiated.)
+KernelShape pick_shape(int M, int, int, const void*) { return shape_for(M); }
 
-KernelFn pick_kernel(int M, int) {
+KernelFn pick_kernel(int M, const KernelShape&) {
   switch (M) {
     case 1: return kernel_for<1>();
     case 2: return kernel_for<2>();
@@ -725,8 +754,8 @@ struct Plan {
   size_t smem;
 };
 
-int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, int kpl, Plan* plan) {
-  const KernelShape ks{kpl, shape_for(M).rc};
+int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, const KernelShape& ks,
+              Plan* plan) {
   Params& p = plan->p;
   p.M = M;
   p.N = N;
@@ -757,10 +786,14 @@ int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, int kpl, Pl
 
   // Shared memory: a ring of stages (codes, scales and zero-points of RC rows),
   // the groups' reduction slots, and the mbarriers.
-  p.rows_stage = ks.rc;
-  p.q_bytes = ks.rc * p.q_pitch;
-  p.sc_bytes = (ks.rc * p.C * 2 + 16 + 15) & ~15;
-  p.zp_bytes = (ks.rc * p.Z + 16 + 15) & ~15;
+  // A stage holds whole tiles of ks.rc rows, about kStageCodeBytes of codes
+  // (large bulk copies stream best), never more rows than the CTA owns.
+  const int unit_tiles = static_cast<int>((rows_per_unit + ks.rc - 1) / ks.rc);
+  const int tps = std::max(1, std::min(unit_tiles, kStageCodeBytes / (ks.rc * p.q_pitch)));
+  p.rows_stage = ks.rc * tps;
+  p.q_bytes = p.rows_stage * p.q_pitch;
+  p.sc_bytes = (p.rows_stage * p.C * 2 + 16 + 15) & ~15;
+  p.zp_bytes = (p.rows_stage * p.Z + 16 + 15) & ~15;
   p.stage_bytes = p.q_bytes + p.sc_bytes + p.zp_bytes;
   const int nslots = p.groups * kSlotsPerGroup;
   const int red_bytes = ((nslots * p.wpg * ks.rc * M * 4) + 15) & ~15;
@@ -869,9 +902,9 @@ int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const ui
   if ((st = device_info(&dev)) != MNB_OK) return st;
   const int split = split_k == 0 ? auto_split(M, N, K, dev.sms) : split_k;
 
-  const int kpl = pick_kpl(M, K / kBlock, split, scales);
+  const KernelShape ks = pick_shape(M, K / kBlock, split, scales);
   Plan plan;
-  if ((st = make_plan(dev, M, N, K, split, kpl, &plan)) != MNB_OK) return st;
+  if ((st = make_plan(dev, M, N, K, split, ks, &plan)) != MNB_OK) return st;
   Params& p = plan.p;
   p.x = static_cast<const uint16_t*>(x);
   p.q = qweight;
@@ -880,7 +913,7 @@ int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const ui
   p.y = y;
   p.out_bf16 = out_dtype == MNB_OUT_BF16;
 
-  KernelFn fn = pick_kernel(M, kpl);
+  KernelFn fn = pick_kernel(M, ks);
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.smem));

@@ -281,7 +281,8 @@ def main():
         # one step: every output dtype of the workload, each on its own weight copy
         for i, o in enumerate(outs):
             q, s, z = copies[(j * L + i) % R]
-            mnb.gemv(x, q, s, z, out_dtype=o, split_k=split_k, y=ys[o], stream=stream)
+            mnb.gemv(x, q, s, z, out_dtype=o, split_k=split_k, y=ys[o], stream=stream,
+                     weights_ready=True)
 
     # Warm-up: W eager steps.
     with torch.cuda.stream(stream):

@@ -60,7 +60,8 @@ typedef enum mnb_status {
     MNB_ERR_ALIGN = 6,   /* a pointer is misaligned for its element type (see mnb_gemv) */
     MNB_ERR_ALIAS = 7,   /* y overlaps an input array */
     MNB_ERR_CUDA = 8,    /* a CUDA runtime call failed; see mnb_last_error_detail */
-    MNB_ERR_DEVICE = 9   /* the current device is not an sm_103 GPU */
+    MNB_ERR_DEVICE = 9,  /* the current device is not an sm_103 GPU */
+    MNB_ERR_FLAGS = 10   /* unknown bits in the flags of mnb_gemv_flags */
 } mnb_status;
 
 /* Limits of mnb_gemv. */
@@ -106,12 +107,36 @@ int mnb_gemv(const void *x, const uint8_t *qweight, const void *scales, const ui
              void *y, int M, int N, int K, int block, int out_dtype, int split_k,
              void *stream);
 
+/*
+ * Flags of mnb_gemv_flags.
+ *
+ * Every GEMV launch lets the next kernel on its stream launch early
+ * (programmatic dependent launch) and, before it reads or writes any caller
+ * array, waits until the kernel launched before it on the stream has completed
+ * and its writes are visible.  So back-to-back calls overlap launch latency
+ * and drain time while keeping stream order for every array.
+ *
+ * MNB_FLAG_WEIGHTS_READY: the caller promises that qweight, scales and zp are
+ * not written by the kernel launched just before this call on the stream (they
+ * are static model weights).  The call then starts streaming them before that
+ * kernel completes; x is still read, and y written, only after it completes.
+ */
+#define MNB_FLAG_WEIGHTS_READY 1u
+
+/* mnb_gemv with flags (0 or MNB_FLAG_WEIGHTS_READY); mnb_gemv(...) is
+ * mnb_gemv_flags(..., 0, stream).  Same arguments, checks and statuses, plus
+ * MNB_ERR_FLAGS for unknown flag bits. */
+int mnb_gemv_flags(const void *x, const uint8_t *qweight, const void *scales, const uint8_t *zp,
+                   void *y, int M, int N, int K, int block, int out_dtype, int split_k,
+                   unsigned int flags, void *stream);
+
 /* split_k that mnb_gemv uses for split_k = 0 on the current device.
  * Writes it to *split_k.  Same shape checks and statuses as mnb_gemv. */
 int mnb_split_k_auto(int M, int N, int K, int *split_k);
 
-/* Smallest split_k mnb_gemv accepts for this M and K (a CTA covers at most
- * 8192 values of K when M >= 4 and 16384 otherwise).  Writes it to *min_split. */
+/* Smallest split_k mnb_gemv accepts for this M and K (one CTA covers at most
+ * 12288 values of K when M <= 2, 16384 when M = 3 and 8192 when M >= 4).
+ * Writes it to *min_split. */
 int mnb_min_split_k(int M, int K, int *min_split);
 
 /* Largest split_k mnb_gemv accepts for this K: min(MNB_MAX_SPLIT_K, K/32). */

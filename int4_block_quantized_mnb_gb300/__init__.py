@@ -10,12 +10,12 @@ from __future__ import annotations
 
 import ctypes
 
-from ._native import (BLOCK, MAX_M, MAX_SPLIT_K, OUT_BF16, OUT_F16, MnbError, check,
-                      load)
+from ._native import (BLOCK, FLAG_WEIGHTS_READY, MAX_M, MAX_SPLIT_K, OUT_BF16, OUT_F16,
+                      MnbError, check, load)
 
 __all__ = ["gemv", "gemv_ptr", "split_k_auto", "min_split_k", "max_split_k", "counters",
            "reset_counters", "device_error", "MnbError", "OUT_F16", "OUT_BF16", "BLOCK",
-           "MAX_M", "MAX_SPLIT_K"]
+           "MAX_M", "MAX_SPLIT_K", "FLAG_WEIGHTS_READY"]
 
 _DTYPES = {"f16": OUT_F16, "float16": OUT_F16, "bf16": OUT_BF16, "bfloat16": OUT_BF16}
 
@@ -35,17 +35,26 @@ def _out_code(out_dtype) -> int:
 
 def gemv_ptr(x: int, qweight: int, scales: int, zp: int, y: int, M: int, N: int, K: int,
              block: int = BLOCK, out_dtype: int = OUT_F16, split_k: int = 0,
-             stream: int = 0) -> None:
+             stream: int = 0, flags: int = 0) -> None:
     """Raw C-ABI call with integer device pointers; raises MnbError on failure."""
-    check(load().mnb_gemv(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, stream))
+    lib = load()
+    if flags:
+        check(lib.mnb_gemv_flags(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k,
+                                 flags, stream))
+    else:
+        check(lib.mnb_gemv(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, stream))
 
 
-def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stream=None):
+def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stream=None,
+         weights_ready: bool = False):
     """y = MatMulNBits(x, qweight, scales, zp) on the current CUDA device.
 
     x [M][K] float16, qweight [N][K/2] uint8, scales [N][K/32] float16,
     zp [N][ceil(K/64)] uint8, all contiguous CUDA tensors.  Returns y [M][N]
-    float16 or bfloat16 (or writes the given ``y``).
+    float16 or bfloat16 (or writes the given ``y``).  ``weights_ready=True``
+    promises that the kernel launched just before on the stream does not
+    write qweight, scales or zp (static weights), so the call may start
+    streaming them before that kernel completes.
     """
     import torch
     code = _out_code(out_dtype)
@@ -72,7 +81,8 @@ def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stre
         stream = torch.cuda.current_stream(x.device)
     with torch.cuda.device(x.device):
         gemv_ptr(x.data_ptr(), qweight.data_ptr(), scales.data_ptr(), zp.data_ptr(),
-                 y.data_ptr(), M, N, K, BLOCK, code, int(split_k), stream.cuda_stream)
+                 y.data_ptr(), M, N, K, BLOCK, code, int(split_k), stream.cuda_stream,
+                 FLAG_WEIGHTS_READY if weights_ready else 0)
     return y
 
 

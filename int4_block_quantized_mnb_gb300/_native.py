@@ -15,7 +15,8 @@ OUT_F16 = 0
 OUT_BF16 = 1
 STATUS = {0: "MNB_OK", 1: "MNB_ERR_NULL", 2: "MNB_ERR_SHAPE", 3: "MNB_ERR_BLOCK",
           4: "MNB_ERR_DTYPE", 5: "MNB_ERR_SPLITK", 6: "MNB_ERR_ALIGN", 7: "MNB_ERR_ALIAS",
-          8: "MNB_ERR_CUDA", 9: "MNB_ERR_DEVICE"}
+          8: "MNB_ERR_CUDA", 9: "MNB_ERR_DEVICE", 10: "MNB_ERR_FLAGS"}
+FLAG_WEIGHTS_READY = 1
 MAX_M = 8
 BLOCK = 32
 MAX_SPLIT_K = 8
@@ -26,6 +27,9 @@ _vp, _u8p, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "mnb_gemv": (ctypes.c_int, [_vp, _u8p, _vp, _u8p, _vp, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp]),
+    "mnb_gemv_flags": (ctypes.c_int, [_vp, _u8p, _vp, _u8p, _vp, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_uint, _vp]),
     "mnb_split_k_auto": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _ip]),
     "mnb_min_split_k": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _ip]),
     "mnb_max_split_k": (ctypes.c_int, [ctypes.c_int, _ip]),

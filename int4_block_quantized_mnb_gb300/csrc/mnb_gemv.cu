@@ -89,6 +89,7 @@ struct Params {
   int C;            // 32-blocks per row
   int Z;            // zero-point bytes per row
   int out_bf16;
+  int weights_ready;  // weights may be read before the preceding grid completes
   int split;        // CTAs per cluster along K
   int groups;       // consumer groups per CTA
   int wpg;          // warps per group
@@ -176,6 +177,15 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Programmatic dependent launch: let the next grid on the stream launch now,
+// and wait until the preceding grid has completed and its writes are visible.
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_prerequisites() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -354,10 +364,15 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  // The next GEMV on the stream may launch while this one runs; every read of
+  // a caller array below waits for the preceding grid first (weights only
+  // when the caller has not promised they are ready).
+  allow_dependents();
 
   if (warp == producer_warp) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
+      if (!p.weights_ready) wait_prerequisites();
       int issued = 0;
       int s = 0;                                        // stage slot of load i
       uint32_t ph = 0;                                  // completed uses of slot s, mod 2
@@ -415,6 +430,7 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
     // ------------------------------------------------------------ epilogue --
     // Adds the K-slice partial sums of every row in slice order, rounds and
     // stores (or keeps them for the cluster reduction), then frees the slot.
+    wait_prerequisites();
     int g = 0, t = 0;                                   // tile i belongs to group g, its t-th
     for (int i = 0; i < ntiles; ++i) {
       const int j = g * kSlotsPerGroup + t % kSlotsPerGroup;
@@ -455,6 +471,7 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
     // Activations for this lane's k values, paired to match the nibble order
     // produced by the dequant below: word i holds k = 8i..8i+7 of the segment
     // and pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7).
+    wait_prerequisites();
     uint32_t xr[M][kWords][4];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
@@ -613,6 +630,7 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
   }
 
   if (split > 1) {
+    wait_prerequisites();
     cluster_sync();  // every CTA of the cluster has written its partial sums
     // Rank r finalises rows r, r + split, ...; peers are added in rank order.
     const uint32_t part_addr = smem_u32(part);
@@ -842,6 +860,7 @@ const char* mnb_status_string(int status) {
     case MNB_ERR_ALIAS: return "output overlaps an input";
     case MNB_ERR_CUDA: return "CUDA runtime error";
     case MNB_ERR_DEVICE: return "unsupported device";
+    case MNB_ERR_FLAGS: return "unknown flag bits";
     default: return "unknown status";
   }
 }
@@ -875,6 +894,14 @@ int mnb_split_k_auto(int M, int N, int K, int* split_k) {
 
 int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp, void* y,
              int M, int N, int K, int block, int out_dtype, int split_k, void* stream) {
+  return mnb_gemv_flags(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, 0u, stream);
+}
+
+int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
+                   void* y, int M, int N, int K, int block, int out_dtype, int split_k,
+                   unsigned int flags, void* stream) {
+  if (flags & ~static_cast<unsigned int>(MNB_FLAG_WEIGHTS_READY))
+    return fail(MNB_ERR_FLAGS, "unknown flag bits");
   if (!x || !qweight || !scales || !zp || !y) return fail(MNB_ERR_NULL, "x, qweight, scales, zp and y are required");
   if (block != kBlock) return fail(MNB_ERR_BLOCK, "only block size 32 is supported");
   int st = check_shape(M, N, K);
@@ -912,6 +939,7 @@ int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const ui
   p.zp = zp;
   p.y = y;
   p.out_bf16 = out_dtype == MNB_OUT_BF16;
+  p.weights_ready = (flags & MNB_FLAG_WEIGHTS_READY) ? 1 : 0;
 
   KernelFn fn = pick_kernel(M, ks);
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
@@ -924,14 +952,17 @@ int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const ui
   cfg.blockDim = plan.block;
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (split > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   e = cudaLaunchKernelEx(&cfg, fn, p);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx");

@@ -38,8 +38,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(10):
-        assert lib.mnb_status_string(s)
+    for s in range(11):
+        assert lib.mnb_status_string(s) != b"unknown status"
     assert lib.mnb_status_string(99) == b"unknown status"
     assert lib.mnb_abi_version() == 1
 
@@ -67,6 +67,13 @@ def call(lib, x=X, q=Q, s=S, z=Z, y=Y, M=1, N=64, K=256, block=32, out=0, split=
 def test_host_validation(lib, kw, status):
     assert call(lib, **kw) == status
     assert lib.mnb_last_error_detail()
+
+
+def test_unknown_flags_rejected(lib):
+    st = lib.mnb_gemv_flags(X, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, 2, None)
+    assert st == 10
+    # valid flags fall through to the ordinary checks (here: a NULL pointer)
+    assert lib.mnb_gemv_flags(0, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, 1, None) == 1
 
 
 def test_split_limits(lib):

@@ -156,5 +156,24 @@ def test_non_finite_inputs_follow_ieee():
     assert np.array_equal(g[np.isinf(r)], r[np.isinf(r)])
 
 
+def test_weights_ready_chain_matches_plain_calls():
+    """Back-to-back calls with the early-weights promise (programmatic
+    dependent launch) give the same bits as plain calls, also when each call's
+    activations are the previous call's output."""
+    inp = make_inputs(1, 4096, 4096, seed=17)
+    x, q, s, z = _gpu.to_device(inp)
+    ref = [x]
+    for i in range(4):
+        ref.append(mnb.gemv(ref[-1], q, s, z, "f16"))
+    torch.cuda.synchronize()
+    got = [x]
+    for i in range(4):
+        got.append(mnb.gemv(got[-1], q, s, z, "f16", weights_ready=True))
+    torch.cuda.synchronize()
+    for a, b in zip(ref[1:], got[1:]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    _gpu.compare(inp, _gpu.bits(got[1]), None)
+
+
 def test_no_device_error_recorded():
     assert mnb.device_error() == 0

@@ -160,9 +160,11 @@ int mnb_device_error(void *stream, unsigned int *code, int clear);
 /* Launch counters, for tests that must prove the GPU kernel ran:
  *   [0] launches, [1] fp16-output launches, [2] bf16-output launches,
  *   [3] launches with split_k > 1 (cluster reduction), [4 + M - 1] launches
- *   with M rows (M = 1..8).
+ *   with M rows (M = 1..8), [12] launches of the tensor-core kernel (M >= 2
+ *   without a K split, K a multiple of 1024, scales and zp 16-byte aligned,
+ *   M * K at most 32768).
  * Copies min(n, MNB_NUM_COUNTERS) counters to out; returns how many. */
-#define MNB_NUM_COUNTERS 12
+#define MNB_NUM_COUNTERS 13
 int mnb_debug_counters(uint64_t *out, int n);
 void mnb_debug_counters_reset(void);
 

@@ -105,8 +105,8 @@ def max_split_k(K: int) -> int:
 
 
 def counters() -> list:
-    buf = (ctypes.c_uint64 * 12)()
-    n = load().mnb_debug_counters(buf, 12)
+    buf = (ctypes.c_uint64 * 13)()
+    n = load().mnb_debug_counters(buf, 13)
     return [int(buf[i]) for i in range(n)]
 
 

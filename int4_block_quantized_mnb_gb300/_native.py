@@ -20,7 +20,7 @@ FLAG_WEIGHTS_READY = 1
 MAX_M = 8
 BLOCK = 32
 MAX_SPLIT_K = 8
-NUM_COUNTERS = 12
+NUM_COUNTERS = 13
 
 # Every symbol the header declares, with (restype, argtypes).
 _vp, _u8p, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)

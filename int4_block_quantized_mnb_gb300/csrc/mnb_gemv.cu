@@ -43,6 +43,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -63,6 +64,15 @@ constexpr int kMaxSplit = MNB_MAX_SPLIT_K;
 // producer and epilogue warps) on an SM sub-partition, i.e. 128 registers per thread.
 constexpr int consumer_warp_budget(int M) { return M <= 2 ? 12 : 16; }
 constexpr int max_threads(int M) { return (consumer_warp_budget(M) + 2) * 32; }
+
+// Tensor-core kernel: up to 16 K-slice consumer warps (18 warps with producer
+// and epilogue); the activations, pre-paired in B-fragment order, live in
+// shared memory (at most kMmaXBytes).
+constexpr int kMmaWarps = 16;
+constexpr int kMmaXBytes = 66 * 1024;
+constexpr int kMmaThreads = (kMmaWarps + 2) * 32;
+constexpr int kMmaRows = 16;                      // weight rows per tile
+constexpr int kMmaSeg = 256;                      // k per segment (128 code bytes)
 constexpr int kSmemBudget = 200 * 1024;           // stages + bookkeeping
 constexpr int kPartBudget = 32 * 1024;            // cluster partial sums per CTA
 constexpr int kMaxStages = 16;
@@ -96,10 +106,21 @@ struct Params {
   int stages;
   int rows_stage;   // rows of the weight matrix per stage (a multiple of the chunk rows)
   int q_pitch;      // bytes per row inside a stage's weight area
+  // tensor-core kernel only
+  int parts;        // K parts of a 16-row tile (one stage each)
+  int seg_part;     // 256-k segments per part
+  int wpp;          // consumer warps per part
+  int sc_sb;        // 16-byte scale chunks per row in a stage (odd)
+  int zp_zb;        // 16-byte zero-point chunks per row in a stage (odd)
+  int sc_offset;    // offset of a stage's scale box
+  int zp_offset;    // offset of a stage's zero-point box
+  int tx_bytes;     // bytes the three tensor copies of a stage write
   int q_bytes, sc_bytes, zp_bytes, stage_bytes;
   int bar_offset;   // shared-memory offset of the mbarrier array
   int red_offset;   // offset of the cross-warp reduction slots
   int part_offset;  // offset of the cluster partial sums
+  int xp_offset;    // offset of the tensor-core kernel's activation fragments
+  int xp_pitch;     // bytes per activation row of those fragments
   int flag_offset;  // offset of the CTA abort flag
 };
 
@@ -232,6 +253,78 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float c) {
   return d;
 }
 
+// D = A * B + C for one m16n8k16 tile, fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1,
+                                          const float (&c)[4]) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
+}
+
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Zero-points of a block pair (low nibble: even block, high nibble: odd
+// block) as the fp16 pairs the code extraction subtracts: 1024 + z for codes
+// taken from low nibbles, 64 + z for codes taken from high nibbles.  The
+// 64 + z / 1024 + z forms not produced by a mask come from the other by an
+// exact fp16 shift of 960.
+struct ZpPairs {
+  uint32_t lo_e, hi_e, lo_o, hi_o;
+};
+
+// Byte jp of a zero-point word in the low byte of both 16-bit halves.
+__device__ __forceinline__ uint32_t zp_byte_pair(uint32_t zword, int jp) {
+  return __byte_perm(zword, 0u, 0x4040u | static_cast<uint32_t>(jp) | (static_cast<uint32_t>(jp) << 8));
+}
+
+// fp16 number h (0 = low half, 1 = high half) of a 32-bit word, as fp32.
+__device__ __forceinline__ float half_word_to_float(uint32_t w, int h) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h ? (w >> 16) : (w & 0xFFFFu))));
+}
+
+// zw: the block pair's zero-point byte in the low byte of both halves.
+__device__ __forceinline__ ZpPairs zp_pairs(uint32_t zw) {
+  ZpPairs z;
+  z.lo_e = and_or(zw, 0x000F000Fu, 0x64006400u);             // 1024 + z_even
+  z.hi_o = and_or(zw, 0x00F000F0u, 0x54005400u);             // 64 + z_odd
+  z.hi_e = hsub2(z.lo_e, 0x63806380u);                       // 1024 + z - 960
+  z.lo_o = hadd2(z.hi_o, 0x63806380u);                       // 64 + z + 960
+  return z;
+}
+
+// One 32-block of a 16-row tile for the lane holding fragment rows g (codes
+// w0, zero-point pairs zl0/zh0, scale s0) and g + 8 (w1, zl1/zh1, s1), k
+// group tq: the exact code differences q - zp of word tq are the A operand of
+// two m16n8k16 products with the activation fragment xf, k paired as
+// (k0,k4) (k1,k5) in the first and (k2,k6) (k3,k7) in the second; the fresh
+// block sum is then scaled into the fp32 accumulators.
+__device__ __forceinline__ void mma_block(float (&acc)[4], uint32_t w0, uint32_t w1, uint4 xf,
+                                          uint32_t zl0, uint32_t zh0, uint32_t zl1,
+                                          uint32_t zh1, float s0, float s1) {
+  const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+  float d[4];
+  mma_16816(d, hsub2(and_or(w0, 0x000F000Fu, 0x64006400u), zl0),
+            hsub2(and_or(w1, 0x000F000Fu, 0x64006400u), zl1),
+            hsub2(and_or(w0, 0x00F000F0u, 0x54005400u), zh0),
+            hsub2(and_or(w1, 0x00F000F0u, 0x54005400u), zh1), xf.x, xf.y, zero4);
+  const uint32_t u0 = w0 >> 8, u1 = w1 >> 8;
+  mma_16816(d, hsub2(and_or(u0, 0x000F000Fu, 0x64006400u), zl0),
+            hsub2(and_or(u1, 0x000F000Fu, 0x64006400u), zl1),
+            hsub2(and_or(u0, 0x00F000F0u, 0x54005400u), zh0),
+            hsub2(and_or(u1, 0x00F000F0u, 0x54005400u), zh1), xf.z, xf.w, d);
+  acc[0] = fmaf(d[0], s0, acc[0]);                             // row g,   m = 2tq
+  acc[1] = fmaf(d[1], s0, acc[1]);                             // row g,   m = 2tq + 1
+  acc[2] = fmaf(d[2], s1, acc[2]);                             // row g+8, m = 2tq
+  acc[3] = fmaf(d[3], s1, acc[3]);                             // row g+8, m = 2tq + 1
+}
+
 // Butterfly that leaves lane L holding, summed over all 32 lanes, value
 // number (L >> (5 - log2(VP))) of the VP values every lane started with.
 template <int VP>
@@ -293,6 +386,106 @@ __device__ __forceinline__ RegionCopy plan_region(unsigned char* dst_base, const
   for (uint32_t i = 0; i < head; ++i) dst[i] = __ldg(src + i);
   for (uint32_t i = tail_start; i < n; ++i) dst[i] = __ldg(src + i);
   return RegionCopy{smem_u32(dst + head), src + head, body};
+}
+
+// ------------------------------------------------------------ warp roles --
+
+// Producer (one thread): streams stage loads of RS rows -- codes of the CTA's K
+// range, and the rows' scales and zero-points -- into the ring, each load
+// completing on its stage's mbarrier transaction count; then lets every copy
+// it issued land before the CTA may exit.
+__device__ __forceinline__ void run_producer(const Params& p, unsigned char* smem, uint32_t full0,
+                                             uint32_t empty0, volatile int* abort_flag,
+                                             int row_begin, int row_end, int RS, int nstages,
+                                             int k_begin, int k_len) {
+  const int split = p.split;
+  if (!p.weights_ready) wait_prerequisites();
+  int issued = 0;
+  int s = 0;                                        // stage slot of load i
+  uint32_t ph = 0;                                  // completed uses of slot s, mod 2
+  for (int i = 0; i < nstages; ++i) {
+    if (i >= p.stages && !mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, kErrStageFree))
+      break;
+    const int r0 = row_begin + i * RS;
+    const int nr = min(RS, row_end - r0);
+    unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+    const uint32_t bar = full0 + 8u * s;
+    // Scales and zero-points of these rows are contiguous in global memory.
+    const RegionCopy sc = plan_region(
+        st + p.q_bytes,
+        reinterpret_cast<const uint8_t*>(p.scales) + static_cast<size_t>(r0) * p.C * 2,
+        static_cast<uint32_t>(nr) * p.C * 2);
+    const RegionCopy zc = plan_region(st + p.q_bytes + p.sc_bytes,
+                                      p.zp + static_cast<size_t>(r0) * p.Z,
+                                      static_cast<uint32_t>(nr) * p.Z);
+    fence_proxy_async_smem();
+    const uint32_t q_row_bytes = static_cast<uint32_t>(k_len / 2);
+    const uint32_t tx = static_cast<uint32_t>(nr) * q_row_bytes + sc.body + zc.body;
+    mbar_arrive_expect_tx(bar, tx);
+    const uint8_t* qsrc = p.q + static_cast<size_t>(r0) * (p.K / 2) + k_begin / 2;
+    if (split == 1) {
+      bulk_copy_g2s(smem_u32(st), qsrc, static_cast<uint32_t>(nr) * q_row_bytes, bar);
+    } else {
+      for (int r = 0; r < nr; ++r)
+        bulk_copy_g2s(smem_u32(st + static_cast<size_t>(r) * p.q_pitch),
+                      qsrc + static_cast<size_t>(r) * (p.K / 2), q_row_bytes, bar);
+    }
+    if (sc.body) bulk_copy_g2s(sc.dst, sc.src, sc.body, bar);
+    if (zc.body) bulk_copy_g2s(zc.dst, zc.src, zc.body, bar);
+    issued = i + 1;
+    if (++s == p.stages) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  // Let every copy this thread issued land before the CTA may exit.
+  for (int i = max(0, issued - p.stages); i < issued; ++i) {
+    const int s = i % p.stages;
+    if (!mbar_try_wait(full0 + 8u * s, (i / p.stages) & 1)) {
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(full0 + 8u * s, (i / p.stages) & 1)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          atomicCAS(&g_device_error, 0u, kErrDrain);
+          break;
+        }
+      }
+    }
+  }
+}
+
+// Epilogue (one warp): for each tile of RC rows, in tile order, adds the
+// K-slice partial sums of every (row, m) value in slice order, rounds and
+// stores them (or keeps them for the cluster reduction), then frees the slot.
+// Tile i belongs to group i % groups, its (i / groups)-th tile.
+__device__ __forceinline__ void run_epilogue(const Params& p, const float* red, float* part,
+                                             uint32_t ready0, uint32_t free0,
+                                             volatile int* abort_flag, int row_begin,
+                                             int row_end, int RC, int ntiles, int M, int lane) {
+  wait_prerequisites();
+  const int vals_tile = RC * M;
+  int g = 0, t = 0;
+  for (int i = 0; i < ntiles; ++i) {
+    const int j = g * kSlotsPerGroup + t % kSlotsPerGroup;
+    if (!mbar_wait(ready0 + 8u * j, (t / kSlotsPerGroup) & 1, abort_flag, kErrReduceSlot)) break;
+    const int r0 = row_begin + i * RC;
+    const int vals = min(RC, row_end - r0) * M;
+    const float* slot = red + static_cast<size_t>(j) * p.wpg * vals_tile;
+    for (int e = lane; e < vals; e += 32) {
+      float sum = 0.f;
+      for (int w = 0; w < p.wpg; ++w) sum += slot[w * vals_tile + e];
+      const int r = e / M, m = e % M;
+      if (p.split == 1)
+        store_output(p.y, static_cast<size_t>(m) * p.N + r0 + r, sum, p.out_bf16);
+      else
+        part[(r0 - row_begin + r) * M + m] = sum;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(free0 + 8u * j);
+    if (++g == p.groups) {
+      g = 0;
+      ++t;
+    }
+  }
 }
 
 // ------------------------------------------------------------------ kernel --
@@ -371,89 +564,14 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
 
   if (warp == producer_warp) {
     // ------------------------------------------------------------ producer --
-    if (lane == 0) {
-      if (!p.weights_ready) wait_prerequisites();
-      int issued = 0;
-      int s = 0;                                        // stage slot of load i
-      uint32_t ph = 0;                                  // completed uses of slot s, mod 2
-      for (int i = 0; i < nstages; ++i) {
-        if (i >= p.stages && !mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, kErrStageFree))
-          break;
-        const int r0 = row_begin + i * RS;
-        const int nr = min(RS, row_end - r0);
-        unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-        const uint32_t bar = full0 + 8u * s;
-        // Scales and zero-points of these rows are contiguous in global memory.
-        const RegionCopy sc = plan_region(
-            st + p.q_bytes,
-            reinterpret_cast<const uint8_t*>(p.scales) + static_cast<size_t>(r0) * p.C * 2,
-            static_cast<uint32_t>(nr) * p.C * 2);
-        const RegionCopy zc = plan_region(st + p.q_bytes + p.sc_bytes,
-                                          p.zp + static_cast<size_t>(r0) * p.Z,
-                                          static_cast<uint32_t>(nr) * p.Z);
-        fence_proxy_async_smem();
-        const uint32_t q_row_bytes = static_cast<uint32_t>(k_len / 2);
-        const uint32_t tx = static_cast<uint32_t>(nr) * q_row_bytes + sc.body + zc.body;
-        mbar_arrive_expect_tx(bar, tx);
-        const uint8_t* qsrc = p.q + static_cast<size_t>(r0) * (p.K / 2) + k_begin / 2;
-        if (split == 1) {
-          bulk_copy_g2s(smem_u32(st), qsrc, static_cast<uint32_t>(nr) * q_row_bytes, bar);
-        } else {
-          for (int r = 0; r < nr; ++r)
-            bulk_copy_g2s(smem_u32(st + static_cast<size_t>(r) * p.q_pitch),
-                          qsrc + static_cast<size_t>(r) * (p.K / 2), q_row_bytes, bar);
-        }
-        if (sc.body) bulk_copy_g2s(sc.dst, sc.src, sc.body, bar);
-        if (zc.body) bulk_copy_g2s(zc.dst, zc.src, zc.body, bar);
-        issued = i + 1;
-        if (++s == p.stages) {
-          s = 0;
-          ph ^= 1u;
-        }
-      }
-      // Let every copy this thread issued land before the CTA may exit.
-      for (int i = max(0, issued - p.stages); i < issued; ++i) {
-        const int s = i % p.stages;
-        if (!mbar_try_wait(full0 + 8u * s, (i / p.stages) & 1)) {
-          const uint64_t t0 = global_ns();
-          while (!mbar_try_wait(full0 + 8u * s, (i / p.stages) & 1)) {
-            if (global_ns() - t0 > kWaitLimitNs) {
-              atomicCAS(&g_device_error, 0u, kErrDrain);
-              break;
-            }
-          }
-        }
-      }
-    }
+    if (lane == 0)
+      run_producer(p, smem, full0, empty0, abort_flag, row_begin, row_end, RS, nstages, k_begin,
+                   k_len);
     __syncwarp();
   } else if (warp == epilogue_warp) {
     // ------------------------------------------------------------ epilogue --
-    // Adds the K-slice partial sums of every row in slice order, rounds and
-    // stores (or keeps them for the cluster reduction), then frees the slot.
-    wait_prerequisites();
-    int g = 0, t = 0;                                   // tile i belongs to group g, its t-th
-    for (int i = 0; i < ntiles; ++i) {
-      const int j = g * kSlotsPerGroup + t % kSlotsPerGroup;
-      if (!mbar_wait(ready0 + 8u * j, (t / kSlotsPerGroup) & 1, abort_flag, kErrReduceSlot)) break;
-      const int r0 = row_begin + i * RC;
-      const int vals = min(RC, row_end - r0) * M;
-      const float* slot = red + static_cast<size_t>(j) * p.wpg * kVals;
-      if (lane < vals) {
-        float sum = 0.f;
-        for (int w = 0; w < p.wpg; ++w) sum += slot[w * kVals + lane];
-        const int r = lane / M, m = lane % M;
-        if (split == 1)
-          store_output(p.y, static_cast<size_t>(m) * p.N + r0 + r, sum, p.out_bf16);
-        else
-          part[(r0 - row_begin + r) * M + m] = sum;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(free0 + 8u * j);
-      if (++g == p.groups) {
-        g = 0;
-        ++t;
-      }
-    }
+    run_epilogue(p, red, part, ready0, free0, abort_flag, row_begin, row_end, RC, ntiles, M,
+                 lane);
   } else {
     // ----------------------------------------------------------- consumers --
     const int g = warp / p.wpg;
@@ -642,6 +760,277 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
       store_output(p.y, static_cast<size_t>(e % M) * p.N + row_begin + r, sum, p.out_bf16);
     }
     cluster_sync();  // peers' shared memory stays alive until everyone is done
+  }
+}
+
+
+// ------------------------------------------------------ tensor-core kernel --
+//
+// The multiply-accumulate of M >= 2 runs on the tensor cores (mma.sync
+// m16n8k16, fp16 operands, fp32 accumulation):
+//   A = 16 weight rows x 16 k: lane (g, t) holds code word t (k = 8t..8t+7 of
+//       the block) of rows g and g+8, dequantized exactly to q - zp by the same
+//       lop3 + packed subtraction as the CUDA-core kernel; the word's pairs
+//       (k0,k4) (k1,k5) feed one mma and (k2,k6) (k3,k7) the next, so the two
+//       mmas cover the 32-block.
+//   B = the same 16 k of activation row m = g (zero for g >= M), paired the
+//       same way; the whole activation block is staged once per CTA in shared
+//       memory in this fragment order (16 bytes per lane and block).
+//   D = 16 rows x 8 activation rows, fresh per block, multiplied by the rows'
+//       fp32 scales into fp32 accumulators.
+// Products of fp16 codes and activations are exact in the fp32 accumulate.
+//
+// Work: a CTA owns a contiguous range of 16-row tiles; each tile is cut into
+// `parts` K parts of whole 256-k segments, and each (tile, part) is one stage,
+// loaded by three TMA tensor copies and consumed by the `wpp` warps of that
+// part, each on a fixed run of segments.  Shared-memory layout of a stage:
+//   codes : box {128 B, 16 rows, seg_part segments} of the code matrix viewed
+//           as (byte in segment, row, segment), 128-byte swizzle: chunk j
+//           (block 8s + j) of row r of segment s lands at
+//           (16 s + r) * 128 + 16 * (j ^ (r & 7)), so the eight rows a
+//           fragment load touches sit in eight different bank groups.
+//   scales: box {8 scales, sc_sb chunks, 16 rows} of (scale in chunk, chunk,
+//           row), no swizzle: the 8 scales of segment s of row r at
+//           (r * sc_sb + s) * 16; sc_sb is odd (a chunk past the part is
+//           loaded or zero-filled) so rows land in different bank groups.
+//   zeros : box {16 B, zp_zb chunks, 16 rows} of (byte, chunk, row): the 4
+//           zero-point bytes of segment s of row r at (r * zp_zb + s / 4) * 16
+//           + 4 (s % 4); zp_zb odd for the same reason.
+// Rows past N are zero-filled by the copies and never stored.
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Producer of the tensor-core kernel (one thread): one stage per (tile, part),
+// three tensor copies completing on the stage's mbarrier.
+__device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* smem,
+                                                uint32_t full0, uint32_t empty0,
+                                                volatile int* abort_flag, int t_begin,
+                                                int nunits, const CUtensorMap* tm_q,
+                                                const CUtensorMap* tm_sc,
+                                                const CUtensorMap* tm_zp) {
+  prefetch_tensor_map(tm_q);
+  prefetch_tensor_map(tm_sc);
+  prefetch_tensor_map(tm_zp);
+  if (!p.weights_ready) wait_prerequisites();
+  int issued = 0, s = 0, part = 0, tile = t_begin;
+  uint32_t ph = 0;
+  for (int i = 0; i < nunits; ++i) {
+    if (i >= p.stages && !mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, kErrStageFree)) break;
+    const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
+    const uint32_t bar = full0 + 8u * s;
+    const int row0 = tile * kMmaRows;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.tx_bytes));
+    tma_load_3d(st, tm_q, 0, row0, part * p.seg_part, bar);
+    tma_load_3d(st + p.sc_offset, tm_sc, 0, part * p.seg_part, row0, bar);
+    tma_load_3d(st + p.zp_offset, tm_zp, 0, part * (p.seg_part / 4), row0, bar);
+    issued = i + 1;
+    if (++part == p.parts) {
+      part = 0;
+      ++tile;
+    }
+    if (++s == p.stages) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  for (int i = max(0, issued - p.stages); i < issued; ++i) {
+    const int si = i % p.stages;
+    if (!mbar_try_wait(full0 + 8u * si, (i / p.stages) & 1)) {
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(full0 + 8u * si, (i / p.stages) & 1)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          atomicCAS(&g_device_error, 0u, kErrDrain);
+          break;
+        }
+      }
+    }
+  }
+}
+
+template <int M>
+__global__ void __launch_bounds__(kMmaThreads, 1)
+    gemv_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_sc,
+                    const __grid_constant__ CUtensorMap tm_zp) {
+  constexpr int RC = kMmaRows;
+  constexpr int kVals = RC * M;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the 128-byte swizzle is a function of address bits 7-9: align to 1 KB
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int W = p.wpg;                                 // consumer warps
+  const int producer_warp = W;
+  const int epilogue_warp = W + 1;
+  const int nslots = kSlotsPerGroup;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_offset);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8u * p.stages;
+  const uint32_t ready0 = empty0 + 8u * p.stages;
+  const uint32_t free0 = ready0 + 8u * nslots;
+  float* red = reinterpret_cast<float*>(smem + p.red_offset);     // [slots][W][16 * M]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.flag_offset);
+
+  const int tiles = (p.N + RC - 1) / RC;
+  const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * tiles) / gridDim.x);
+  const int t_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * tiles) / gridDim.x);
+  const int ntiles = t_end - t_begin;
+  const int row_begin = t_begin * RC;
+  const int row_end = min(p.N, t_end * RC);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, p.wpp);
+    }
+    for (int j = 0; j < nslots; ++j) {
+      mbar_init(ready0 + 8u * j, W);
+      mbar_init(free0 + 8u * j, 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  allow_dependents();
+
+  if (warp == producer_warp) {
+    if (lane == 0)
+      run_tc_producer(p, smem, full0, empty0, abort_flag, t_begin, ntiles * p.parts, &tm_q,
+                      &tm_sc, &tm_zp);
+    __syncwarp();
+    return;
+  }
+  if (warp == epilogue_warp) {
+    run_epilogue(p, red, nullptr, ready0, free0, abort_flag, row_begin, row_end, RC, ntiles, M,
+                 lane);
+    return;
+  }
+
+  // ------------------------------------------------------------- consumers --
+  const int part = warp / p.wpp;
+  const int wi = warp - part * p.wpp;
+  const int s0 = (wi * p.seg_part) / p.wpp;            // this warp's segments [s0, s1)
+  const int s1 = ((wi + 1) * p.seg_part) / p.wpp;      //   of its part
+  const int gq = lane >> 2;                            // fragment row group
+  const int tq = lane & 3;                             // fragment k group
+
+  // Activation fragments: row m, block b, k group tq -> 16 bytes at
+  // xp + m * xp_pitch + b * 64 + tq * 16 holding x[m][32b + 8tq + {0..7}]
+  // paired (0,4) (1,5) (2,6) (3,7).  The consumer warps fill it together.
+  wait_prerequisites();
+  unsigned char* xp = smem + p.xp_offset;
+  {
+    const int total = M * p.C * 4;
+    for (int e = threadIdx.x; e < total; e += W * 32) {
+      const int m = e / (p.C * 4);
+      const int rem = e - m * p.C * 4;
+      const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + 8 * rem;
+      uint16_t h[8];
+      if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+        h[0] = v.x & 0xFFFF; h[1] = v.x >> 16; h[2] = v.y & 0xFFFF; h[3] = v.y >> 16;
+        h[4] = v.z & 0xFFFF; h[5] = v.z >> 16; h[6] = v.w & 0xFFFF; h[7] = v.w >> 16;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) h[k] = __ldg(src + k);
+      }
+      uint4 out;
+      out.x = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[4]) << 16);
+      out.y = static_cast<uint32_t>(h[1]) | (static_cast<uint32_t>(h[5]) << 16);
+      out.z = static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[6]) << 16);
+      out.w = static_cast<uint32_t>(h[3]) | (static_cast<uint32_t>(h[7]) << 16);
+      *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + rem * 16) = out;
+    }
+    // all consumer warps (named barrier 1; producer and epilogue do not take part)
+    asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
+  }
+  const unsigned char* xfrag = xp + min(gq, M - 1) * p.xp_pitch +
+                               (part * p.seg_part + s0) * 512 + tq * 16;
+  const bool x_lane = gq < M;
+
+  // Lane offsets inside a stage.  Codes: row gq of segment s, chunk j at
+  // s * 2048 + gq * 128 + 16 * (j ^ gq) + 4 tq; row gq + 8 is 1024 bytes on.
+  uint32_t qoff[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) qoff[j] = gq * 128 + 16 * (j ^ gq) + 4 * tq;
+  const int sc_lane = p.sc_offset + gq * p.sc_sb * 16;
+  const int sc_hi = 8 * p.sc_sb * 16;                  // row gq + 8
+  const int zp_lane = p.zp_offset + gq * p.zp_zb * 16;
+  const int zp_hi = 8 * p.zp_zb * 16;
+
+  int s = part;                                        // stage of unit (t * parts + part)
+  uint32_t ph = 0;
+  for (int t = 0; t < ntiles; ++t) {
+    if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) break;
+    const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int sg = s0; sg < s1; ++sg) {
+      const unsigned char* qs = st + sg * 2048;
+      const uint4 sca = *reinterpret_cast<const uint4*>(st + sc_lane + sg * 16);
+      const uint4 scb = *reinterpret_cast<const uint4*>(st + sc_lane + sc_hi + sg * 16);
+      const int zo = zp_lane + (sg >> 2) * 16 + (sg & 3) * 4;
+      const uint32_t zwa = *reinterpret_cast<const uint32_t*>(st + zo);
+      const uint32_t zwb = *reinterpret_cast<const uint32_t*>(st + zo + zp_hi);
+      const unsigned char* xs = xfrag + (sg - s0) * 512;
+      const uint32_t scw_a[4] = {sca.x, sca.y, sca.z, sca.w};
+      const uint32_t scw_b[4] = {scb.x, scb.y, scb.z, scb.w};
+#pragma unroll
+      for (int jp = 0; jp < 4; ++jp) {                 // block pair (2 jp, 2 jp + 1)
+        const ZpPairs z0 = zp_pairs(zp_byte_pair(zwa, jp));
+        const ZpPairs z1 = zp_pairs(zp_byte_pair(zwb, jp));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = 2 * jp + h;
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(qs + qoff[j]);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(qs + qoff[j] + 1024);
+          uint4 xf = make_uint4(0u, 0u, 0u, 0u);
+          if (x_lane) xf = *reinterpret_cast<const uint4*>(xs + 64 * j);
+          const float sa = half_word_to_float(scw_a[jp], h);
+          const float sb = half_word_to_float(scw_b[jp], h);
+          if (h == 0)
+            mma_block(acc, w0, w1, xf, z0.lo_e, z0.hi_e, z1.lo_e, z1.hi_e, sa, sb);
+          else
+            mma_block(acc, w0, w1, xf, z0.lo_o, z0.hi_o, z1.lo_o, z1.hi_o, sa, sb);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8u * s);
+
+    const int j = t % nslots;
+    if (t >= nslots && !mbar_wait(free0 + 8u * j, ((t / nslots) - 1) & 1, abort_flag,
+                                  kErrReduceSlot))
+      break;
+    float* slot = red + (static_cast<size_t>(j) * W + warp) * kVals;
+    const int m0 = 2 * tq;
+    if (m0 < M) {
+      slot[gq * M + m0] = acc[0];
+      slot[(gq + 8) * M + m0] = acc[2];
+    }
+    if (m0 + 1 < M) {
+      slot[gq * M + m0 + 1] = acc[1];
+      slot[(gq + 8) * M + m0 + 1] = acc[3];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ready0 + 8u * j);
+    s += p.parts;                                      // this part of the next tile
+    while (s >= p.stages) {
+      s -= p.stages;
+      ph ^= 1u;
+    }
   }
 }
 
@@ -835,6 +1224,204 @@ int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, const Kerne
   return MNB_OK;
 }
 
+// Activation fragments of the tensor-core kernel: 64 bytes per block and row;
+// a row pitch of 64 mod 128 bytes puts two activation rows (4 lanes x 16
+// bytes each) in one shared-memory wavefront.
+int mma_x_pitch(int C) { return C * 64 + ((C & 1) ? 0 : 64); }
+int mma_x_bytes(int M, int C) { return M * mma_x_pitch(C); }
+
+// The tensor-core kernel takes M >= 2 without a K split when K is a multiple
+// of 1024 (whole 256-k segments and 16-byte zero-point rows for the tensor
+// copies), scales and zero-points are 16-byte aligned, and the activation
+// fragments fit in kMmaXBytes.
+bool use_mma(int M, int K, int split, const void* scales, const void* zp) {
+  return M >= 2 && split == 1 && K % 1024 == 0 && K <= 65536 &&
+         (reinterpret_cast<uintptr_t>(scales) & 15u) == 0 &&
+         (reinterpret_cast<uintptr_t>(zp) & 15u) == 0 && mma_x_bytes(M, K / kBlock) <= kMmaXBytes;
+}
+
+using MmaFn = void (*)(const Params, const CUtensorMap, const CUtensorMap, const CUtensorMap);
+
+MmaFn pick_mma_kernel(int M) {
+  switch (M) {
+    case 1: return &gemv_mma_kernel<1>;
+    case 2: return &gemv_mma_kernel<2>;
+    case 3: return &gemv_mma_kernel<3>;
+    case 4: return &gemv_mma_kernel<4>;
+    case 5: return &gemv_mma_kernel<5>;
+    case 6: return &gemv_mma_kernel<6>;
+    case 7: return &gemv_mma_kernel<7>;
+    default: return &gemv_mma_kernel<8>;
+  }
+}
+
+int round_up(int v, int a) { return (v + a - 1) / a * a; }
+int odd_at_least(int v) { return v | 1; }
+
+// Stage layout and K split of the tensor-core kernel: the fewest K parts per
+// tile that still leave at least four stages in shared memory (more parts
+// mean smaller stages released by fewer warps each).
+int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, Plan* plan) {
+  Params& p = plan->p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.C = K / kBlock;
+  p.Z = (p.C + 1) / 2;
+  p.split = 1;
+  p.groups = 1;
+  const int segs = K / kMmaSeg;
+  const int nslots = kSlotsPerGroup;
+  p.xp_pitch = mma_x_pitch(p.C);
+  const int x_bytes = mma_x_bytes(M, p.C);
+  const int budget = static_cast<int>(dev.smem_optin) - 1024;   // 1 KB for the alignment
+  int best = -1;
+  for (int parts = 1; parts <= 8; parts *= 2) {
+    if (segs % parts || (segs / parts) % 4 || segs / parts + 1 > 256) continue;
+    const int seg_part = segs / parts;
+    const int wpp = std::min(kMmaWarps / parts, seg_part);
+    const int W = wpp * parts;
+    const int q_bytes = kMmaRows * seg_part * 128;
+    const int sc_sb = odd_at_least(seg_part);
+    const int zp_zb = odd_at_least(seg_part / 4);
+    const int sc_bytes = round_up(kMmaRows * sc_sb * 16, 128);
+    const int zp_bytes = round_up(kMmaRows * zp_zb * 16, 128);
+    const int stage_bytes = round_up(q_bytes + sc_bytes + zp_bytes, 1024);
+    const int red_bytes = round_up(nslots * W * kMmaRows * M * 4, 16);
+    const int fixed = x_bytes + red_bytes + 8 * 2 * nslots + 16;
+    const int stages = std::min(kMaxStages, (budget - fixed) / (stage_bytes + 16));
+    if (stages < std::max(2, parts)) continue;
+    best = parts;
+    p.parts = parts;
+    p.seg_part = seg_part;
+    p.wpp = wpp;
+    p.wpg = W;
+    p.sc_sb = sc_sb;
+    p.zp_zb = zp_zb;
+    p.q_bytes = q_bytes;
+    p.sc_offset = q_bytes;
+    p.sc_bytes = sc_bytes;
+    p.zp_offset = q_bytes + sc_bytes;
+    p.zp_bytes = zp_bytes;
+    p.tx_bytes = kMmaRows * (seg_part * 128 + sc_sb * 16 + zp_zb * 16);
+    p.stage_bytes = stage_bytes;
+    p.stages = stages;
+    if (stages >= 4) break;
+  }
+  if (best < 0) return fail(MNB_ERR_SHAPE, "shape needs more shared memory than one SM has");
+  const int red_bytes = round_up(nslots * p.wpg * kMmaRows * M * 4, 16);
+  int off = p.stages * p.stage_bytes;
+  p.xp_offset = off;
+  off += x_bytes;
+  p.red_offset = off;
+  off += red_bytes;
+  p.bar_offset = off;
+  off += 8 * (2 * p.stages + 2 * nslots);
+  p.part_offset = off;
+  p.flag_offset = off;
+  off += 16;
+  const long long tiles = (static_cast<long long>(N) + kMmaRows - 1) / kMmaRows;
+  plan->smem = static_cast<size_t>(off) + 1024;
+  plan->grid = dim3(static_cast<unsigned>(std::max<long long>(1, std::min<long long>(dev.sms, tiles))));
+  plan->block = dim3(static_cast<unsigned>((p.wpg + 2) * 32));
+  return MNB_OK;
+}
+
+// ---------------------------------------------------------- tensor maps --
+//
+// The three views the tensor-core kernel copies from (see its layout notes),
+// encoded with the driver's cuTensorMapEncodeTiled (fetched once through the
+// runtime, no link-time dependence on libcuda).  A map depends only on the
+// array's address, N, K and the part count, so encoded maps are kept in a
+// small cache: static weights are encoded once.
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct MapEntry {
+  const void* ptr = nullptr;
+  int kind = -1, N = 0, K = 0, parts = 0;
+  CUtensorMap map;
+};
+
+constexpr int kMapCache = 96;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+std::mutex g_map_mutex;
+EncodeTiledFn g_encode = nullptr;
+
+enum MapKind { kMapCodes = 0, kMapScales = 1, kMapZeros = 2 };
+
+int encode_map(MapKind kind, const void* ptr, const Params& p, CUtensorMap* out) {
+  const cuuint64_t N = static_cast<cuuint64_t>(p.N);
+  const cuuint64_t K = static_cast<cuuint64_t>(p.K);
+  const cuuint32_t ones[3] = {1, 1, 1};
+  void* base = const_cast<void*>(ptr);
+  CUresult r;
+  if (kind == kMapCodes) {
+    // (byte in segment, row, segment): rows K/2 bytes apart, segments 128
+    const cuuint64_t dims[3] = {128, N, K / kMmaSeg};
+    const cuuint64_t strides[2] = {K / 2, 128};
+    const cuuint32_t box[3] = {128, kMmaRows, static_cast<cuuint32_t>(p.seg_part)};
+    r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, ones,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (kind == kMapScales) {
+    // (scale in 8-scale chunk, chunk, row)
+    const cuuint64_t dims[3] = {8, K / 256, N};
+    const cuuint64_t strides[2] = {16, K / 16};
+    const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(p.sc_sb), kMmaRows};
+    r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, base, dims, strides, box, ones,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    // (byte in 16-byte chunk, chunk, row)
+    const cuuint64_t dims[3] = {16, K / 1024, N};
+    const cuuint64_t strides[2] = {16, K / 64};
+    const cuuint32_t box[3] = {16, static_cast<cuuint32_t>(p.zp_zb), kMmaRows};
+    r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, ones,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS)
+    return fail(MNB_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult " + std::to_string(r) + ")");
+  return MNB_OK;
+}
+
+int tensor_map(MapKind kind, const void* ptr, const Params& p, CUtensorMap* out) {
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(MNB_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  for (const MapEntry& m : g_maps)
+    if (m.ptr == ptr && m.kind == kind && m.N == p.N && m.K == p.K && m.parts == p.parts) {
+      *out = m.map;
+      return MNB_OK;
+    }
+  MapEntry& slot = g_maps[g_map_next];
+  const int st = encode_map(kind, ptr, p, &slot.map);
+  if (st != MNB_OK) {
+    slot.ptr = nullptr;
+    return st;
+  }
+  slot.ptr = ptr;
+  slot.kind = kind;
+  slot.N = p.N;
+  slot.K = p.K;
+  slot.parts = p.parts;
+  g_map_next = (g_map_next + 1) % kMapCache;
+  *out = slot.map;
+  return MNB_OK;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x0 = reinterpret_cast<uintptr_t>(a), y0 = reinterpret_cast<uintptr_t>(b);
   return x0 < y0 + nb && y0 < x0 + na;
@@ -929,9 +1516,14 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   if ((st = device_info(&dev)) != MNB_OK) return st;
   const int split = split_k == 0 ? auto_split(M, N, K, dev.sms) : split_k;
 
+  bool mma = use_mma(M, K, split, scales, zp);
   const KernelShape ks = pick_shape(M, K / kBlock, split, scales);
-  Plan plan;
-  if ((st = make_plan(dev, M, N, K, split, ks, &plan)) != MNB_OK) return st;
+  Plan plan{};
+  if (mma && make_mma_plan(dev, M, N, K, &plan) != MNB_OK) {
+    mma = false;                                  // no stage layout fits: CUDA-core kernel
+    plan = Plan{};
+  }
+  if (!mma && (st = make_plan(dev, M, N, K, split, ks, &plan)) != MNB_OK) return st;
   Params& p = plan.p;
   p.x = static_cast<const uint16_t*>(x);
   p.q = qweight;
@@ -941,8 +1533,16 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   p.out_bf16 = out_dtype == MNB_OUT_BF16;
   p.weights_ready = (flags & MNB_FLAG_WEIGHTS_READY) ? 1 : 0;
 
-  KernelFn fn = pick_kernel(M, ks);
-  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+  CUtensorMap maps[3];
+  if (mma) {
+    if ((st = tensor_map(kMapCodes, qweight, p, &maps[0])) != MNB_OK ||
+        (st = tensor_map(kMapScales, scales, p, &maps[1])) != MNB_OK ||
+        (st = tensor_map(kMapZeros, zp, p, &maps[2])) != MNB_OK)
+      return st;
+  }
+  const void* fn = mma ? reinterpret_cast<const void*>(pick_mma_kernel(M))
+                       : reinterpret_cast<const void*>(pick_kernel(M, ks));
+  cudaError_t e = cudaFuncSetAttribute(fn,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.smem));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
@@ -964,12 +1564,14 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  e = cudaLaunchKernelEx(&cfg, fn, p);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx");
+  void* args[4] = {&p, &maps[0], &maps[1], &maps[2]};
+  e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
   g_counters[0].fetch_add(1, std::memory_order_relaxed);
   g_counters[p.out_bf16 ? 2 : 1].fetch_add(1, std::memory_order_relaxed);
   if (split > 1) g_counters[3].fetch_add(1, std::memory_order_relaxed);
   g_counters[4 + M - 1].fetch_add(1, std::memory_order_relaxed);
+  if (mma) g_counters[12].fetch_add(1, std::memory_order_relaxed);
   return MNB_OK;
 }
 

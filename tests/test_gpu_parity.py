@@ -97,6 +97,36 @@ def test_counters_prove_the_kernel_ran():
     assert d[0] == 2 and d[1] == 1 and d[2] == 1 and d[3] == 1 and d[4 + 2 - 1] == 2
 
 
+def test_tensor_core_kernel_runs_for_small_batches():
+    """M >= 2 without a K split runs the tensor-core kernel; a K split or M = 1
+    runs the CUDA-core kernel.  Both meet the bound."""
+    for M, N, split, want in ((4, 130, 1, 1), (2, 4096, 0, 1), (8, 130, 1, 1), (4, 130, 2, 0),
+                              (1, 130, 1, 0)):
+        inp = make_inputs(M, N, 4096, seed=M + split)
+        dev = _gpu.to_device(inp)
+        before = mnb.counters()[12]
+        y16 = _gpu.bits(_gpu.run(dev, "f16", split))
+        ybf = _gpu.bits(_gpu.run(dev, "bf16", split))
+        assert mnb.counters()[12] - before == 2 * want, (M, split)
+        cols = None if N <= 256 else np.arange(0, N, 7)
+        _gpu.compare(inp, y16, ybf, cols=cols)
+
+
+def test_all_zero_weight_rows_give_exact_zero():
+    """Rows whose codes all equal their block's zero-point contribute exactly
+    zero: the bound is 0 there, so the result must be +-0, on both kernels."""
+    for M in (1, 2, 8):
+        inp = make_inputs(M, 64, 1024, seed=40 + M)
+        q = inp.qweight.copy()
+        zp = inp.zp.copy()
+        q[::2] = 0x77                      # every code 7 in even rows
+        zp[::2] = 0x77                     # every zero-point 7 in even rows
+        inp.qweight, inp.zp = q, zp
+        y16 = _gpu.bits(_gpu.run(_gpu.to_device(inp), "f16", 1))
+        assert np.all((y16[:, ::2] & 0x7FFF) == 0)
+        _gpu.compare(inp, y16, None)
+
+
 def test_misaligned_pointers():
     """x, scales and zp need not be 16-byte aligned (qweight must be)."""
     M, N, K = 2, 75, 96 * 3

@@ -123,7 +123,17 @@ int mnb_gemv(const void *x, const uint8_t *qweight, const void *scales, const ui
  */
 #define MNB_FLAG_WEIGHTS_READY 1u
 
-/* mnb_gemv with flags (0 or MNB_FLAG_WEIGHTS_READY); mnb_gemv(...) is
+/*
+ * MNB_FLAG_TENSOR_CORES: permit the tensor-core kernel where it applies (no K
+ * split, K a multiple of 1024, scales and zp 16-byte aligned, M * K at most
+ * 33792).  It forms the same exact fp16 products (q - zp) * x and accumulates
+ * them in fp32 with mma.sync m16n8k16 instead of fp32 FMAs; results meet the
+ * same error bound and bf16 invariant, but their bits may differ from the
+ * default kernels'.  Without the flag no tensor-core instruction is used.
+ */
+#define MNB_FLAG_TENSOR_CORES 2u
+
+/* mnb_gemv with flags (0 or an OR of the MNB_FLAG_* bits); mnb_gemv(...) is
  * mnb_gemv_flags(..., 0, stream).  Same arguments, checks and statuses, plus
  * MNB_ERR_FLAGS for unknown flag bits. */
 int mnb_gemv_flags(const void *x, const uint8_t *qweight, const void *scales, const uint8_t *zp,
@@ -160,9 +170,8 @@ int mnb_device_error(void *stream, unsigned int *code, int clear);
 /* Launch counters, for tests that must prove the GPU kernel ran:
  *   [0] launches, [1] fp16-output launches, [2] bf16-output launches,
  *   [3] launches with split_k > 1 (cluster reduction), [4 + M - 1] launches
- *   with M rows (M = 1..8), [12] launches of the tensor-core kernel (M >= 2
- *   without a K split, K a multiple of 1024, scales and zp 16-byte aligned,
- *   M * K at most 32768).
+ *   with M rows (M = 1..8), [12] launches of the tensor-core kernel (only
+ *   with MNB_FLAG_TENSOR_CORES).
  * Copies min(n, MNB_NUM_COUNTERS) counters to out; returns how many. */
 #define MNB_NUM_COUNTERS 13
 int mnb_debug_counters(uint64_t *out, int n);

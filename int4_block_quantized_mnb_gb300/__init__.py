@@ -10,12 +10,13 @@ from __future__ import annotations
 
 import ctypes
 
-from ._native import (BLOCK, FLAG_WEIGHTS_READY, MAX_M, MAX_SPLIT_K, OUT_BF16, OUT_F16,
+from ._native import (BLOCK, FLAG_TENSOR_CORES, FLAG_WEIGHTS_READY, MAX_M, MAX_SPLIT_K,
+                      OUT_BF16, OUT_F16,
                       MnbError, check, load)
 
 __all__ = ["gemv", "gemv_ptr", "split_k_auto", "min_split_k", "max_split_k", "counters",
            "reset_counters", "device_error", "MnbError", "OUT_F16", "OUT_BF16", "BLOCK",
-           "MAX_M", "MAX_SPLIT_K", "FLAG_WEIGHTS_READY"]
+           "MAX_M", "MAX_SPLIT_K", "FLAG_WEIGHTS_READY", "FLAG_TENSOR_CORES"]
 
 _DTYPES = {"f16": OUT_F16, "float16": OUT_F16, "bf16": OUT_BF16, "bfloat16": OUT_BF16}
 
@@ -46,7 +47,7 @@ def gemv_ptr(x: int, qweight: int, scales: int, zp: int, y: int, M: int, N: int,
 
 
 def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stream=None,
-         weights_ready: bool = False):
+         weights_ready: bool = False, tensor_cores: bool = False):
     """y = MatMulNBits(x, qweight, scales, zp) on the current CUDA device.
 
     x [M][K] float16, qweight [N][K/2] uint8, scales [N][K/32] float16,
@@ -54,7 +55,8 @@ def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stre
     float16 or bfloat16 (or writes the given ``y``).  ``weights_ready=True``
     promises that the kernel launched just before on the stream does not
     write qweight, scales or zp (static weights), so the call may start
-    streaming them before that kernel completes.
+    streaming them before that kernel completes.  ``tensor_cores=True``
+    permits the tensor-core kernel where it applies (MNB_FLAG_TENSOR_CORES).
     """
     import torch
     code = _out_code(out_dtype)
@@ -82,7 +84,8 @@ def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stre
     with torch.cuda.device(x.device):
         gemv_ptr(x.data_ptr(), qweight.data_ptr(), scales.data_ptr(), zp.data_ptr(),
                  y.data_ptr(), M, N, K, BLOCK, code, int(split_k), stream.cuda_stream,
-                 FLAG_WEIGHTS_READY if weights_ready else 0)
+                 (FLAG_WEIGHTS_READY if weights_ready else 0) |
+                 (FLAG_TENSOR_CORES if tensor_cores else 0))
     return y
 
 

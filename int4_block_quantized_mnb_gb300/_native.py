@@ -17,6 +17,7 @@ STATUS = {0: "MNB_OK", 1: "MNB_ERR_NULL", 2: "MNB_ERR_SHAPE", 3: "MNB_ERR_BLOCK"
           4: "MNB_ERR_DTYPE", 5: "MNB_ERR_SPLITK", 6: "MNB_ERR_ALIGN", 7: "MNB_ERR_ALIAS",
           8: "MNB_ERR_CUDA", 9: "MNB_ERR_DEVICE", 10: "MNB_ERR_FLAGS"}
 FLAG_WEIGHTS_READY = 1
+FLAG_TENSOR_CORES = 2
 MAX_M = 8
 BLOCK = 32
 MAX_SPLIT_K = 8

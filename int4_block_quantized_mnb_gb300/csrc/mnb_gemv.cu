@@ -107,9 +107,10 @@ struct Params {
   int rows_stage;   // rows of the weight matrix per stage (a multiple of the chunk rows)
   int q_pitch;      // bytes per row inside a stage's weight area
   // tensor-core kernel only
-  int parts;        // K parts of a 16-row tile (one stage each)
-  int seg_part;     // 256-k segments per part
-  int wpp;          // consumer warps per part
+  int tr;           // 16-row sub-tiles per tile
+  int wk;           // K slices = 256-k segments per stage
+  int steps;        // stages per tile (K / 256 / wk)
+  int wtc;          // consumer warps (wk * tr)
   int sc_sb;        // 16-byte scale chunks per row in a stage (odd)
   int zp_zb;        // 16-byte zero-point chunks per row in a stage (odd)
   int sc_offset;    // offset of a stage's scale box
@@ -286,7 +287,12 @@ __device__ __forceinline__ uint32_t zp_byte_pair(uint32_t zword, int jp) {
 
 // fp16 number h (0 = low half, 1 = high half) of a 32-bit word, as fp32.
 __device__ __forceinline__ float half_word_to_float(uint32_t w, int h) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(h ? (w >> 16) : (w & 0xFFFFu))));
+  float f;
+  if (h)
+    asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.f32.f16 %0, hi;\n}" : "=f"(f) : "r"(w));
+  else
+    asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.f32.f16 %0, lo;\n}" : "=f"(f) : "r"(w));
+  return f;
 }
 
 // zw: the block pair's zero-point byte in the low byte of both halves.
@@ -299,6 +305,28 @@ __device__ __forceinline__ ZpPairs zp_pairs(uint32_t zw) {
   return z;
 }
 
+// Eight activations k0..k7 (packed two per word) regrouped into the B
+// fragment pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7).
+__device__ __forceinline__ uint4 pair_k4(uint4 v) {
+  uint4 o;
+  o.x = __byte_perm(v.x, v.z, 0x5410);
+  o.y = __byte_perm(v.x, v.z, 0x7632);
+  o.z = __byte_perm(v.y, v.w, 0x5410);
+  o.w = __byte_perm(v.y, v.w, 0x7632);
+  return o;
+}
+
+// D = A * B for one m16n8k16 tile (zero accumulator input).
+__device__ __forceinline__ void mma_16816_zero(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm("{\n .reg .f32 z;\n mov.f32 z, 0f00000000;\n"
+      " mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {z,z,z,z};\n}"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // One 32-block of a 16-row tile for the lane holding fragment rows g (codes
 // w0, zero-point pairs zl0/zh0, scale s0) and g + 8 (w1, zl1/zh1, s1), k
 // group tq: the exact code differences q - zp of word tq are the A operand of
@@ -308,12 +336,11 @@ __device__ __forceinline__ ZpPairs zp_pairs(uint32_t zw) {
 __device__ __forceinline__ void mma_block(float (&acc)[4], uint32_t w0, uint32_t w1, uint4 xf,
                                           uint32_t zl0, uint32_t zh0, uint32_t zl1,
                                           uint32_t zh1, float s0, float s1) {
-  const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
   float d[4];
-  mma_16816(d, hsub2(and_or(w0, 0x000F000Fu, 0x64006400u), zl0),
-            hsub2(and_or(w1, 0x000F000Fu, 0x64006400u), zl1),
-            hsub2(and_or(w0, 0x00F000F0u, 0x54005400u), zh0),
-            hsub2(and_or(w1, 0x00F000F0u, 0x54005400u), zh1), xf.x, xf.y, zero4);
+  mma_16816_zero(d, hsub2(and_or(w0, 0x000F000Fu, 0x64006400u), zl0),
+                 hsub2(and_or(w1, 0x000F000Fu, 0x64006400u), zl1),
+                 hsub2(and_or(w0, 0x00F000F0u, 0x54005400u), zh0),
+                 hsub2(and_or(w1, 0x00F000F0u, 0x54005400u), zh1), xf.x, xf.y);
   const uint32_t u0 = w0 >> 8, u1 = w1 >> 8;
   mma_16816(d, hsub2(and_or(u0, 0x000F000Fu, 0x64006400u), zl0),
             hsub2(and_or(u1, 0x000F000Fu, 0x64006400u), zl1),
@@ -511,9 +538,10 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
 
   // mbarriers:
   //   full[s]   (stage)  1 arrival + transaction bytes: the stage's data landed
-  //   empty[s]  (stage)  wpg arrivals per tile of the stage: once every tile's
-  //                      K-slice warps hold their data in registers the stage
-  //                      may be refilled
+  //   empty[s]  (stage)  one arrival per consumer warp: every consumer warp
+  //                      passes every stage load in order (so no parity wait
+  //                      can alias an older phase), and arrives once it holds
+  //                      the data of its group's tiles there in registers
   //   ready[j]  (slot)   wpg arrivals: every K-slice warp filed its partial sums
   //   free[j]   (slot)   1 arrival: the epilogue has consumed the slot
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_offset);
@@ -547,7 +575,7 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, p.wpg * TPS);
+      mbar_init(empty0 + 8u * s, p.groups * p.wpg);
     }
     for (int j = 0; j < nslots; ++j) {
       mbar_init(ready0 + 8u * j, p.wpg);
@@ -619,130 +647,140 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
     const uintptr_t sc_mis = reinterpret_cast<uintptr_t>(p.scales) & 15u;
     const uintptr_t zp_mis = reinterpret_cast<uintptr_t>(p.zp) & 15u;
     const int q_pitch = p.q_pitch, C = p.C, Z = p.Z;
-    // Tile i sits in stage load si = i / TPS at row ti * RC; the load uses
-    // slot s = si % stages for the ph-th time (mod 2).  Kept incrementally:
-    // no division in the loop.
-    int si = g / TPS;
-    int ti = g - si * TPS;
-    int s = si % p.stages;
-    uint32_t ph = static_cast<uint32_t>(si / p.stages) & 1u;
+    // Stage load si (slot s, its ph-th use mod 2) holds tiles
+    // [si * TPS, si * TPS + TPS); this group's tiles are g, g + groups, ...
+    int s = 0;
+    uint32_t ph = 0;
+    int i = g;                                          // this group's next tile
     int t = 0;                                          // this group's tile counter
-    for (int i = g; i < ntiles; ++t) {
+    bool run = true;
+    for (int si = 0; si < nstages && run; ++si) {
       if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) break;
-      const int r0 = row_begin + i * RC;
-      const int nr = min(RC, row_end - r0);
-      const int rin = ti * RC;                          // tile's first row inside the stage
-      const int rs0 = r0 - rin;                         // first row of the stage
-      const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-      // Misalignment offsets chosen by the producer's region copies.
-      const uint32_t sc_off =
-          static_cast<uint32_t>((sc_mis + static_cast<uintptr_t>(rs0) * C * 2) & 15u);
-      const uint32_t zp_off = static_cast<uint32_t>((zp_mis + static_cast<uintptr_t>(rs0) * Z) & 15u);
-      const unsigned char* qp = st + rin * q_pitch + klc / 2;
-      const uint16_t* sp = reinterpret_cast<const uint16_t*>(st + p.q_bytes + sc_off) + rin * C + bl;
-      const unsigned char* zpp = st + p.q_bytes + p.sc_bytes + zp_off + rin * Z + (bl >> 1);
+      const int stage_end = min(ntiles, (si + 1) * TPS);
+      bool held = true;
+      for (; i < stage_end; i += p.groups, ++t) {
+        const int ti = i - si * TPS;
+        const int r0 = row_begin + i * RC;
+        const int nr = min(RC, row_end - r0);
+        const int rin = ti * RC;                          // tile's first row inside the stage
+        const int rs0 = r0 - rin;                         // first row of the stage
+        const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+        // Misalignment offsets chosen by the producer's region copies.
+        const uint32_t sc_off =
+            static_cast<uint32_t>((sc_mis + static_cast<uintptr_t>(rs0) * C * 2) & 15u);
+        const uint32_t zp_off = static_cast<uint32_t>((zp_mis + static_cast<uintptr_t>(rs0) * Z) & 15u);
+        const unsigned char* qp = st + rin * q_pitch + klc / 2;
+        const uint16_t* sp = reinterpret_cast<const uint16_t*>(st + p.q_bytes + sc_off) + rin * C + bl;
+        const unsigned char* zpp = st + p.q_bytes + p.sc_bytes + zp_off + rin * Z + (bl >> 1);
 
-      // Pull this lane's codes, zero-point bytes and scales of every row into
-      // registers and give the stage straight back to the producer.  Rows past
-      // the end of a ragged tile re-read its last row; they are never stored.
-      uint32_t words[RC][kWords];
-      uint32_t zbyte[RC];
-      uint32_t sbits[RC];
+        // Pull this lane's codes, zero-point bytes and scales of every row into
+        // registers and give the stage straight back to the producer.  Rows past
+        // the end of a ragged tile re-read its last row; they are never stored.
+        uint32_t words[RC][kWords];
+        uint32_t zbyte[RC];
+        uint32_t sbits[RC];
 #pragma unroll
-      for (int r = 0; r < RC; ++r) {
-        const int rr = (nr == RC) ? r : min(r, nr - 1);
-        const unsigned char* qrow = qp + rr * q_pitch;
-        if constexpr (kWords == 2) {
-          const uint2 a = *reinterpret_cast<const uint2*>(qrow);
-          words[r][0] = a.x; words[r][1] = a.y;
-        } else {
+        for (int r = 0; r < RC; ++r) {
+          const int rr = (nr == RC) ? r : min(r, nr - 1);
+          const unsigned char* qrow = qp + rr * q_pitch;
+          if constexpr (kWords == 2) {
+            const uint2 a = *reinterpret_cast<const uint2*>(qrow);
+            words[r][0] = a.x; words[r][1] = a.y;
+          } else {
 #pragma unroll
-          for (int h = 0; h < kWords / 4; ++h) {
-            const uint4 a = *reinterpret_cast<const uint4*>(qrow + 16 * h);
-            words[r][4 * h] = a.x; words[r][4 * h + 1] = a.y;
-            words[r][4 * h + 2] = a.z; words[r][4 * h + 3] = a.w;
-          }
-        }
-        zbyte[r] = zpp[rr * Z];
-        if constexpr (kLaneBlocks == 2)
-          sbits[r] = *reinterpret_cast<const uint32_t*>(sp + rr * C);
-        else
-          sbits[r] = sp[rr * C];
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8u * s);
-
-      float v[kVP];
-#pragma unroll
-      for (int j = 0; j < kVP; ++j) v[j] = 0.f;
-#pragma unroll
-      for (int r = 0; r < RC; ++r) {
-        uint32_t zl[kLaneBlocks], zh[kLaneBlocks];
-        float scale[kLaneBlocks];
-        if constexpr (kLaneBlocks == 2) {
-          // Blocks bl (even, low nibble) and bl + 1 (high nibble) share one byte.
-          const uint32_t tz = zbyte[r] * 0x00010001u;
-          zl[0] = and_or(tz, 0x000F000Fu, 0x64006400u);         // 1024 + zp, twice
-          zh[0] = and_or(tz << 4, 0x00F000F0u, 0x54005400u);    //   64 + zp, twice
-          zl[1] = and_or(tz >> 4, 0x000F000Fu, 0x64006400u);
-          zh[1] = and_or(tz, 0x00F000F0u, 0x54005400u);
-          scale[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sbits[r] & 0xFFFFu)));
-          scale[1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sbits[r] >> 16)));
-        } else {
-          const uint32_t tz = zbyte[r] >> zshift;
-          zl[0] = and_or(tz * 0x00010001u, 0x000F000Fu, 0x64006400u);
-          zh[0] = and_or(tz * 0x00100010u, 0x00F000F0u, 0x54005400u);
-          scale[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sbits[r])));
-        }
-        float res[M];
-#pragma unroll
-        for (int m = 0; m < M; ++m) res[m] = 0.f;
-#pragma unroll
-        for (int j = 0; j < kLaneBlocks; ++j) {
-          float acc[M];
-#pragma unroll
-          for (int m = 0; m < M; ++m) acc[m] = 0.f;
-#pragma unroll
-          for (int w = j * kBlockWords; w < (j + 1) * kBlockWords; ++w) {
-            const uint32_t word = words[r][w];
-            const uint32_t w8 = word >> 8;
-            const uint32_t d0 = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl[j]);   // k0, k4
-            const uint32_t d1 = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh[j]);   // k1, k5
-            const uint32_t d2 = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl[j]);     // k2, k6
-            const uint32_t d3 = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh[j]);     // k3, k7
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-              acc[m] = fma2_f16_f32(xr[m][w][0], d0, acc[m]);
-              acc[m] = fma2_f16_f32(xr[m][w][1], d1, acc[m]);
-              acc[m] = fma2_f16_f32(xr[m][w][2], d2, acc[m]);
-              acc[m] = fma2_f16_f32(xr[m][w][3], d3, acc[m]);
+            for (int h = 0; h < kWords / 4; ++h) {
+              const uint4 a = *reinterpret_cast<const uint4*>(qrow + 16 * h);
+              words[r][4 * h] = a.x; words[r][4 * h + 1] = a.y;
+              words[r][4 * h + 2] = a.z; words[r][4 * h + 3] = a.w;
             }
           }
-#pragma unroll
-          for (int m = 0; m < M; ++m) res[m] = fmaf(acc[m], scale[j], res[m]);
+          zbyte[r] = zpp[rr * Z];
+          if constexpr (kLaneBlocks == 2)
+            sbits[r] = *reinterpret_cast<const uint32_t*>(sp + rr * C);
+          else
+            sbits[r] = sp[rr * C];
         }
-#pragma unroll
-        for (int m = 0; m < M; ++m) v[r * M + m] = res[m];
-      }
+        if (i + p.groups >= stage_end) {                  // last tile of this group here
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty0 + 8u * s);
+          held = false;
+        }
 
-      // Warp sum of every (row, m) value; the owning lane files it in this K
-      // slice's part of a reduction slot, which the epilogue warp finishes.
-      const float total = transpose_reduce<kVP>(v, lane);
-      const int idx = lane >> kOwnerShift;
-      const int j = g * kSlotsPerGroup + t % kSlotsPerGroup;
-      if (t >= kSlotsPerGroup &&
-          !mbar_wait(free0 + 8u * j, ((t / kSlotsPerGroup) - 1) & 1, abort_flag, kErrReduceSlot))
-        break;
-      if ((lane & ((1 << kOwnerShift) - 1)) == 0 && idx < kVals)
-        red[(static_cast<size_t>(j) * p.wpg + wg) * kVals + idx] = total;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ready0 + 8u * j);
-      i += p.groups;
-      for (ti += p.groups; ti >= TPS; ti -= TPS) {
-        if (++s == p.stages) {
-          s = 0;
-          ph ^= 1u;
+        float v[kVP];
+#pragma unroll
+        for (int j = 0; j < kVP; ++j) v[j] = 0.f;
+#pragma unroll
+        for (int r = 0; r < RC; ++r) {
+          uint32_t zl[kLaneBlocks], zh[kLaneBlocks];
+          float scale[kLaneBlocks];
+          if constexpr (kLaneBlocks == 2) {
+            // Blocks bl (even, low nibble) and bl + 1 (high nibble) share one byte.
+            const uint32_t tz = zbyte[r] * 0x00010001u;
+            zl[0] = and_or(tz, 0x000F000Fu, 0x64006400u);         // 1024 + zp, twice
+            zh[0] = and_or(tz << 4, 0x00F000F0u, 0x54005400u);    //   64 + zp, twice
+            zl[1] = and_or(tz >> 4, 0x000F000Fu, 0x64006400u);
+            zh[1] = and_or(tz, 0x00F000F0u, 0x54005400u);
+            scale[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sbits[r] & 0xFFFFu)));
+            scale[1] = __half2float(__ushort_as_half(static_cast<unsigned short>(sbits[r] >> 16)));
+          } else {
+            const uint32_t tz = zbyte[r] >> zshift;
+            zl[0] = and_or(tz * 0x00010001u, 0x000F000Fu, 0x64006400u);
+            zh[0] = and_or(tz * 0x00100010u, 0x00F000F0u, 0x54005400u);
+            scale[0] = __half2float(__ushort_as_half(static_cast<unsigned short>(sbits[r])));
+          }
+          float res[M];
+#pragma unroll
+          for (int m = 0; m < M; ++m) res[m] = 0.f;
+#pragma unroll
+          for (int j = 0; j < kLaneBlocks; ++j) {
+            float acc[M];
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[m] = 0.f;
+#pragma unroll
+            for (int w = j * kBlockWords; w < (j + 1) * kBlockWords; ++w) {
+              const uint32_t word = words[r][w];
+              const uint32_t w8 = word >> 8;
+              const uint32_t d0 = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl[j]);   // k0, k4
+              const uint32_t d1 = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh[j]);   // k1, k5
+              const uint32_t d2 = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl[j]);     // k2, k6
+              const uint32_t d3 = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh[j]);     // k3, k7
+#pragma unroll
+              for (int m = 0; m < M; ++m) {
+                acc[m] = fma2_f16_f32(xr[m][w][0], d0, acc[m]);
+                acc[m] = fma2_f16_f32(xr[m][w][1], d1, acc[m]);
+                acc[m] = fma2_f16_f32(xr[m][w][2], d2, acc[m]);
+                acc[m] = fma2_f16_f32(xr[m][w][3], d3, acc[m]);
+              }
+            }
+#pragma unroll
+            for (int m = 0; m < M; ++m) res[m] = fmaf(acc[m], scale[j], res[m]);
+          }
+#pragma unroll
+          for (int m = 0; m < M; ++m) v[r * M + m] = res[m];
         }
+
+        // Warp sum of every (row, m) value; the owning lane files it in this K
+        // slice's part of a reduction slot, which the epilogue warp finishes.
+        const float total = transpose_reduce<kVP>(v, lane);
+        const int idx = lane >> kOwnerShift;
+        const int j = g * kSlotsPerGroup + t % kSlotsPerGroup;
+        if (t >= kSlotsPerGroup &&
+            !mbar_wait(free0 + 8u * j, ((t / kSlotsPerGroup) - 1) & 1, abort_flag, kErrReduceSlot)) {
+          run = false;
+          break;
+        }
+        if ((lane & ((1 << kOwnerShift) - 1)) == 0 && idx < kVals)
+          red[(static_cast<size_t>(j) * p.wpg + wg) * kVals + idx] = total;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ready0 + 8u * j);
+      }
+      if (held) {                                       // no tile of this group here
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8u * s);
+      }
+      if (++s == p.stages) {
+        s = 0;
+        ph ^= 1u;
       }
     }
   }
@@ -766,36 +804,45 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
 
 // ------------------------------------------------------ tensor-core kernel --
 //
-// The multiply-accumulate of M >= 2 runs on the tensor cores (mma.sync
-// m16n8k16, fp16 operands, fp32 accumulation):
+// The multiply-accumulate of small batches runs on the tensor cores
+// (mma.sync m16n8k16, fp16 operands, fp32 accumulation):
 //   A = 16 weight rows x 16 k: lane (g, t) holds code word t (k = 8t..8t+7 of
 //       the block) of rows g and g+8, dequantized exactly to q - zp by the same
 //       lop3 + packed subtraction as the CUDA-core kernel; the word's pairs
 //       (k0,k4) (k1,k5) feed one mma and (k2,k6) (k3,k7) the next, so the two
 //       mmas cover the 32-block.
-//   B = the same 16 k of activation row m = g (zero for g >= M), paired the
-//       same way; the whole activation block is staged once per CTA in shared
-//       memory in this fragment order (16 bytes per lane and block).
+//   B = the same 16 k of activation row m = g (rows g >= M re-read row M - 1;
+//       their D columns are never stored), paired the same way; the whole
+//       activation block is staged once per CTA in shared memory in this
+//       fragment order (16 bytes per lane and block).
 //   D = 16 rows x 8 activation rows, fresh per block, multiplied by the rows'
 //       fp32 scales into fp32 accumulators.
 // Products of fp16 codes and activations are exact in the fp32 accumulate.
 //
-// Work: a CTA owns a contiguous range of 16-row tiles; each tile is cut into
-// `parts` K parts of whole 256-k segments, and each (tile, part) is one stage,
-// loaded by three TMA tensor copies and consumed by the `wpp` warps of that
-// part, each on a fixed run of segments.  Shared-memory layout of a stage:
-//   codes : box {128 B, 16 rows, seg_part segments} of the code matrix viewed
-//           as (byte in segment, row, segment), 128-byte swizzle: chunk j
+// Work: a CTA owns a contiguous range of tiles of R = 16 * tr rows.  A tile
+// is streamed in K steps; step sigma is one stage holding R rows x W_k
+// consecutive 256-k segments (codes, scales, zero-points), loaded by three TMA
+// tensor copies.  Consumer warp (slice ks, sub-tile rho) multiplies rows
+// 16 rho .. 16 rho + 15 by segment ks of every stage, so slice ks owns
+// segments ks, ks + W_k, ...; the epilogue warp sums the W_k slice partials of
+// each output in slice order.  Every consumer warp uses every stage, in
+// order, and arrives on its empty barrier, so a stage is refilled only after
+// all of them have passed it and no parity wait can alias an older phase.
+//
+// Shared-memory layout of a stage:
+//   codes : box {128 B, R rows, W_k segments} of the code matrix viewed as
+//           (byte in segment, row, segment), 128-byte swizzle: chunk j
 //           (block 8s + j) of row r of segment s lands at
-//           (16 s + r) * 128 + 16 * (j ^ (r & 7)), so the eight rows a
+//           (R s + r) * 128 + 16 * (j ^ (r & 7)), so the eight rows a
 //           fragment load touches sit in eight different bank groups.
-//   scales: box {8 scales, sc_sb chunks, 16 rows} of (scale in chunk, chunk,
+//   scales: box {8 scales, sc_sb chunks, R rows} of (scale in chunk, chunk,
 //           row), no swizzle: the 8 scales of segment s of row r at
-//           (r * sc_sb + s) * 16; sc_sb is odd (a chunk past the part is
+//           (r * sc_sb + s) * 16; sc_sb is odd (a chunk past the stage is
 //           loaded or zero-filled) so rows land in different bank groups.
-//   zeros : box {16 B, zp_zb chunks, 16 rows} of (byte, chunk, row): the 4
-//           zero-point bytes of segment s of row r at (r * zp_zb + s / 4) * 16
-//           + 4 (s % 4); zp_zb odd for the same reason.
+//   zeros : box {16 B, zp_zb chunks, R rows} of (byte, chunk, row), starting
+//           at the chunk holding the stage's first segment: the 4 zero-point
+//           bytes of global segment G of row r at
+//           (r * zp_zb + G / 4 - first chunk) * 16 + 4 (G % 4); zp_zb odd.
 // Rows past N are zero-filled by the copies and never stored.
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
@@ -823,21 +870,23 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
   prefetch_tensor_map(tm_sc);
   prefetch_tensor_map(tm_zp);
   if (!p.weights_ready) wait_prerequisites();
-  int issued = 0, s = 0, part = 0, tile = t_begin;
+  const int R = kMmaRows * p.tr;
+  int issued = 0, s = 0, step = 0, tile = t_begin;
   uint32_t ph = 0;
   for (int i = 0; i < nunits; ++i) {
     if (i >= p.stages && !mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, kErrStageFree)) break;
     const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
     const uint32_t bar = full0 + 8u * s;
-    const int row0 = tile * kMmaRows;
+    const int row0 = tile * R;
+    const int seg0 = step * p.wk;
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.tx_bytes));
-    tma_load_3d(st, tm_q, 0, row0, part * p.seg_part, bar);
-    tma_load_3d(st + p.sc_offset, tm_sc, 0, part * p.seg_part, row0, bar);
-    tma_load_3d(st + p.zp_offset, tm_zp, 0, part * (p.seg_part / 4), row0, bar);
+    tma_load_3d(st, tm_q, 0, row0, seg0, bar);
+    tma_load_3d(st + p.sc_offset, tm_sc, 0, seg0, row0, bar);
+    tma_load_3d(st + p.zp_offset, tm_zp, 0, seg0 >> 2, row0, bar);
     issued = i + 1;
-    if (++part == p.parts) {
-      part = 0;
+    if (++step == p.steps) {
+      step = 0;
       ++tile;
     }
     if (++s == p.stages) {
@@ -864,37 +913,37 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     gemv_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_sc,
                     const __grid_constant__ CUtensorMap tm_zp) {
-  constexpr int RC = kMmaRows;
-  constexpr int kVals = RC * M;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the 128-byte swizzle is a function of address bits 7-9: align to 1 KB
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int W = p.wpg;                                 // consumer warps
+  const int W = p.wtc;                                 // consumer warps
   const int producer_warp = W;
   const int epilogue_warp = W + 1;
   const int nslots = kSlotsPerGroup;
+  const int R = kMmaRows * p.tr;                       // rows per tile
+  const int vals = R * M;                              // outputs per tile
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_offset);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * p.stages;
   const uint32_t ready0 = empty0 + 8u * p.stages;
   const uint32_t free0 = ready0 + 8u * nslots;
-  float* red = reinterpret_cast<float*>(smem + p.red_offset);     // [slots][W][16 * M]
+  float* red = reinterpret_cast<float*>(smem + p.red_offset);     // [slots][slices][R * M]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.flag_offset);
 
-  const int tiles = (p.N + RC - 1) / RC;
+  const int tiles = (p.N + R - 1) / R;
   const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * tiles) / gridDim.x);
   const int t_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * tiles) / gridDim.x);
   const int ntiles = t_end - t_begin;
-  const int row_begin = t_begin * RC;
-  const int row_end = min(p.N, t_end * RC);
+  const int row_begin = t_begin * R;
+  const int row_end = min(p.N, t_end * R);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, p.wpp);
+      mbar_init(empty0 + 8u * s, W);
     }
     for (int j = 0; j < nslots; ++j) {
       mbar_init(ready0 + 8u * j, W);
@@ -908,24 +957,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   if (warp == producer_warp) {
     if (lane == 0)
-      run_tc_producer(p, smem, full0, empty0, abort_flag, t_begin, ntiles * p.parts, &tm_q,
+      run_tc_producer(p, smem, full0, empty0, abort_flag, t_begin, ntiles * p.steps, &tm_q,
                       &tm_sc, &tm_zp);
     __syncwarp();
     return;
   }
   if (warp == epilogue_warp) {
-    run_epilogue(p, red, nullptr, ready0, free0, abort_flag, row_begin, row_end, RC, ntiles, M,
+    // p.wpg is the number of K-slice partials per output here
+    run_epilogue(p, red, nullptr, ready0, free0, abort_flag, row_begin, row_end, R, ntiles, M,
                  lane);
     return;
   }
 
   // ------------------------------------------------------------- consumers --
-  const int part = warp / p.wpp;
-  const int wi = warp - part * p.wpp;
-  const int s0 = (wi * p.seg_part) / p.wpp;            // this warp's segments [s0, s1)
-  const int s1 = ((wi + 1) * p.seg_part) / p.wpp;      //   of its part
-  const int gq = lane >> 2;                            // fragment row group
-  const int tq = lane & 3;                             // fragment k group
+  const int ks = warp / p.tr;                               // K slice (segment in a stage)
+  const int rho = warp - ks * p.tr;                         // 16-row sub-tile
+  const int gq = lane >> 2;                                 // fragment row group
+  const int tq = lane & 3;                                  // fragment k group
+  const int row_l = rho * kMmaRows + gq;                    // fragment row in the tile
 
   // Activation fragments: row m, block b, k group tq -> 16 bytes at
   // xp + m * xp_pitch + b * 64 + tq * 16 holding x[m][32b + 8tq + {0..7}]
@@ -933,71 +982,80 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   wait_prerequisites();
   unsigned char* xp = smem + p.xp_offset;
   {
+    // 8 activations (one k group of a block) per element; K is a multiple of
+    // 1024, so every row starts 16-byte aligned when x does.
     const int total = M * p.C * 4;
-    for (int e = threadIdx.x; e < total; e += W * 32) {
-      const int m = e / (p.C * 4);
-      const int rem = e - m * p.C * 4;
-      const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + 8 * rem;
-      uint16_t h[8];
-      if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
-        h[0] = v.x & 0xFFFF; h[1] = v.x >> 16; h[2] = v.y & 0xFFFF; h[3] = v.y >> 16;
-        h[4] = v.z & 0xFFFF; h[5] = v.z >> 16; h[6] = v.w & 0xFFFF; h[7] = v.w >> 16;
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) h[k] = __ldg(src + k);
+    const int per_row = p.C * 4;
+    if ((reinterpret_cast<uintptr_t>(p.x) & 15u) == 0) {
+      for (int e = threadIdx.x; e < total; e += W * 32) {
+        const int m = e / per_row;
+        const int rem = e - m * per_row;
+        const uint4 v =
+            __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K) + rem);
+        *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + rem * 16) = pair_k4(v);
       }
-      uint4 out;
-      out.x = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[4]) << 16);
-      out.y = static_cast<uint32_t>(h[1]) | (static_cast<uint32_t>(h[5]) << 16);
-      out.z = static_cast<uint32_t>(h[2]) | (static_cast<uint32_t>(h[6]) << 16);
-      out.w = static_cast<uint32_t>(h[3]) | (static_cast<uint32_t>(h[7]) << 16);
-      *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + rem * 16) = out;
+    } else {
+      for (int e = threadIdx.x; e < total; e += W * 32) {
+        const int m = e / per_row;
+        const int rem = e - m * per_row;
+        const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + 8 * rem;
+        uint4 v;
+        v.x = __ldg(src + 0) | (static_cast<uint32_t>(__ldg(src + 1)) << 16);
+        v.y = __ldg(src + 2) | (static_cast<uint32_t>(__ldg(src + 3)) << 16);
+        v.z = __ldg(src + 4) | (static_cast<uint32_t>(__ldg(src + 5)) << 16);
+        v.w = __ldg(src + 6) | (static_cast<uint32_t>(__ldg(src + 7)) << 16);
+        *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + rem * 16) = pair_k4(v);
+      }
     }
     // all consumer warps (named barrier 1; producer and epilogue do not take part)
     asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
   }
-  const unsigned char* xfrag = xp + min(gq, M - 1) * p.xp_pitch +
-                               (part * p.seg_part + s0) * 512 + tq * 16;
-  const bool x_lane = gq < M;
+  // Lanes of activation rows gq >= M read row M - 1: their D columns are
+  // never stored.
+  const unsigned char* xfrag = xp + min(gq, M - 1) * p.xp_pitch + ks * 512 + tq * 16;
 
-  // Lane offsets inside a stage.  Codes: row gq of segment s, chunk j at
-  // s * 2048 + gq * 128 + 16 * (j ^ gq) + 4 tq; row gq + 8 is 1024 bytes on.
+  // Lane offsets inside a stage, the same for every stage.  Codes: row row_l
+  // of segment ks, chunk j at (R ks + row_l) * 128 + 16 * (j ^ gq) + 4 tq;
+  // row row_l + 8 is 1024 bytes on.
   uint32_t qoff[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) qoff[j] = gq * 128 + 16 * (j ^ gq) + 4 * tq;
-  const int sc_lane = p.sc_offset + gq * p.sc_sb * 16;
-  const int sc_hi = 8 * p.sc_sb * 16;                  // row gq + 8
-  const int zp_lane = p.zp_offset + gq * p.zp_zb * 16;
+  for (int j = 0; j < 8; ++j) qoff[j] = (R * ks + row_l) * 128 + 16 * (j ^ gq) + 4 * tq;
+  const int sc_lane = p.sc_offset + (row_l * p.sc_sb + ks) * 16;
+  const int sc_hi = 8 * p.sc_sb * 16;                      // row row_l + 8
+  const int zp_lane = p.zp_offset + row_l * p.zp_zb * 16;
   const int zp_hi = 8 * p.zp_zb * 16;
 
-  int s = part;                                        // stage of unit (t * parts + part)
+  int s = 0;                                               // stage of the next unit
   uint32_t ph = 0;
-  for (int t = 0; t < ntiles; ++t) {
-    if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) break;
-    const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+  bool run = true;
+  for (int t = 0; t < ntiles && run; ++t) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int sg = s0; sg < s1; ++sg) {
-      const unsigned char* qs = st + sg * 2048;
-      const uint4 sca = *reinterpret_cast<const uint4*>(st + sc_lane + sg * 16);
-      const uint4 scb = *reinterpret_cast<const uint4*>(st + sc_lane + sc_hi + sg * 16);
-      const int zo = zp_lane + (sg >> 2) * 16 + (sg & 3) * 4;
+    const unsigned char* xs = xfrag;
+    for (int step = 0; step < p.steps; ++step, xs += p.wk * 512) {
+      if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) {
+        run = false;
+        break;
+      }
+      const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+      const uint4 sca = *reinterpret_cast<const uint4*>(st + sc_lane);
+      const uint4 scb = *reinterpret_cast<const uint4*>(st + sc_lane + sc_hi);
+      const int seg0 = step * p.wk;                        // the stage's first segment
+      const int G = seg0 + ks;                             // this warp's segment
+      const int zo = zp_lane + ((G >> 2) - (seg0 >> 2)) * 16 + (G & 3) * 4;
       const uint32_t zwa = *reinterpret_cast<const uint32_t*>(st + zo);
       const uint32_t zwb = *reinterpret_cast<const uint32_t*>(st + zo + zp_hi);
-      const unsigned char* xs = xfrag + (sg - s0) * 512;
       const uint32_t scw_a[4] = {sca.x, sca.y, sca.z, sca.w};
       const uint32_t scw_b[4] = {scb.x, scb.y, scb.z, scb.w};
 #pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {                 // block pair (2 jp, 2 jp + 1)
+      for (int jp = 0; jp < 4; ++jp) {                     // block pair (2 jp, 2 jp + 1)
         const ZpPairs z0 = zp_pairs(zp_byte_pair(zwa, jp));
         const ZpPairs z1 = zp_pairs(zp_byte_pair(zwb, jp));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int j = 2 * jp + h;
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(qs + qoff[j]);
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(qs + qoff[j] + 1024);
-          uint4 xf = make_uint4(0u, 0u, 0u, 0u);
-          if (x_lane) xf = *reinterpret_cast<const uint4*>(xs + 64 * j);
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(st + qoff[j]);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(st + qoff[j] + 1024);
+          const uint4 xf = *reinterpret_cast<const uint4*>(xs + 64 * j);
           const float sa = half_word_to_float(scw_a[jp], h);
           const float sb = half_word_to_float(scw_b[jp], h);
           if (h == 0)
@@ -1006,31 +1064,31 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             mma_block(acc, w0, w1, xf, z0.lo_o, z0.hi_o, z1.lo_o, z1.hi_o, sa, sb);
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8u * s);
+      if (++s == p.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8u * s);
+    if (!run) break;
 
     const int j = t % nslots;
     if (t >= nslots && !mbar_wait(free0 + 8u * j, ((t / nslots) - 1) & 1, abort_flag,
                                   kErrReduceSlot))
       break;
-    float* slot = red + (static_cast<size_t>(j) * W + warp) * kVals;
+    float* slot = red + (static_cast<size_t>(j) * p.wpg + ks) * vals;
     const int m0 = 2 * tq;
     if (m0 < M) {
-      slot[gq * M + m0] = acc[0];
-      slot[(gq + 8) * M + m0] = acc[2];
+      slot[row_l * M + m0] = acc[0];
+      slot[(row_l + 8) * M + m0] = acc[2];
     }
     if (m0 + 1 < M) {
-      slot[gq * M + m0 + 1] = acc[1];
-      slot[(gq + 8) * M + m0 + 1] = acc[3];
+      slot[row_l * M + m0 + 1] = acc[1];
+      slot[(row_l + 8) * M + m0 + 1] = acc[3];
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(ready0 + 8u * j);
-    s += p.parts;                                      // this part of the next tile
-    while (s >= p.stages) {
-      s -= p.stages;
-      ph ^= 1u;
-    }
   }
 }
 
@@ -1230,12 +1288,12 @@ int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, const Kerne
 int mma_x_pitch(int C) { return C * 64 + ((C & 1) ? 0 : 64); }
 int mma_x_bytes(int M, int C) { return M * mma_x_pitch(C); }
 
-// The tensor-core kernel takes M >= 2 without a K split when K is a multiple
-// of 1024 (whole 256-k segments and 16-byte zero-point rows for the tensor
-// copies), scales and zero-points are 16-byte aligned, and the activation
-// fragments fit in kMmaXBytes.
+// The tensor-core kernel (only on request) takes a launch without a K split
+// when K is a multiple of 1024 (whole 256-k segments and 16-byte zero-point
+// rows for the tensor copies), scales and zero-points are 16-byte aligned,
+// and the activation fragments fit in kMmaXBytes.
 bool use_mma(int M, int K, int split, const void* scales, const void* zp) {
-  return M >= 2 && split == 1 && K % 1024 == 0 && K <= 65536 &&
+  return split == 1 && K % 1024 == 0 && K <= 65536 &&
          (reinterpret_cast<uintptr_t>(scales) & 15u) == 0 &&
          (reinterpret_cast<uintptr_t>(zp) & 15u) == 0 && mma_x_bytes(M, K / kBlock) <= kMmaXBytes;
 }
@@ -1258,9 +1316,11 @@ MmaFn pick_mma_kernel(int M) {
 int round_up(int v, int a) { return (v + a - 1) / a * a; }
 int odd_at_least(int v) { return v | 1; }
 
-// Stage layout and K split of the tensor-core kernel: the fewest K parts per
-// tile that still leave at least four stages in shared memory (more parts
-// mean smaller stages released by fewer warps each).
+// Tile shape and stage layout of the tensor-core kernel.  Sub-tiles per tile
+// (tr): the largest whose makespan, in 16-row tiles per CTA, is within 5% of
+// the best and that keeps as many SMs busy; K slices: the largest divisor of
+// K / 256 up to 16 / tr (at least 4 where K allows, so a stage's zero-point
+// chunk is never re-read).  A stage always holds about 32 KB of codes.
 int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, Plan* plan) {
   Params& p = plan->p;
   p.M = M;
@@ -1270,46 +1330,53 @@ int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, Plan* plan) {
   p.Z = (p.C + 1) / 2;
   p.split = 1;
   p.groups = 1;
-  const int segs = K / kMmaSeg;
+  const int S = K / kMmaSeg;
   const int nslots = kSlotsPerGroup;
   p.xp_pitch = mma_x_pitch(p.C);
   const int x_bytes = mma_x_bytes(M, p.C);
   const int budget = static_cast<int>(dev.smem_optin) - 1024;   // 1 KB for the alignment
-  int best = -1;
-  for (int parts = 1; parts <= 8; parts *= 2) {
-    if (segs % parts || (segs / parts) % 4 || segs / parts + 1 > 256) continue;
-    const int seg_part = segs / parts;
-    const int wpp = std::min(kMmaWarps / parts, seg_part);
-    const int W = wpp * parts;
-    const int q_bytes = kMmaRows * seg_part * 128;
-    const int sc_sb = odd_at_least(seg_part);
-    const int zp_zb = odd_at_least(seg_part / 4);
-    const int sc_bytes = round_up(kMmaRows * sc_sb * 16, 128);
-    const int zp_bytes = round_up(kMmaRows * zp_zb * 16, 128);
-    const int stage_bytes = round_up(q_bytes + sc_bytes + zp_bytes, 1024);
-    const int red_bytes = round_up(nslots * W * kMmaRows * M * 4, 16);
-    const int fixed = x_bytes + red_bytes + 8 * 2 * nslots + 16;
-    const int stages = std::min(kMaxStages, (budget - fixed) / (stage_bytes + 16));
-    if (stages < std::max(2, parts)) continue;
-    best = parts;
-    p.parts = parts;
-    p.seg_part = seg_part;
-    p.wpp = wpp;
-    p.wpg = W;
-    p.sc_sb = sc_sb;
-    p.zp_zb = zp_zb;
-    p.q_bytes = q_bytes;
-    p.sc_offset = q_bytes;
-    p.sc_bytes = sc_bytes;
-    p.zp_offset = q_bytes + sc_bytes;
-    p.zp_bytes = zp_bytes;
-    p.tx_bytes = kMmaRows * (seg_part * 128 + sc_sb * 16 + zp_zb * 16);
-    p.stage_bytes = stage_bytes;
-    p.stages = stages;
-    if (stages >= 4) break;
+  const long long tiles16 = (static_cast<long long>(N) + kMmaRows - 1) / kMmaRows;
+  const long long sms = std::max(1, dev.sms);
+  auto makespan = [&](int tr) {
+    const long long ct = (tiles16 + tr - 1) / tr;
+    return ((ct + sms - 1) / sms) * tr;
+  };
+  long long best = makespan(1);
+  for (int tr = 2; tr <= 4; tr *= 2) best = std::min(best, makespan(tr));
+  int tr = 1;
+  long long used_best = -1;
+  for (int c = 4; c >= 1; c /= 2) {
+    if (makespan(c) * 100 > best * 105) continue;
+    const long long used = std::min(sms, (tiles16 + c - 1) / c);
+    if (used > used_best) {
+      used_best = used;
+      tr = c;
+    }
   }
-  if (best < 0) return fail(MNB_ERR_SHAPE, "shape needs more shared memory than one SM has");
-  const int red_bytes = round_up(nslots * p.wpg * kMmaRows * M * 4, 16);
+  int wk = std::min(kMmaWarps / tr, S);
+  while (S % wk) --wk;
+  const int R = kMmaRows * tr;
+  int zspan = 1;                                   // zero-point chunks one stage spans
+  for (int st = 0; st < S / wk; ++st)
+    zspan = std::max(zspan, (((st + 1) * wk - 1) >> 2) - ((st * wk) >> 2) + 1);
+  p.tr = tr;
+  p.wk = wk;
+  p.steps = S / wk;
+  p.wtc = wk * tr;
+  p.wpg = wk;                                      // partials per output for the epilogue
+  p.sc_sb = odd_at_least(wk);
+  p.zp_zb = odd_at_least(zspan);
+  p.q_bytes = R * wk * 128;
+  p.sc_bytes = round_up(R * p.sc_sb * 16, 128);
+  p.zp_bytes = round_up(R * p.zp_zb * 16, 128);
+  p.sc_offset = p.q_bytes;
+  p.zp_offset = p.q_bytes + p.sc_bytes;
+  p.tx_bytes = R * (wk * 128 + p.sc_sb * 16 + p.zp_zb * 16);
+  p.stage_bytes = round_up(p.q_bytes + p.sc_bytes + p.zp_bytes, 1024);
+  const int red_bytes = round_up(nslots * wk * R * M * 4, 16);
+  const int fixed = x_bytes + red_bytes + 8 * 2 * nslots + 16;
+  p.stages = std::min(kMaxStages, (budget - fixed) / (p.stage_bytes + 16));
+  if (p.stages < 2) return fail(MNB_ERR_SHAPE, "shape needs more shared memory than one SM has");
   int off = p.stages * p.stage_bytes;
   p.xp_offset = off;
   off += x_bytes;
@@ -1320,10 +1387,10 @@ int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, Plan* plan) {
   p.part_offset = off;
   p.flag_offset = off;
   off += 16;
-  const long long tiles = (static_cast<long long>(N) + kMmaRows - 1) / kMmaRows;
+  const long long tiles = (static_cast<long long>(N) + R - 1) / R;
   plan->smem = static_cast<size_t>(off) + 1024;
-  plan->grid = dim3(static_cast<unsigned>(std::max<long long>(1, std::min<long long>(dev.sms, tiles))));
-  plan->block = dim3(static_cast<unsigned>((p.wpg + 2) * 32));
+  plan->grid = dim3(static_cast<unsigned>(std::max<long long>(1, std::min<long long>(sms, tiles))));
+  plan->block = dim3(static_cast<unsigned>((p.wtc + 2) * 32));
   return MNB_OK;
 }
 
@@ -1332,7 +1399,7 @@ int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, Plan* plan) {
 // The three views the tensor-core kernel copies from (see its layout notes),
 // encoded with the driver's cuTensorMapEncodeTiled (fetched once through the
 // runtime, no link-time dependence on libcuda).  A map depends only on the
-// array's address, N, K and the part count, so encoded maps are kept in a
+// array's address, N, K and the tile shape (tr, wk), so encoded maps are kept in a
 // small cache: static weights are encoded once.
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -1342,7 +1409,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 
 struct MapEntry {
   const void* ptr = nullptr;
-  int kind = -1, N = 0, K = 0, parts = 0;
+  int kind = -1, N = 0, K = 0, tr = 0, wk = 0;
   CUtensorMap map;
 };
 
@@ -1364,7 +1431,8 @@ int encode_map(MapKind kind, const void* ptr, const Params& p, CUtensorMap* out)
     // (byte in segment, row, segment): rows K/2 bytes apart, segments 128
     const cuuint64_t dims[3] = {128, N, K / kMmaSeg};
     const cuuint64_t strides[2] = {K / 2, 128};
-    const cuuint32_t box[3] = {128, kMmaRows, static_cast<cuuint32_t>(p.seg_part)};
+    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(kMmaRows * p.tr),
+                               static_cast<cuuint32_t>(p.wk)};
     r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, ones,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1372,7 +1440,8 @@ int encode_map(MapKind kind, const void* ptr, const Params& p, CUtensorMap* out)
     // (scale in 8-scale chunk, chunk, row)
     const cuuint64_t dims[3] = {8, K / 256, N};
     const cuuint64_t strides[2] = {16, K / 16};
-    const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(p.sc_sb), kMmaRows};
+    const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(p.sc_sb),
+                               static_cast<cuuint32_t>(kMmaRows * p.tr)};
     r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, base, dims, strides, box, ones,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1380,7 +1449,8 @@ int encode_map(MapKind kind, const void* ptr, const Params& p, CUtensorMap* out)
     // (byte in 16-byte chunk, chunk, row)
     const cuuint64_t dims[3] = {16, K / 1024, N};
     const cuuint64_t strides[2] = {16, K / 64};
-    const cuuint32_t box[3] = {16, static_cast<cuuint32_t>(p.zp_zb), kMmaRows};
+    const cuuint32_t box[3] = {16, static_cast<cuuint32_t>(p.zp_zb),
+                               static_cast<cuuint32_t>(kMmaRows * p.tr)};
     r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, ones,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1402,7 +1472,8 @@ int tensor_map(MapKind kind, const void* ptr, const Params& p, CUtensorMap* out)
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
   for (const MapEntry& m : g_maps)
-    if (m.ptr == ptr && m.kind == kind && m.N == p.N && m.K == p.K && m.parts == p.parts) {
+    if (m.ptr == ptr && m.kind == kind && m.N == p.N && m.K == p.K && m.tr == p.tr &&
+        m.wk == p.wk) {
       *out = m.map;
       return MNB_OK;
     }
@@ -1416,7 +1487,8 @@ int tensor_map(MapKind kind, const void* ptr, const Params& p, CUtensorMap* out)
   slot.kind = kind;
   slot.N = p.N;
   slot.K = p.K;
-  slot.parts = p.parts;
+  slot.tr = p.tr;
+  slot.wk = p.wk;
   g_map_next = (g_map_next + 1) % kMapCache;
   *out = slot.map;
   return MNB_OK;
@@ -1487,7 +1559,7 @@ int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const ui
 int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                    void* y, int M, int N, int K, int block, int out_dtype, int split_k,
                    unsigned int flags, void* stream) {
-  if (flags & ~static_cast<unsigned int>(MNB_FLAG_WEIGHTS_READY))
+  if (flags & ~static_cast<unsigned int>(MNB_FLAG_WEIGHTS_READY | MNB_FLAG_TENSOR_CORES))
     return fail(MNB_ERR_FLAGS, "unknown flag bits");
   if (!x || !qweight || !scales || !zp || !y) return fail(MNB_ERR_NULL, "x, qweight, scales, zp and y are required");
   if (block != kBlock) return fail(MNB_ERR_BLOCK, "only block size 32 is supported");
@@ -1516,7 +1588,7 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   if ((st = device_info(&dev)) != MNB_OK) return st;
   const int split = split_k == 0 ? auto_split(M, N, K, dev.sms) : split_k;
 
-  bool mma = use_mma(M, K, split, scales, zp);
+  bool mma = (flags & MNB_FLAG_TENSOR_CORES) && use_mma(M, K, split, scales, zp);
   const KernelShape ks = pick_shape(M, K / kBlock, split, scales);
   Plan plan{};
   if (mma && make_mma_plan(dev, M, N, K, &plan) != MNB_OK) {

@@ -70,10 +70,11 @@ def test_host_validation(lib, kw, status):
 
 
 def test_unknown_flags_rejected(lib):
-    st = lib.mnb_gemv_flags(X, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, 2, None)
+    st = lib.mnb_gemv_flags(X, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, 4, None)
     assert st == 10
     # valid flags fall through to the ordinary checks (here: a NULL pointer)
     assert lib.mnb_gemv_flags(0, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, 1, None) == 1
+    assert lib.mnb_gemv_flags(0, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, 3, None) == 1
 
 
 def test_split_limits(lib):

@@ -51,13 +51,14 @@ def sample_cols(N, rng, n=384):
     return np.unique(np.r_[edge, rng.choice(N, size=min(N, n), replace=False)]).astype(np.int64)
 
 
+@pytest.mark.parametrize("tc", [False, True], ids=["default", "tensor_cores"])
 @pytest.mark.parametrize("name", list(WORKLOADS))
-def test_workload_full_size(name):
+def test_workload_full_size(name, tc):
     w = WORKLOADS[name]
     inp = make_inputs(w.M, w.N, w.K, seed=0)
     dev = _gpu.to_device(inp)
-    y16 = _gpu.bits(_gpu.run(dev, "f16"))
-    ybf = _gpu.bits(_gpu.run(dev, "bf16"))
+    y16 = _gpu.bits(_gpu.run(dev, "f16", tensor_cores=tc))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16", tensor_cores=tc))
     # every element written (the NaN sentinel is gone) in both arms
     o = _gpu.oracle()
     assert not np.isnan(o.f16_to_f64(y16)).any()
@@ -97,19 +98,47 @@ def test_counters_prove_the_kernel_ran():
     assert d[0] == 2 and d[1] == 1 and d[2] == 1 and d[3] == 1 and d[4 + 2 - 1] == 2
 
 
-def test_tensor_core_kernel_runs_for_small_batches():
-    """M >= 2 without a K split runs the tensor-core kernel; a K split or M = 1
-    runs the CUDA-core kernel.  Both meet the bound."""
-    for M, N, split, want in ((4, 130, 1, 1), (2, 4096, 0, 1), (8, 130, 1, 1), (4, 130, 2, 0),
-                              (1, 130, 1, 0)):
-        inp = make_inputs(M, N, 4096, seed=M + split)
+def test_tensor_core_kernel_only_on_request():
+    """The tensor-core kernel runs only with the tensor_cores flag, and then
+    only where it applies (no K split, K a multiple of 1024); every launch
+    meets the bound."""
+    for M, N, K, split, tc, want in ((4, 130, 4096, 1, True, 1), (2, 4096, 4096, 1, True, 1),
+                                     (1, 130, 4096, 1, True, 1), (8, 130, 4096, 1, True, 1),
+                                     (4, 130, 4096, 2, True, 0), (2, 130, 4096, 1, False, 0),
+                                     (1, 4096, 4096, 0, False, 0), (2, 75, 288, 1, True, 0)):
+        inp = make_inputs(M, N, K, seed=M + split + K)
         dev = _gpu.to_device(inp)
         before = mnb.counters()[12]
-        y16 = _gpu.bits(_gpu.run(dev, "f16", split))
-        ybf = _gpu.bits(_gpu.run(dev, "bf16", split))
-        assert mnb.counters()[12] - before == 2 * want, (M, split)
+        y16 = _gpu.bits(_gpu.run(dev, "f16", split, tensor_cores=tc))
+        ybf = _gpu.bits(_gpu.run(dev, "bf16", split, tensor_cores=tc))
+        assert mnb.counters()[12] - before == 2 * want, (M, N, K, split, tc)
         cols = None if N <= 256 else np.arange(0, N, 7)
         _gpu.compare(inp, y16, ybf, cols=cols)
+
+
+TC_SHAPES = [(1, 1024), (17, 1024), (130, 2048), (33, 3072), (300, 5120), (19, 8192)]
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("N,K", TC_SHAPES)
+def test_tensor_core_small_shapes(M, N, K):
+    """Ragged N (partial tiles zero-filled by the tensor copies) and every K
+    layout the tensor-core kernel takes (1 to 8 stages per tile, odd and even
+    slice counts)."""
+    if mnb_x_bytes(M, K) > 66 * 1024:
+        pytest.skip("activations too large for the tensor-core kernel")
+    inp = make_inputs(M, N, K, seed=300 + M * 11 + N + K)
+    dev = _gpu.to_device(inp)
+    before = mnb.counters()[12]
+    y16 = _gpu.bits(_gpu.run(dev, "f16", 1, tensor_cores=True))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16", 1, tensor_cores=True))
+    assert mnb.counters()[12] - before == 2
+    _gpu.compare(inp, y16, ybf)
+
+
+def mnb_x_bytes(M, K):
+    C = K // 32
+    return M * (C * 64 + (0 if C & 1 else 64))
 
 
 def test_all_zero_weight_rows_give_exact_zero():
@@ -122,9 +151,10 @@ def test_all_zero_weight_rows_give_exact_zero():
         q[::2] = 0x77                      # every code 7 in even rows
         zp[::2] = 0x77                     # every zero-point 7 in even rows
         inp.qweight, inp.zp = q, zp
-        y16 = _gpu.bits(_gpu.run(_gpu.to_device(inp), "f16", 1))
-        assert np.all((y16[:, ::2] & 0x7FFF) == 0)
-        _gpu.compare(inp, y16, None)
+        for tc in (False, True):
+            y16 = _gpu.bits(_gpu.run(_gpu.to_device(inp), "f16", 1, tensor_cores=tc))
+            assert np.all((y16[:, ::2] & 0x7FFF) == 0)
+            _gpu.compare(inp, y16, None)
 
 
 def test_misaligned_pointers():
@@ -172,13 +202,13 @@ def test_cuda_graph_capture_matches_eager():
     assert torch.equal(eager.view(torch.int16), y.view(torch.int16))
 
 
-def test_non_finite_inputs_follow_ieee():
-    M, N, K = 1, 16, 64
+@pytest.mark.parametrize("M,N,K,tc", [(1, 16, 64, False), (2, 40, 1024, True)])
+def test_non_finite_inputs_follow_ieee(M, N, K, tc):
     inp = make_inputs(M, N, K, seed=2)
     xs = inp.x.copy()
     xs[0, 3] = 0x7C00          # +inf
     inp.x = xs
-    y16 = _gpu.bits(_gpu.run(_gpu.to_device(inp), "f16"))
+    y16 = _gpu.bits(_gpu.run(_gpu.to_device(inp), "f16", 1, tensor_cores=tc))
     ref = _gpu.oracle().gemv(inp.x, inp.qweight, inp.scales, inp.zp, M, N, K)
     o = _gpu.oracle()
     g, r = o.f16_to_f64(y16), o.f16_to_f64(ref["y_f16"])
@@ -186,7 +216,8 @@ def test_non_finite_inputs_follow_ieee():
     assert np.array_equal(g[np.isinf(r)], r[np.isinf(r)])
 
 
-def test_weights_ready_chain_matches_plain_calls():
+@pytest.mark.parametrize("tc", [False, True], ids=["default", "tensor_cores"])
+def test_weights_ready_chain_matches_plain_calls(tc):
     """Back-to-back calls with the early-weights promise (programmatic
     dependent launch) give the same bits as plain calls, also when each call's
     activations are the previous call's output."""
@@ -194,11 +225,11 @@ def test_weights_ready_chain_matches_plain_calls():
     x, q, s, z = _gpu.to_device(inp)
     ref = [x]
     for i in range(4):
-        ref.append(mnb.gemv(ref[-1], q, s, z, "f16"))
+        ref.append(mnb.gemv(ref[-1], q, s, z, "f16", tensor_cores=tc))
     torch.cuda.synchronize()
     got = [x]
     for i in range(4):
-        got.append(mnb.gemv(got[-1], q, s, z, "f16", weights_ready=True))
+        got.append(mnb.gemv(got[-1], q, s, z, "f16", weights_ready=True, tensor_cores=tc))
     torch.cuda.synchronize()
     for a, b in zip(ref[1:], got[1:]):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))

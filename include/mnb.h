@@ -140,8 +140,11 @@ int mnb_gemv_flags(const void *x, const uint8_t *qweight, const void *scales, co
                    void *y, int M, int N, int K, int block, int out_dtype, int split_k,
                    unsigned int flags, void *stream);
 
-/* split_k that mnb_gemv uses for split_k = 0 on the current device.
- * Writes it to *split_k.  Same shape checks and statuses as mnb_gemv. */
+/* split_k that mnb_gemv uses for split_k = 0 on the current device, for
+ * 16-byte aligned scales and zp and without MNB_FLAG_TENSOR_CORES (1 whenever
+ * the step kernel takes the launch: K a multiple of 1024, M <= 3, M * K at
+ * most 33792).  Writes it to *split_k.  Same shape checks and statuses as
+ * mnb_gemv. */
 int mnb_split_k_auto(int M, int N, int K, int *split_k);
 
 /* Smallest split_k mnb_gemv accepts for this M and K (one CTA covers at most
@@ -170,10 +173,11 @@ int mnb_device_error(void *stream, unsigned int *code, int clear);
 /* Launch counters, for tests that must prove the GPU kernel ran:
  *   [0] launches, [1] fp16-output launches, [2] bf16-output launches,
  *   [3] launches with split_k > 1 (cluster reduction), [4 + M - 1] launches
- *   with M rows (M = 1..8), [12] launches of the tensor-core kernel (only
- *   with MNB_FLAG_TENSOR_CORES).
+ *   with M rows (M = 1..8), [12] launches with tensor-core math (only with
+ *   MNB_FLAG_TENSOR_CORES), [13] launches of the step kernel (either math:
+ *   tiles streamed in K steps by TMA tensor copies, no K split).
  * Copies min(n, MNB_NUM_COUNTERS) counters to out; returns how many. */
-#define MNB_NUM_COUNTERS 13
+#define MNB_NUM_COUNTERS 14
 int mnb_debug_counters(uint64_t *out, int n);
 void mnb_debug_counters_reset(void);
 

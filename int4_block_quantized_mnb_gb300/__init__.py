@@ -11,7 +11,7 @@ from __future__ import annotations
 import ctypes
 
 from ._native import (BLOCK, FLAG_TENSOR_CORES, FLAG_WEIGHTS_READY, MAX_M, MAX_SPLIT_K,
-                      OUT_BF16, OUT_F16,
+                      NUM_COUNTERS, OUT_BF16, OUT_F16,
                       MnbError, check, load)
 
 __all__ = ["gemv", "gemv_ptr", "split_k_auto", "min_split_k", "max_split_k", "counters",
@@ -108,8 +108,8 @@ def max_split_k(K: int) -> int:
 
 
 def counters() -> list:
-    buf = (ctypes.c_uint64 * 13)()
-    n = load().mnb_debug_counters(buf, 13)
+    buf = (ctypes.c_uint64 * NUM_COUNTERS)()
+    n = load().mnb_debug_counters(buf, NUM_COUNTERS)
     return [int(buf[i]) for i in range(n)]
 
 

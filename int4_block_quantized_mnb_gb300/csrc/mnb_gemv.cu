@@ -908,9 +908,9 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
   }
 }
 
-template <int M>
+template <int M, bool kMma>
 __global__ void __launch_bounds__(kMmaThreads, 1)
-    gemv_mma_kernel(const Params p, const __grid_constant__ CUtensorMap tm_q,
+    gemv_step_kernel(const Params p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_sc,
                     const __grid_constant__ CUtensorMap tm_zp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -972,15 +972,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   // ------------------------------------------------------------- consumers --
   const int ks = warp / p.tr;                               // K slice (segment in a stage)
   const int rho = warp - ks * p.tr;                         // 16-row sub-tile
-  const int gq = lane >> 2;                                 // fragment row group
-  const int tq = lane & 3;                                  // fragment k group
-  const int row_l = rho * kMmaRows + gq;                    // fragment row in the tile
 
-  // Activation fragments: row m, block b, k group tq -> 16 bytes at
-  // xp + m * xp_pitch + b * 64 + tq * 16 holding x[m][32b + 8tq + {0..7}]
-  // paired (0,4) (1,5) (2,6) (3,7).  The consumer warps fill it together.
+  // Activations, staged once per CTA by the consumer warps: row m, block b,
+  // k group tq -> 16 bytes holding x[m][32b + 8tq + {0..7}] paired (0,4)
+  // (1,5) (2,6) (3,7), at xp + m * xp_pitch + b * 64 + tq * 16 (the B
+  // fragments of the tensor-core math) or + tq * C * 16 + b * 16 (CUDA-core
+  // math: eight lanes read eight consecutive blocks).
   wait_prerequisites();
   unsigned char* xp = smem + p.xp_offset;
+  auto x_off = [&](int rem) {
+    return kMma ? rem * 16 : ((rem & 3) * p.C + (rem >> 2)) * 16;
+  };
   {
     // 8 activations (one k group of a block) per element; K is a multiple of
     // 1024, so every row starts 16-byte aligned when x does.
@@ -992,7 +994,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const int rem = e - m * per_row;
         const uint4 v =
             __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K) + rem);
-        *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + rem * 16) = pair_k4(v);
+        *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + x_off(rem)) = pair_k4(v);
       }
     } else {
       for (int e = threadIdx.x; e < total; e += W * 32) {
@@ -1004,91 +1006,204 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         v.y = __ldg(src + 2) | (static_cast<uint32_t>(__ldg(src + 3)) << 16);
         v.z = __ldg(src + 4) | (static_cast<uint32_t>(__ldg(src + 5)) << 16);
         v.w = __ldg(src + 6) | (static_cast<uint32_t>(__ldg(src + 7)) << 16);
-        *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + rem * 16) = pair_k4(v);
+        *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + x_off(rem)) = pair_k4(v);
       }
     }
     // all consumer warps (named barrier 1; producer and epilogue do not take part)
     asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
   }
-  // Lanes of activation rows gq >= M read row M - 1: their D columns are
-  // never stored.
-  const unsigned char* xfrag = xp + min(gq, M - 1) * p.xp_pitch + ks * 512 + tq * 16;
+  if constexpr (kMma) {
+    const int gq = lane >> 2;                               // fragment row group
+    const int tq = lane & 3;                                // fragment k group
+    const int row_l = rho * kMmaRows + gq;                  // fragment row in the tile
+    // Lanes of activation rows gq >= M read row M - 1: their D columns are
+    // never stored.
+    const unsigned char* xfrag = xp + min(gq, M - 1) * p.xp_pitch + ks * 512 + tq * 16;
 
-  // Lane offsets inside a stage, the same for every stage.  Codes: row row_l
-  // of segment ks, chunk j at (R ks + row_l) * 128 + 16 * (j ^ gq) + 4 tq;
-  // row row_l + 8 is 1024 bytes on.
-  uint32_t qoff[8];
+    // Lane offsets inside a stage, the same for every stage.  Codes: row row_l
+    // of segment ks, chunk j at (R ks + row_l) * 128 + 16 * (j ^ gq) + 4 tq;
+    // row row_l + 8 is 1024 bytes on.
+    uint32_t qoff[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) qoff[j] = (R * ks + row_l) * 128 + 16 * (j ^ gq) + 4 * tq;
-  const int sc_lane = p.sc_offset + (row_l * p.sc_sb + ks) * 16;
-  const int sc_hi = 8 * p.sc_sb * 16;                      // row row_l + 8
-  const int zp_lane = p.zp_offset + row_l * p.zp_zb * 16;
-  const int zp_hi = 8 * p.zp_zb * 16;
+    for (int j = 0; j < 8; ++j) qoff[j] = (R * ks + row_l) * 128 + 16 * (j ^ gq) + 4 * tq;
+    const int sc_lane = p.sc_offset + (row_l * p.sc_sb + ks) * 16;
+    const int sc_hi = 8 * p.sc_sb * 16;                      // row row_l + 8
+    const int zp_lane = p.zp_offset + row_l * p.zp_zb * 16;
+    const int zp_hi = 8 * p.zp_zb * 16;
 
-  int s = 0;                                               // stage of the next unit
-  uint32_t ph = 0;
-  bool run = true;
-  for (int t = 0; t < ntiles && run; ++t) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const unsigned char* xs = xfrag;
-    for (int step = 0; step < p.steps; ++step, xs += p.wk * 512) {
-      if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) {
-        run = false;
-        break;
-      }
-      const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-      const uint4 sca = *reinterpret_cast<const uint4*>(st + sc_lane);
-      const uint4 scb = *reinterpret_cast<const uint4*>(st + sc_lane + sc_hi);
-      const int seg0 = step * p.wk;                        // the stage's first segment
-      const int G = seg0 + ks;                             // this warp's segment
-      const int zo = zp_lane + ((G >> 2) - (seg0 >> 2)) * 16 + (G & 3) * 4;
-      const uint32_t zwa = *reinterpret_cast<const uint32_t*>(st + zo);
-      const uint32_t zwb = *reinterpret_cast<const uint32_t*>(st + zo + zp_hi);
-      const uint32_t scw_a[4] = {sca.x, sca.y, sca.z, sca.w};
-      const uint32_t scw_b[4] = {scb.x, scb.y, scb.z, scb.w};
+    int s = 0;                                               // stage of the next unit
+    uint32_t ph = 0;
+    bool run = true;
+    for (int t = 0; t < ntiles && run; ++t) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const unsigned char* xs = xfrag;
+      for (int step = 0; step < p.steps; ++step, xs += p.wk * 512) {
+        if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) {
+          run = false;
+          break;
+        }
+        const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+        const uint4 sca = *reinterpret_cast<const uint4*>(st + sc_lane);
+        const uint4 scb = *reinterpret_cast<const uint4*>(st + sc_lane + sc_hi);
+        const int seg0 = step * p.wk;                        // the stage's first segment
+        const int G = seg0 + ks;                             // this warp's segment
+        const int zo = zp_lane + ((G >> 2) - (seg0 >> 2)) * 16 + (G & 3) * 4;
+        const uint32_t zwa = *reinterpret_cast<const uint32_t*>(st + zo);
+        const uint32_t zwb = *reinterpret_cast<const uint32_t*>(st + zo + zp_hi);
+        const uint32_t scw_a[4] = {sca.x, sca.y, sca.z, sca.w};
+        const uint32_t scw_b[4] = {scb.x, scb.y, scb.z, scb.w};
 #pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {                     // block pair (2 jp, 2 jp + 1)
-        const ZpPairs z0 = zp_pairs(zp_byte_pair(zwa, jp));
-        const ZpPairs z1 = zp_pairs(zp_byte_pair(zwb, jp));
+        for (int jp = 0; jp < 4; ++jp) {                     // block pair (2 jp, 2 jp + 1)
+          const ZpPairs z0 = zp_pairs(zp_byte_pair(zwa, jp));
+          const ZpPairs z1 = zp_pairs(zp_byte_pair(zwb, jp));
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int j = 2 * jp + h;
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(st + qoff[j]);
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(st + qoff[j] + 1024);
-          const uint4 xf = *reinterpret_cast<const uint4*>(xs + 64 * j);
-          const float sa = half_word_to_float(scw_a[jp], h);
-          const float sb = half_word_to_float(scw_b[jp], h);
-          if (h == 0)
-            mma_block(acc, w0, w1, xf, z0.lo_e, z0.hi_e, z1.lo_e, z1.hi_e, sa, sb);
-          else
-            mma_block(acc, w0, w1, xf, z0.lo_o, z0.hi_o, z1.lo_o, z1.hi_o, sa, sb);
+          for (int h = 0; h < 2; ++h) {
+            const int j = 2 * jp + h;
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(st + qoff[j]);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(st + qoff[j] + 1024);
+            const uint4 xf = *reinterpret_cast<const uint4*>(xs + 64 * j);
+            const float sa = half_word_to_float(scw_a[jp], h);
+            const float sb = half_word_to_float(scw_b[jp], h);
+            if (h == 0)
+              mma_block(acc, w0, w1, xf, z0.lo_e, z0.hi_e, z1.lo_e, z1.hi_e, sa, sb);
+            else
+              mma_block(acc, w0, w1, xf, z0.lo_o, z0.hi_o, z1.lo_o, z1.hi_o, sa, sb);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8u * s);
+        if (++s == p.stages) {
+          s = 0;
+          ph ^= 1u;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8u * s);
-      if (++s == p.stages) {
-        s = 0;
-        ph ^= 1u;
-      }
-    }
-    if (!run) break;
+      if (!run) break;
 
-    const int j = t % nslots;
-    if (t >= nslots && !mbar_wait(free0 + 8u * j, ((t / nslots) - 1) & 1, abort_flag,
-                                  kErrReduceSlot))
-      break;
-    float* slot = red + (static_cast<size_t>(j) * p.wpg + ks) * vals;
-    const int m0 = 2 * tq;
-    if (m0 < M) {
-      slot[row_l * M + m0] = acc[0];
-      slot[(row_l + 8) * M + m0] = acc[2];
+      const int j = t % nslots;
+      if (t >= nslots && !mbar_wait(free0 + 8u * j, ((t / nslots) - 1) & 1, abort_flag,
+                                    kErrReduceSlot))
+        break;
+      float* slot = red + (static_cast<size_t>(j) * p.wpg + ks) * vals;
+      const int m0 = 2 * tq;
+      if (m0 < M) {
+        slot[row_l * M + m0] = acc[0];
+        slot[(row_l + 8) * M + m0] = acc[2];
+      }
+      if (m0 + 1 < M) {
+        slot[row_l * M + m0 + 1] = acc[1];
+        slot[(row_l + 8) * M + m0 + 1] = acc[3];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ready0 + 8u * j);
     }
-    if (m0 + 1 < M) {
-      slot[row_l * M + m0 + 1] = acc[1];
-      slot[(row_l + 8) * M + m0 + 1] = acc[3];
+  } else {
+    // CUDA-core math.  Lane (rg, j) = (lane >> 3, lane & 7) takes block j of
+    // the warp's segment of every stage for rows 16 rho + rg + 4 i, i = 0..3:
+    // one 16-byte code load per row, exact q - zp pairs, and fp32 accumulation
+    // of the fp16 products (fma.rn.f32.f16); each block sum is scaled into the
+    // row's accumulator.  A tile ends with a butterfly over the eight lanes of
+    // a row and one partial per (row, m) for the epilogue.
+    const int j = lane & 7;
+    const int rg = lane >> 3;
+    const uint32_t zsh = (j & 1) * 4;                     // this block's nibble in its zp byte
+    int qo[4], so[4], zo[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = rho * kMmaRows + rg + 4 * i;
+      qo[i] = (R * ks + r) * 128 + 16 * (j ^ (r & 7));
+      so[i] = p.sc_offset + (r * p.sc_sb + ks) * 16 + 2 * j;
+      zo[i] = p.zp_offset + r * p.zp_zb * 16 + (j >> 1);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(ready0 + 8u * j);
+    const unsigned char* xl = xp + j * 16;
+    const int kg_pitch = p.C * 16;                        // bytes per k group of a row
+    int s = 0;
+    uint32_t ph = 0;
+    bool run = true;
+    for (int t = 0; t < ntiles && run; ++t) {
+      float acc[4][M];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
+      for (int step = 0; step < p.steps; ++step) {
+        if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) {
+          run = false;
+          break;
+        }
+        const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+        const int seg0 = step * p.wk;
+        const int G = seg0 + ks;                            // this warp's segment
+        const int zb = ((G >> 2) - (seg0 >> 2)) * 16 + (G & 3) * 4;
+        const unsigned char* xb = xl + G * 128;             // block 8 G + j
+        uint4 xr[M][4];
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            xr[m][g] = *reinterpret_cast<const uint4*>(xb + m * p.xp_pitch + g * kg_pitch);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 w = *reinterpret_cast<const uint4*>(st + qo[i]);
+          const uint32_t z = (static_cast<uint32_t>(st[zo[i] + zb]) >> zsh) & 0xFu;
+          const uint32_t zl = and_or(z * 0x00010001u, 0x000F000Fu, 0x64006400u);   // 1024 + zp
+          const uint32_t zh = and_or(z * 0x00100010u, 0x00F000F0u, 0x54005400u);   //   64 + zp
+          const float sc = half_word_to_float(*reinterpret_cast<const uint16_t*>(st + so[i]), 0);
+          const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+          float bs[M];
+#pragma unroll
+          for (int m = 0; m < M; ++m) bs[m] = 0.f;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t word = words[g];
+            const uint32_t w8 = word >> 8;
+            const uint32_t d0 = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl);   // k0, k4
+            const uint32_t d1 = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh);   // k1, k5
+            const uint32_t d2 = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl);     // k2, k6
+            const uint32_t d3 = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh);     // k3, k7
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+              bs[m] = fma2_f16_f32(xr[m][g].x, d0, bs[m]);
+              bs[m] = fma2_f16_f32(xr[m][g].y, d1, bs[m]);
+              bs[m] = fma2_f16_f32(xr[m][g].z, d2, bs[m]);
+              bs[m] = fma2_f16_f32(xr[m][g].w, d3, bs[m]);
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < M; ++m) acc[i][m] = fmaf(bs[m], sc, acc[i][m]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8u * s);
+        if (++s == p.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!run) break;
+      // the eight blocks of each row's segment, in a fixed butterfly order
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          float v = acc[i][m];
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+          acc[i][m] = v;
+        }
+      const int js = t % nslots;
+      if (t >= nslots && !mbar_wait(free0 + 8u * js, ((t / nslots) - 1) & 1, abort_flag,
+                                    kErrReduceSlot))
+        break;
+      if (j == 0) {
+        float* slot = red + (static_cast<size_t>(js) * p.wpg + ks) * vals;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int m = 0; m < M; ++m) slot[(rho * kMmaRows + rg + 4 * i) * M + m] = acc[i][m];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ready0 + 8u * js);
+    }
   }
 }
 
@@ -1282,34 +1397,51 @@ int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, const Kerne
   return MNB_OK;
 }
 
-// Activation fragments of the tensor-core kernel: 64 bytes per block and row;
-// a row pitch of 64 mod 128 bytes puts two activation rows (4 lanes x 16
-// bytes each) in one shared-memory wavefront.
+// Staged activations of the step kernel: 64 bytes per block and row; a row
+// pitch of 64 mod 128 bytes puts two activation rows (4 lanes x 16 bytes
+// each) in one shared-memory wavefront of the tensor-core fragment loads.
 int mma_x_pitch(int C) { return C * 64 + ((C & 1) ? 0 : 64); }
 int mma_x_bytes(int M, int C) { return M * mma_x_pitch(C); }
 
-// The tensor-core kernel (only on request) takes a launch without a K split
-// when K is a multiple of 1024 (whole 256-k segments and 16-byte zero-point
-// rows for the tensor copies), scales and zero-points are 16-byte aligned,
-// and the activation fragments fit in kMmaXBytes.
-bool use_mma(int M, int K, int split, const void* scales, const void* zp) {
-  return split == 1 && K % 1024 == 0 && K <= 65536 &&
+// The step kernel takes a launch without a K split (split_k 0 or 1) when K
+// is a multiple of 1024 (whole 256-k segments and 16-byte zero-point rows for
+// the tensor copies), scales and zero-points are 16-byte aligned and the
+// staged activations fit in kMmaXBytes: with CUDA-core math for M <= 3
+// (activation registers; M = 4 spills), with tensor-core math for any M on
+// request.
+constexpr int kStepFmaMaxM = 3;
+
+bool step_shape(int M, int K, bool tensor_cores) {
+  return K % 1024 == 0 && K <= 65536 && mma_x_bytes(M, K / kBlock) <= kMmaXBytes &&
+         (tensor_cores || M <= kStepFmaMaxM);
+}
+
+bool use_step(int M, int K, int split_k, const void* scales, const void* zp,
+              bool tensor_cores) {
+  return (split_k == 0 || split_k == 1) && step_shape(M, K, tensor_cores) &&
          (reinterpret_cast<uintptr_t>(scales) & 15u) == 0 &&
-         (reinterpret_cast<uintptr_t>(zp) & 15u) == 0 && mma_x_bytes(M, K / kBlock) <= kMmaXBytes;
+         (reinterpret_cast<uintptr_t>(zp) & 15u) == 0;
 }
 
 using MmaFn = void (*)(const Params, const CUtensorMap, const CUtensorMap, const CUtensorMap);
 
-MmaFn pick_mma_kernel(int M) {
+MmaFn pick_step_kernel(int M, bool mma) {
+  if (mma) {
+    switch (M) {
+      case 1: return &gemv_step_kernel<1, true>;
+      case 2: return &gemv_step_kernel<2, true>;
+      case 3: return &gemv_step_kernel<3, true>;
+      case 4: return &gemv_step_kernel<4, true>;
+      case 5: return &gemv_step_kernel<5, true>;
+      case 6: return &gemv_step_kernel<6, true>;
+      case 7: return &gemv_step_kernel<7, true>;
+      default: return &gemv_step_kernel<8, true>;
+    }
+  }
   switch (M) {
-    case 1: return &gemv_mma_kernel<1>;
-    case 2: return &gemv_mma_kernel<2>;
-    case 3: return &gemv_mma_kernel<3>;
-    case 4: return &gemv_mma_kernel<4>;
-    case 5: return &gemv_mma_kernel<5>;
-    case 6: return &gemv_mma_kernel<6>;
-    case 7: return &gemv_mma_kernel<7>;
-    default: return &gemv_mma_kernel<8>;
+    case 1: return &gemv_step_kernel<1, false>;
+    case 2: return &gemv_step_kernel<2, false>;
+    default: return &gemv_step_kernel<3, false>;
   }
 }
 
@@ -1547,7 +1679,7 @@ int mnb_split_k_auto(int M, int N, int K, int* split_k) {
   if (st != MNB_OK) return st;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != MNB_OK) return st;
-  *split_k = auto_split(M, N, K, dev.sms);
+  *split_k = step_shape(M, K, false) ? 1 : auto_split(M, N, K, dev.sms);
   return MNB_OK;
 }
 
@@ -1586,16 +1718,17 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
                                     std::to_string(hi) + "] for this M and K");
   DeviceInfo dev;
   if ((st = device_info(&dev)) != MNB_OK) return st;
-  const int split = split_k == 0 ? auto_split(M, N, K, dev.sms) : split_k;
-
-  bool mma = (flags & MNB_FLAG_TENSOR_CORES) && use_mma(M, K, split, scales, zp);
-  const KernelShape ks = pick_shape(M, K / kBlock, split, scales);
+  const bool tc = (flags & MNB_FLAG_TENSOR_CORES) != 0;
+  bool step = use_step(M, K, split_k, scales, zp, tc);
   Plan plan{};
-  if (mma && make_mma_plan(dev, M, N, K, &plan) != MNB_OK) {
-    mma = false;                                  // no stage layout fits: CUDA-core kernel
+  if (step && make_mma_plan(dev, M, N, K, &plan) != MNB_OK) {
+    step = false;                                 // no stage layout fits: row-tile kernel
     plan = Plan{};
   }
-  if (!mma && (st = make_plan(dev, M, N, K, split, ks, &plan)) != MNB_OK) return st;
+  const bool mma = step && tc;
+  const int split = step ? 1 : (split_k == 0 ? auto_split(M, N, K, dev.sms) : split_k);
+  const KernelShape ks = pick_shape(M, K / kBlock, split, scales);
+  if (!step && (st = make_plan(dev, M, N, K, split, ks, &plan)) != MNB_OK) return st;
   Params& p = plan.p;
   p.x = static_cast<const uint16_t*>(x);
   p.q = qweight;
@@ -1606,14 +1739,14 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   p.weights_ready = (flags & MNB_FLAG_WEIGHTS_READY) ? 1 : 0;
 
   CUtensorMap maps[3];
-  if (mma) {
+  if (step) {
     if ((st = tensor_map(kMapCodes, qweight, p, &maps[0])) != MNB_OK ||
         (st = tensor_map(kMapScales, scales, p, &maps[1])) != MNB_OK ||
         (st = tensor_map(kMapZeros, zp, p, &maps[2])) != MNB_OK)
       return st;
   }
-  const void* fn = mma ? reinterpret_cast<const void*>(pick_mma_kernel(M))
-                       : reinterpret_cast<const void*>(pick_kernel(M, ks));
+  const void* fn = step ? reinterpret_cast<const void*>(pick_step_kernel(M, mma))
+                        : reinterpret_cast<const void*>(pick_kernel(M, ks));
   cudaError_t e = cudaFuncSetAttribute(fn,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.smem));
@@ -1644,6 +1777,7 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   if (split > 1) g_counters[3].fetch_add(1, std::memory_order_relaxed);
   g_counters[4 + M - 1].fetch_add(1, std::memory_order_relaxed);
   if (mma) g_counters[12].fetch_add(1, std::memory_order_relaxed);
+  if (step) g_counters[13].fetch_add(1, std::memory_order_relaxed);
   return MNB_OK;
 }
 

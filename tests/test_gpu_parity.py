@@ -116,6 +116,27 @@ def test_tensor_core_kernel_only_on_request():
         _gpu.compare(inp, y16, ybf, cols=cols)
 
 
+def test_step_kernel_takes_default_launches():
+    """Without a K split, K a multiple of 1024 and M <= 3 run the step kernel
+    (TMA tensor copies, CUDA-core math); other launches run the row-tile
+    kernel.  No default launch uses tensor-core math."""
+    for M, N, K, split, want in ((1, 4096, 4096, 0, 1), (2, 300, 8192, 1, 1), (4, 130, 4096, 0, 0),
+                                 (3, 77, 1024, 1, 1), (5, 130, 4096, 0, 0), (2, 130, 4096, 2, 0),
+                                 (1, 75, 288, 0, 0)):
+        inp = make_inputs(M, N, K, seed=M * 3 + split + K)
+        dev = _gpu.to_device(inp)
+        c0 = mnb.counters()
+        y16 = _gpu.bits(_gpu.run(dev, "f16", split))
+        ybf = _gpu.bits(_gpu.run(dev, "bf16", split))
+        c1 = mnb.counters()
+        assert c1[13] - c0[13] == 2 * want, (M, N, K, split)
+        assert c1[12] == c0[12]
+        if want:
+            assert mnb.split_k_auto(M, N, K) == 1
+        cols = None if N <= 256 else np.arange(0, N, 5)
+        _gpu.compare(inp, y16, ybf, cols=cols)
+
+
 TC_SHAPES = [(1, 1024), (17, 1024), (130, 2048), (33, 3072), (300, 5120), (19, 8192)]
 
 

@@ -172,12 +172,20 @@ def oracle_sample(w, inp, seconds, threads):
     rate = probe.size / max(time.perf_counter() - t0, 1e-6)          # columns per second
     ncols = int(max(threads, min(w.N, rate * seconds)))
     cols = rng.choice(w.N, size=ncols, replace=False).astype(np.int64)
+    # whole passes over the sample until about `seconds` have elapsed
+    passes = 0
     t0 = time.perf_counter()
-    o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=cols, threads=threads)
-    dt = time.perf_counter() - t0
-    gbs = w.algorithmic_bytes() * n_calls * (ncols / w.N) / dt / 1e9
-    desc = (f"{ncols} of {w.N} output columns (all {w.M} rows, full K={w.K}), one pass producing "
-            f"the fp16 and bf16 results, {dt:.1f} s on {threads} threads")
+    while True:
+        o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=cols, threads=threads)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= 0.9 * seconds:
+            break
+    gbs = w.algorithmic_bytes() * n_calls * passes * (ncols / w.N) / dt / 1e9
+    what = (f"{passes} passes over all {w.N} output columns" if passes > 1 else
+            f"{ncols} of {w.N} output columns")
+    desc = (f"{what} (all {w.M} rows, full K={w.K}), each pass producing the fp16 and bf16 "
+            f"results, {dt:.1f} s on {threads} threads")
     return gbs, desc, dt
 
 

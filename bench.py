@@ -52,7 +52,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["mnb", "reference"], default="mnb")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--split-k", type=int, default=0)
+    ap.add_argument("--split-k", type=int, default=0,
+                    help="0 = the library's choice (as a user calling with split_k=0 gets)")
+    ap.add_argument("--tensor-cores", action="store_true",
+                    help="permit the tensor-core kernel (MNB_FLAG_TENSOR_CORES)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -282,7 +285,8 @@ def main():
     R = max(L, math.ceil(4 * l2 / wbytes))
     R = int(math.ceil(R / L) * L)
     copies = [(q0, s0, z0)] + [(q0.clone(), s0.clone(), z0.clone()) for _ in range(R - 1)]
-    split_k = args.split_k if args.split_k else mnb.split_k_auto(w.M, w.N, w.K)
+    split_k = args.split_k
+    tc = bool(args.tensor_cores)
     stream = torch.cuda.Stream(dev)
 
     def step(j):
@@ -290,7 +294,7 @@ def main():
         for i, o in enumerate(outs):
             q, s, z = copies[(j * L + i) % R]
             mnb.gemv(x, q, s, z, out_dtype=o, split_k=split_k, y=ys[o], stream=stream,
-                     weights_ready=True)
+                     weights_ready=True, tensor_cores=tc)
 
     # Warm-up: W eager steps.
     with torch.cuda.stream(stream):
@@ -367,7 +371,8 @@ def main():
             ds.copy_(hs, non_blocking=True)
             dz.copy_(hz, non_blocking=True)
             for o in outs:
-                mnb.gemv(dx, dq, ds, dz, out_dtype=o, split_k=split_k, y=ys[o], stream=stream)
+                mnb.gemv(dx, dq, ds, dz, out_dtype=o, split_k=split_k, y=ys[o], stream=stream,
+                         tensor_cores=tc)
                 hy[o].copy_(ys[o], non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -396,7 +401,8 @@ def main():
         "us_per_call": per_launch_s * 1e6,
         "pct_of_hbm_peak": 100.0 * achieved / peak,
         "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "out_dtypes": outs,
-                   "split_k": split_k, "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "split_k": split_k if split_k else "auto", "tensor_cores": tc,
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"inputs larger than L2: {R} rotating weight copies, "
                          f"{R * wbytes / 2**20:.0f} MiB vs L2 {l2 / 2**20:.0f} MiB",
                    "timing": f"CUDA events around {full} replays of a {G}-step graph"
@@ -404,7 +410,7 @@ def main():
                              + "; warm-up: W eager steps, then one untimed replay per graph"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": recorded_traffic(w.name),
+                     "traffic": None if tc else recorded_traffic(w.name),
                      "algorithmic_bytes_per_launch": bytes_call},
         "cpu_baseline": cpu,
         "e2e": e2e,

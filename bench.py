@@ -28,6 +28,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -66,6 +67,25 @@ def parse():
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
             int(os.environ.get("WORLD_SIZE", "1")))
+
+
+DATASHEET_HBM_GBS = 8000.0      # GB300 HBM3e, ~8 TB/s (the datasheet figure used here)
+
+
+def pct(sorted_vals, q):
+    """Nearest-rank percentile of an ascending list."""
+    i = min(len(sorted_vals) - 1, max(0, int(round(q / 100.0 * (len(sorted_vals) - 1)))))
+    return sorted_vals[i]
+
+
+def fma_bound(w, props, clk):
+    """The non-tensor FP32 FMA bound of an M > 1 call: M*N*K FMAs at SMs x 128
+    FP32 lanes x the maximum SM clock seen (derived, not measured)."""
+    mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+    rate = props.multi_processor_count * 128 * mhz * 1e6          # FMA/s
+    fmas = w.M * w.N * w.K
+    return {"fmas_per_launch": fmas, "tfma_per_s": rate / 1e12, "us": fmas / rate * 1e6,
+            "rate_source": f"{props.multi_processor_count} SMs x 128 FP32 lanes x {mhz:.0f} MHz"}
 
 
 def measured_peaks():
@@ -162,6 +182,23 @@ class ClockSampler:
 
 # ------------------------------------------------------------- CPU oracle --
 
+def cpu_model():
+    """Host CPU description from /proc/cpuinfo (model name, or the Arm part)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return platform.machine()
+    fields = {}
+    for line in info:
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    parts = [f"{k} {fields[k]}" for k in ("CPU implementer", "CPU part") if k in fields]
+    return f"{platform.machine()} ({', '.join(parts)})" if parts else platform.machine()
+
+
 def oracle_sample(w, inp, seconds, threads):
     """Times the CPU oracle on about `seconds` of work: a sample of output
     columns of the workload.  Returns (GB/s, description, threads used)."""
@@ -257,7 +294,9 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         gbs, desc, _ = oracle_sample(w, inp, args.cpu_seconds, threads)
-        cpu = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+        gbs1, desc1, _ = oracle_sample(w, inp, args.cpu_seconds / 2, 1)
+        cpu = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+               "single_thread": {"value": gbs1, "sample": desc1}, "cpu_model": cpu_model()}
 
     import torch
     import int4_block_quantized_mnb_gb300 as mnb
@@ -328,17 +367,20 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    ev0 = torch.cuda.Event(enable_timing=True)
+    # one event between consecutive replays: the spread of per-call times
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(full + 1)]
     ev1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(full):
+        evs[0].record(stream)
+        for i in range(full):
             g_main.replay()
+            evs[i + 1].record(stream)
         if g_rem is not None:
             g_rem.replay()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
-    t_ms = ev0.elapsed_time(ev1)
+    t_ms = evs[0].elapsed_time(ev1)
+    per_call_us = sorted(evs[i].elapsed_time(evs[i + 1]) * 1e3 / (G * L) for i in range(full))
     clk = clocks.stop()
     if world > 1:
         t = torch.tensor([t_ms], device=dev)
@@ -399,6 +441,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "us_per_call": per_launch_s * 1e6,
+        "us_per_call_p10_p50_p90": ([pct(per_call_us, q) for q in (10, 50, 90)]
+                                    if per_call_us else None),
         "pct_of_hbm_peak": 100.0 * achieved / peak,
         "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "out_dtypes": outs,
                    "split_k": split_k if split_k else "auto", "tensor_cores": tc,
@@ -411,7 +455,10 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": None if tc else recorded_traffic(w.name),
-                     "algorithmic_bytes_per_launch": bytes_call},
+                     "algorithmic_bytes_per_launch": bytes_call,
+                     "peak_datasheet": DATASHEET_HBM_GBS,
+                     "frac_datasheet": achieved / DATASHEET_HBM_GBS,
+                     "fma_bound": fma_bound(w, props, clk) if w.M > 1 else None},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,

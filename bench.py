@@ -57,6 +57,9 @@ def parse():
                     help="0 = the library's choice (as a user calling with split_k=0 gets)")
     ap.add_argument("--tensor-cores", action="store_true",
                     help="permit the tensor-core kernel (MNB_FLAG_TENSOR_CORES)")
+    ap.add_argument("--ab-staged", action="store_true",
+                    help="time a synthetic decode step of bf16 GEMVs: fp16 GEMV + separate "
+                         "narrowing launch (staged route) against the direct bf16 store")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -278,8 +281,113 @@ def run_reference(args, w):
 
 # --------------------------------------------------------------- GPU arm --
 
+# A synthetic decoder layer at hidden size 4096 (q, k, v, o, fused gate_up,
+# down; grouped k/v of 1024; intermediate 12288), M = 1: the GEMVs of one
+# decode step of a bf16 model, for the staged-route A/B.
+AB_LAYERS = 4
+AB_LAYER = [("q", 4096, 4096), ("k", 4096, 1024), ("v", 4096, 1024), ("o", 4096, 4096),
+            ("gate_up", 4096, 24576), ("down", 12288, 4096)]
+
+
+def run_ab_staged(args):
+    """The staged route (fp16 GEMV into a staging buffer, then the separate
+    narrowing launch) against the GEMV's direct bf16 store, over the GEMVs of
+    AB_LAYERS synthetic decoder layers, each route captured in one CUDA graph."""
+    rank, local_rank, world = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    import int4_block_quantized_mnb_gb300 as mnb
+    from int4_block_quantized_mnb_gb300.synth import make_inputs
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    mnb.load()
+
+    def to_dev(a, dtype):
+        return torch.from_numpy(a.view(np.int16).copy() if a.dtype == np.uint16 else a).view(
+            dtype).to(dev)
+
+    gemvs = []
+    wbytes = 0
+    for layer in range(AB_LAYERS):
+        for i, (name, K, N) in enumerate(AB_LAYER):
+            inp = make_inputs(1, N, K, seed=1000 * layer + i)
+            g = dict(name=f"{name}{layer}", K=K, N=N, x=to_dev(inp.x, torch.float16),
+                     q=to_dev(inp.qweight, torch.uint8), s=to_dev(inp.scales, torch.float16),
+                     z=to_dev(inp.zp, torch.uint8),
+                     y16=torch.empty((1, N), dtype=torch.float16, device=dev),
+                     ybf=torch.empty((1, N), dtype=torch.bfloat16, device=dev))
+            wbytes += g["q"].numel() + 2 * g["s"].numel() + g["z"].numel()
+            gemvs.append(g)
+    stream = torch.cuda.Stream(dev)
+    tc = bool(args.tensor_cores)
+
+    def staged():
+        for g in gemvs:
+            mnb.gemv(g["x"], g["q"], g["s"], g["z"], "f16", y=g["y16"], stream=stream,
+                     weights_ready=True, tensor_cores=tc)
+            mnb.cast_f16_to_bf16(g["y16"], g["ybf"], stream=stream)
+
+    def direct():
+        for g in gemvs:
+            mnb.gemv(g["x"], g["q"], g["s"], g["z"], "bf16", y=g["ybf"], stream=stream,
+                     weights_ready=True, tensor_cores=tc)
+
+    def casts():
+        for g in gemvs:
+            mnb.cast_f16_to_bf16(g["y16"], g["ybf"], stream=stream)
+
+    def timed(fn, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                fn()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    reps = max(20, args.steps if args.steps < 100000 else 200)
+    us_direct = timed(direct, reps)
+    us_staged = timed(staged, reps)
+    us_casts = timed(casts, reps)
+    # the staged route's bits equal the direct store's
+    staged()
+    torch.cuda.synchronize(dev)
+    same = all(torch.equal(g["ybf"].view(torch.int16), mnb.cast_f16_to_bf16(g["y16"]).view(
+        torch.int16)) for g in gemvs)
+    n = len(gemvs)
+    line = {
+        "metric": "decode step us: staged fp16 GEMV + narrowing launch vs direct bf16 store",
+        "unit": "us", "higher_is_better": False, "data": "synthetic", "n_gpus": 1,
+        "config": {"workload": f"decode-step-{AB_LAYERS}x-h4096-kv1024-i12288-m1",
+                   "gemvs_per_step": n, "weight_bytes": wbytes, "tensor_cores": tc,
+                   "timing": f"CUDA events around {reps} replays of one graph per route"},
+        "direct": {"us_per_step": us_direct, "launches_per_step": n},
+        "staged": {"us_per_step": us_staged, "launches_per_step": 2 * n},
+        "narrowing_launches_alone_us_per_step": us_casts,
+        "saved_us_per_step": us_staged - us_direct,
+        "saved_pct": 100.0 * (us_staged - us_direct) / us_staged,
+        "staged_bits_equal_direct": bool(same),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.ab_staged:
+        return run_ab_staged(args)
     from int4_block_quantized_mnb_gb300.synth import WORKLOADS, make_inputs
     if args.workload not in WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {list(WORKLOADS)}")

@@ -47,7 +47,8 @@ extern "C" {
 /* Output element type of mnb_gemv. */
 typedef enum mnb_out_dtype {
     MNB_OUT_F16 = 0,   /* y holds the fp16 result */
-    MNB_OUT_BF16 = 1   /* y holds bf16( fp16 result ), i.e. double-rounded */
+    MNB_OUT_BF16 = 1   /* y holds bf16( fp16 result ), i.e. double-rounded; an fp16
+                          NaN becomes the quiet bf16 NaN 0x7FC0 with its sign */
 } mnb_out_dtype;
 
 typedef enum mnb_status {
@@ -140,6 +141,20 @@ int mnb_gemv_flags(const void *x, const uint8_t *qweight, const void *scales, co
                    void *y, int M, int N, int K, int block, int out_dtype, int split_k,
                    unsigned int flags, void *stream);
 
+/*
+ * mnb_cast_f16_to_bf16 -- dst[i] = bf16(src[i]) for n elements: fp16 -> fp32
+ * exactly, then round-to-nearest-even to bf16 (a NaN becomes the quiet NaN
+ * 0x7FC0 with its sign), the same narrowing mnb_gemv's bf16 output applies.  It is the separate
+ * narrowing launch of the staged route ("perf(cuda): let the split-K decode
+ * GEMV store bf16 directly", onnx-genai PR 1550, paragraphs 1-3), provided to
+ * measure that route against the direct bf16 store.
+ *   src, dst  device arrays of n 16-bit values, 2-byte aligned (16-byte
+ *             alignment of both is faster); dst may equal src (in place) but
+ *             must not otherwise overlap it.
+ * n = 0 launches nothing.  Asynchronous on `stream`; MNB_OK once enqueued.
+ */
+int mnb_cast_f16_to_bf16(const void *src, void *dst, size_t n, void *stream);
+
 /* split_k that mnb_gemv uses for split_k = 0 on the current device, for
  * 16-byte aligned scales and zp and without MNB_FLAG_TENSOR_CORES (1 whenever
  * the step kernel takes the launch: K a multiple of 1024, M <= 3, M * K at
@@ -175,9 +190,10 @@ int mnb_device_error(void *stream, unsigned int *code, int clear);
  *   [3] launches with split_k > 1 (cluster reduction), [4 + M - 1] launches
  *   with M rows (M = 1..8), [12] launches with tensor-core math (only with
  *   MNB_FLAG_TENSOR_CORES), [13] launches of the step kernel (either math:
- *   tiles streamed in K steps by TMA tensor copies, no K split).
+ *   tiles streamed in K steps by TMA tensor copies, no K split), [14]
+ *   launches of mnb_cast_f16_to_bf16.
  * Copies min(n, MNB_NUM_COUNTERS) counters to out; returns how many. */
-#define MNB_NUM_COUNTERS 14
+#define MNB_NUM_COUNTERS 15
 int mnb_debug_counters(uint64_t *out, int n);
 void mnb_debug_counters_reset(void);
 

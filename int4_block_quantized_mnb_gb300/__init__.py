@@ -14,7 +14,7 @@ from ._native import (BLOCK, FLAG_TENSOR_CORES, FLAG_WEIGHTS_READY, MAX_M, MAX_S
                       NUM_COUNTERS, OUT_BF16, OUT_F16,
                       MnbError, check, load)
 
-__all__ = ["gemv", "gemv_ptr", "split_k_auto", "min_split_k", "max_split_k", "counters",
+__all__ = ["gemv", "gemv_ptr", "cast_f16_to_bf16", "split_k_auto", "min_split_k", "max_split_k", "counters",
            "reset_counters", "device_error", "MnbError", "OUT_F16", "OUT_BF16", "BLOCK",
            "MAX_M", "MAX_SPLIT_K", "FLAG_WEIGHTS_READY", "FLAG_TENSOR_CORES"]
 
@@ -87,6 +87,26 @@ def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stre
                  (FLAG_WEIGHTS_READY if weights_ready else 0) |
                  (FLAG_TENSOR_CORES if tensor_cores else 0))
     return y
+
+
+def cast_f16_to_bf16(src, dst=None, stream=None):
+    """bf16(src) for a contiguous CUDA float16 tensor, as its own launch (the
+    staged route's narrowing kernel); writes ``dst`` (bfloat16, same shape)
+    when given, else returns a new tensor."""
+    import torch
+    if src.dtype != torch.float16 or not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA float16 tensor")
+    if dst is None:
+        dst = torch.empty(src.shape, dtype=torch.bfloat16, device=src.device)
+    elif (dst.dtype != torch.bfloat16 or dst.shape != src.shape or not dst.is_contiguous()
+          or not dst.is_cuda):
+        raise ValueError("dst must be a contiguous CUDA bfloat16 tensor of src's shape")
+    if stream is None:
+        stream = torch.cuda.current_stream(src.device)
+    with torch.cuda.device(src.device):
+        check(load().mnb_cast_f16_to_bf16(src.data_ptr(), dst.data_ptr(), src.numel(),
+                                          stream.cuda_stream))
+    return dst
 
 
 def split_k_auto(M: int, N: int, K: int) -> int:

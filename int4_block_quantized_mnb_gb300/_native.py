@@ -21,11 +21,12 @@ FLAG_TENSOR_CORES = 2
 MAX_M = 8
 BLOCK = 32
 MAX_SPLIT_K = 8
-NUM_COUNTERS = 14
+NUM_COUNTERS = 15
 
 # Every symbol the header declares, with (restype, argtypes).
 _vp, _u8p, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
+    "mnb_cast_f16_to_bf16": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp]),
     "mnb_gemv": (ctypes.c_int, [_vp, _u8p, _vp, _u8p, _vp, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp]),
     "mnb_gemv_flags": (ctypes.c_int, [_vp, _u8p, _vp, _u8p, _vp, ctypes.c_int, ctypes.c_int,

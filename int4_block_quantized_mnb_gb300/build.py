@@ -7,7 +7,7 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "mnb_gemv.cu")]
+SOURCES = [os.path.join(PKG, "csrc", "mnb_gemv.cu"), os.path.join(PKG, "csrc", "mnb_cast.cu")]
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(PKG, "libmnb.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -28,7 +28,7 @@ def command(out: str = LIBRARY) -> list:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile libmnb.so unless it is newer than every source and the header."""
-    deps = SOURCES + [os.path.join(INCLUDE, "mnb.h")]
+    deps = SOURCES + [os.path.join(INCLUDE, "mnb.h"), os.path.join(PKG, "csrc", "mnb_narrow.cuh")]
     if not force and os.path.exists(LIBRARY) and \
             all(os.path.getmtime(LIBRARY) >= os.path.getmtime(d) for d in deps):
         return LIBRARY

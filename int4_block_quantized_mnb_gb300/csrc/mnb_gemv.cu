@@ -40,6 +40,7 @@
 //     stop, lets in-flight copies land and returns.
 
 #include "mnb.h"
+#include "mnb_narrow.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -159,6 +160,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread until the phase completes or about
+// `ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -182,9 +196,13 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
 }
 
 // Waits for the phase of `bar` with the given parity; false if the wait gave up.
+// Up to eight plain polls (each try_wait already blocks briefly in hardware)
+// before the slow path with its deadline.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned code) {
-  if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+  for (int i = 0; i < 8; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, abort_flag, code);
 }
 
@@ -385,7 +403,7 @@ struct Pow2Ceil<1> {
 __device__ __forceinline__ void store_output(void* y, size_t idx, float v, int out_bf16) {
   const __half h = __float2half_rn(v);
   if (out_bf16) {
-    static_cast<__nv_bfloat16*>(y)[idx] = __float2bfloat16_rn(__half2float(h));
+    static_cast<uint16_t*>(y)[idx] = narrow_f16_bits_to_bf16(__half_as_ushort(h));
   } else {
     static_cast<__half*>(y)[idx] = h;
   }
@@ -874,7 +892,11 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
   int issued = 0, s = 0, step = 0, tile = t_begin;
   uint32_t ph = 0;
   for (int i = 0; i < nunits; ++i) {
-    if (i >= p.stages && !mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, kErrStageFree)) break;
+    // the producer sleeps in the barrier until the stage is released (4 us
+    // at most per call) so it refills the stage as soon as it is free
+    if (i >= p.stages && !mbar_try_wait_for(empty0 + 8u * s, ph ^ 1u, 4000u) &&
+        !mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, kErrStageFree))
+      break;
     const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
     const uint32_t bar = full0 + 8u * s;
     const int row0 = tile * R;

@@ -92,3 +92,12 @@ def test_no_fallback_when_library_missing(tmp_path):
     from int4_block_quantized_mnb_gb300 import _native
     with pytest.raises(RuntimeError, match="not found"):
         _native.load(str(tmp_path / "libmnb.so"))
+
+
+def test_cast_host_validation(lib):
+    """mnb_cast_f16_to_bf16 checks its arguments before touching the device."""
+    assert lib.mnb_cast_f16_to_bf16(0, 0, 0, None) == 0                 # n = 0: nothing to do
+    assert lib.mnb_cast_f16_to_bf16(0, 4096, 8, None) == 1              # NULL
+    assert lib.mnb_cast_f16_to_bf16(4096, 0, 8, None) == 1
+    assert lib.mnb_cast_f16_to_bf16(4097, 8192, 8, None) == 6           # odd address
+    assert lib.mnb_cast_f16_to_bf16(4096, 4100, 8, None) == 7           # partial overlap

@@ -229,12 +229,22 @@ def test_non_finite_inputs_follow_ieee(M, N, K, tc):
     xs = inp.x.copy()
     xs[0, 3] = 0x7C00          # +inf
     inp.x = xs
-    y16 = _gpu.bits(_gpu.run(_gpu.to_device(inp), "f16", 1, tensor_cores=tc))
+    # row 0: code at k = 3 equals its block's zero-point, so +inf * 0 = NaN
+    qw = inp.qweight.copy()
+    z0 = int(inp.zp[0, 0]) & 0xF
+    qw[0, 1] = (qw[0, 1] & 0x0F) | (z0 << 4)
+    inp.qweight = qw
+    dev = _gpu.to_device(inp)
+    y16 = _gpu.bits(_gpu.run(dev, "f16", 1, tensor_cores=tc))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16", 1, tensor_cores=tc))
     ref = _gpu.oracle().gemv(inp.x, inp.qweight, inp.scales, inp.zp, M, N, K)
     o = _gpu.oracle()
     g, r = o.f16_to_f64(y16), o.f16_to_f64(ref["y_f16"])
+    assert np.isnan(r).any()
     assert np.array_equal(np.isnan(g), np.isnan(r))
     assert np.array_equal(g[np.isinf(r)], r[np.isinf(r)])
+    # the bf16 arm is the narrowed fp16 arm bit for bit, NaNs included
+    assert np.array_equal(ybf, o.f16_to_bf16(y16))
 
 
 @pytest.mark.parametrize("tc", [False, True], ids=["default", "tensor_cores"])

@@ -101,9 +101,13 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("int4_block_quantized_mnb_gb300/csrc/mnb_gemv.cu",
+                  "int4_block_quantized_mnb_gb300/csrc/mnb_narrow.cuh", "include/mnb.h")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
-    for rel in ("int4_block_quantized_mnb_gb300/csrc/mnb_gemv.cu", "include/mnb.h"):
+    for rel in KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()

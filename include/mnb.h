@@ -157,8 +157,9 @@ int mnb_cast_f16_to_bf16(const void *src, void *dst, size_t n, void *stream);
 
 /* split_k that mnb_gemv uses for split_k = 0 on the current device, for
  * 16-byte aligned scales and zp and without MNB_FLAG_TENSOR_CORES (1 whenever
- * the step kernel takes the launch: K a multiple of 1024, M <= 3, M * K at
- * most 33792).  Writes it to *split_k.  Same shape checks and statuses as
+ * the step kernel takes the launch: K a multiple of 1024 and staged
+ * activations M * (2K + 64) bytes at most 66 KiB for M <= 3, 136 KiB for
+ * M >= 4).  Writes it to *split_k.  Same shape checks and statuses as
  * mnb_gemv. */
 int mnb_split_k_auto(int M, int N, int K, int *split_k);
 

@@ -112,6 +112,7 @@ struct Params {
   int wk;           // K slices = 256-k segments per stage
   int steps;        // stages per tile (K / 256 / wk)
   int wtc;          // consumer warps (wk * tr)
+  int nslots;       // reduction slots
   int sc_sb;        // 16-byte scale chunks per row in a stage (odd)
   int zp_zb;        // 16-byte zero-point chunks per row in a stage (odd)
   int sc_offset;    // offset of a stage's scale box
@@ -501,17 +502,19 @@ __device__ __forceinline__ void run_producer(const Params& p, unsigned char* sme
 // Epilogue (one warp): for each tile of RC rows, in tile order, adds the
 // K-slice partial sums of every (row, m) value in slice order, rounds and
 // stores them (or keeps them for the cluster reduction), then frees the slot.
-// Tile i belongs to group i % groups, its (i / groups)-th tile.
+// Tile i belongs to group i % groups, its (i / groups)-th tile; each group has
+// `nslots` reduction slots.
 __device__ __forceinline__ void run_epilogue(const Params& p, const float* red, float* part,
                                              uint32_t ready0, uint32_t free0,
                                              volatile int* abort_flag, int row_begin,
-                                             int row_end, int RC, int ntiles, int M, int lane) {
+                                             int row_end, int RC, int ntiles, int M, int lane,
+                                             int nslots) {
   wait_prerequisites();
   const int vals_tile = RC * M;
   int g = 0, t = 0;
   for (int i = 0; i < ntiles; ++i) {
-    const int j = g * kSlotsPerGroup + t % kSlotsPerGroup;
-    if (!mbar_wait(ready0 + 8u * j, (t / kSlotsPerGroup) & 1, abort_flag, kErrReduceSlot)) break;
+    const int j = g * nslots + t % nslots;
+    if (!mbar_wait(ready0 + 8u * j, (t / nslots) & 1, abort_flag, kErrReduceSlot)) break;
     const int r0 = row_begin + i * RC;
     const int vals = min(RC, row_end - r0) * M;
     const float* slot = red + static_cast<size_t>(j) * p.wpg * vals_tile;
@@ -616,8 +619,8 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
     __syncwarp();
   } else if (warp == epilogue_warp) {
     // ------------------------------------------------------------ epilogue --
-    run_epilogue(p, red, part, ready0, free0, abort_flag, row_begin, row_end, RC, ntiles, M,
-                 lane);
+    run_epilogue(p, red, part, ready0, free0, abort_flag, row_begin, row_end, RC, ntiles, M, lane,
+                 kSlotsPerGroup);
   } else {
     // ----------------------------------------------------------- consumers --
     const int g = warp / p.wpg;
@@ -930,7 +933,12 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
   }
 }
 
-template <int M, bool kMma>
+// Math of the step kernel: CUDA-core with four rows per lane (small M),
+// CUDA-core with one row per lane and broadcast activations (larger M), or
+// tensor-core (on request).
+enum StepMath : int { kMathFma = 0, kMathWide = 1, kMathMma = 2 };
+
+template <int M, int kMath>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     gemv_step_kernel(const Params p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_sc,
@@ -943,7 +951,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int W = p.wtc;                                 // consumer warps
   const int producer_warp = W;
   const int epilogue_warp = W + 1;
-  const int nslots = kSlotsPerGroup;
+  const int nslots = p.nslots;
   const int R = kMmaRows * p.tr;                       // rows per tile
   const int vals = R * M;                              // outputs per tile
 
@@ -987,7 +995,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   if (warp == epilogue_warp) {
     // p.wpg is the number of K-slice partials per output here
     run_epilogue(p, red, nullptr, ready0, free0, abort_flag, row_begin, row_end, R, ntiles, M,
-                 lane);
+                 lane, p.nslots);
     return;
   }
 
@@ -1003,38 +1011,35 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   wait_prerequisites();
   unsigned char* xp = smem + p.xp_offset;
   auto x_off = [&](int rem) {
-    return kMma ? rem * 16 : ((rem & 3) * p.C + (rem >> 2)) * 16;
+    return kMath == kMathMma ? rem * 16 : ((rem & 3) * p.C + (rem >> 2)) * 16;
   };
   {
     // 8 activations (one k group of a block) per element; K is a multiple of
     // 1024, so every row starts 16-byte aligned when x does.
-    const int total = M * p.C * 4;
     const int per_row = p.C * 4;
     if ((reinterpret_cast<uintptr_t>(p.x) & 15u) == 0) {
-      for (int e = threadIdx.x; e < total; e += W * 32) {
-        const int m = e / per_row;
-        const int rem = e - m * per_row;
-        const uint4 v =
-            __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K) + rem);
-        *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + x_off(rem)) = pair_k4(v);
-      }
+      for (int m = 0; m < M; ++m)
+        for (int rem = threadIdx.x; rem < per_row; rem += W * 32) {
+          const uint4 v =
+              __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K) + rem);
+          *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + x_off(rem)) = pair_k4(v);
+        }
     } else {
-      for (int e = threadIdx.x; e < total; e += W * 32) {
-        const int m = e / per_row;
-        const int rem = e - m * per_row;
-        const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + 8 * rem;
-        uint4 v;
-        v.x = __ldg(src + 0) | (static_cast<uint32_t>(__ldg(src + 1)) << 16);
-        v.y = __ldg(src + 2) | (static_cast<uint32_t>(__ldg(src + 3)) << 16);
-        v.z = __ldg(src + 4) | (static_cast<uint32_t>(__ldg(src + 5)) << 16);
-        v.w = __ldg(src + 6) | (static_cast<uint32_t>(__ldg(src + 7)) << 16);
-        *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + x_off(rem)) = pair_k4(v);
-      }
+      for (int m = 0; m < M; ++m)
+        for (int rem = threadIdx.x; rem < per_row; rem += W * 32) {
+          const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + 8 * rem;
+          uint4 v;
+          v.x = __ldg(src + 0) | (static_cast<uint32_t>(__ldg(src + 1)) << 16);
+          v.y = __ldg(src + 2) | (static_cast<uint32_t>(__ldg(src + 3)) << 16);
+          v.z = __ldg(src + 4) | (static_cast<uint32_t>(__ldg(src + 5)) << 16);
+          v.w = __ldg(src + 6) | (static_cast<uint32_t>(__ldg(src + 7)) << 16);
+          *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + x_off(rem)) = pair_k4(v);
+        }
     }
     // all consumer warps (named barrier 1; producer and epilogue do not take part)
     asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
   }
-  if constexpr (kMma) {
+  if constexpr (kMath == kMathMma) {
     const int gq = lane >> 2;                               // fragment row group
     const int tq = lane & 3;                                // fragment k group
     const int row_l = rho * kMmaRows + gq;                  // fragment row in the tile
@@ -1118,7 +1123,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(ready0 + 8u * j);
     }
-  } else {
+  } else if constexpr (kMath == kMathFma) {
     // CUDA-core math.  Lane (rg, j) = (lane >> 3, lane & 7) takes block j of
     // the warp's segment of every stage for rows 16 rho + rg + 4 i, i = 0..3:
     // one 16-byte code load per row, exact q - zp pairs, and fp32 accumulation
@@ -1222,6 +1227,133 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int m = 0; m < M; ++m) slot[(rho * kMmaRows + rg + 4 * i) * M + m] = acc[i][m];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ready0 + 8u * js);
+    }
+  } else {
+    // CUDA-core math for larger M.  Lane (q, rr) = (lane >> 3, lane & 7) takes
+    // rows 16 rho + rr and 16 rho + rr + 8 and the block pair (2q, 2q + 1) of
+    // the warp's segment of every stage.  An activation load (16 bytes of one
+    // 8-k group, shared by the eight lanes of a quarter warp) feeds both rows,
+    // which balances shared-memory bandwidth against the FMA pipe; a lane holds
+    // 2M accumulators, 2M block sums and one group's 4M activation registers.
+    const int rr = lane & 7;
+    const int q = lane >> 3;
+    const int r0 = rho * kMmaRows + rr;                  // rows r0 and r0 + 8 (both rr mod 8)
+    uint32_t qo[2];                                      // block 2q + e of row r0; row r0 + 8 is +1024
+#pragma unroll
+    for (int e = 0; e < 2; ++e) qo[e] = (R * ks + r0) * 128 + 16 * ((2 * q + e) ^ rr);
+    int so[2], zo[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      so[i] = p.sc_offset + ((r0 + 8 * i) * p.sc_sb + ks) * 16 + 4 * q;   // scales of the pair
+      zo[i] = p.zp_offset + (r0 + 8 * i) * p.zp_zb * 16 + q;             // its zero-point byte
+    }
+    const unsigned char* xq = xp + (8 * ks + 2 * q) * 16;                // block 8 G + 2 q
+    const int kg_pitch = p.C * 16;                                         // bytes per k group
+    int s = 0;
+    uint32_t ph = 0;
+    bool run = true;
+    for (int t = 0; t < ntiles && run; ++t) {
+      float acc[2][M];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
+      const unsigned char* xs = xq;
+      for (int step = 0; step < p.steps; ++step, xs += p.wk * 128) {
+        if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) {
+          run = false;
+          break;
+        }
+        const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+        const int seg0 = step * p.wk;
+        const int G = seg0 + ks;                            // this warp's segment
+        const int zb = ((G >> 2) - (seg0 >> 2)) * 16 + (G & 3) * 4;
+        uint32_t sw[2];
+        ZpPairs zz[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          sw[i] = *reinterpret_cast<const uint32_t*>(st + so[i]);
+          const uint32_t zbyte = st[zo[i] + zb];
+          zz[i] = zp_pairs(zbyte * 0x00010001u);
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {                       // block 2q + e
+          float bs[2][M];
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int m = 0; m < M; ++m) bs[i][m] = 0.f;
+          uint4 w[2];                                       // both rows' 32 codes
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            w[i] = *reinterpret_cast<const uint4*>(st + qo[e] + 1024 * i);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            // both rows' q - zp pairs of this 8-k group, then one activation
+            // row at a time
+            uint32_t d[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const uint32_t zl = e ? zz[i].lo_o : zz[i].lo_e;      // 1024 + zp
+              const uint32_t zh = e ? zz[i].hi_o : zz[i].hi_e;      //   64 + zp
+              const uint32_t word = g == 0 ? w[i].x : g == 1 ? w[i].y : g == 2 ? w[i].z : w[i].w;
+              const uint32_t w8 = word >> 8;
+              d[i][0] = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl);   // k0, k4
+              d[i][1] = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh);   // k1, k5
+              d[i][2] = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl);     // k2, k6
+              d[i][3] = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh);     // k3, k7
+            }
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+              const uint4 xv =
+                  *reinterpret_cast<const uint4*>(xs + 16 * e + m * p.xp_pitch + g * kg_pitch);
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                bs[i][m] = fma2_f16_f32(xv.x, d[i][0], bs[i][m]);
+                bs[i][m] = fma2_f16_f32(xv.y, d[i][1], bs[i][m]);
+                bs[i][m] = fma2_f16_f32(xv.z, d[i][2], bs[i][m]);
+                bs[i][m] = fma2_f16_f32(xv.w, d[i][3], bs[i][m]);
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float sc = half_word_to_float(sw[i], e);
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[i][m] = fmaf(bs[i][m], sc, acc[i][m]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8u * s);
+        if (++s == p.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!run) break;
+      // the four block pairs of each row's segment, in a fixed butterfly order
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          float v = acc[i][m];
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+          v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+          acc[i][m] = v;
+        }
+      const int js = t % nslots;
+      if (t >= nslots && !mbar_wait(free0 + 8u * js, ((t / nslots) - 1) & 1, abort_flag,
+                                    kErrReduceSlot))
+        break;
+      if (q == 0) {
+        float* slot = red + (static_cast<size_t>(js) * p.wpg + ks) * vals;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int m = 0; m < M; ++m) slot[(r0 + 8 * i) * M + m] = acc[i][m];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(ready0 + 8u * js);
@@ -1428,14 +1560,22 @@ int mma_x_bytes(int M, int C) { return M * mma_x_pitch(C); }
 // The step kernel takes a launch without a K split (split_k 0 or 1) when K
 // is a multiple of 1024 (whole 256-k segments and 16-byte zero-point rows for
 // the tensor copies), scales and zero-points are 16-byte aligned and the
-// staged activations fit in kMmaXBytes: with CUDA-core math for M <= 3
-// (activation registers; M = 4 spills), with tensor-core math for any M on
-// request.
+// staged activations fit.  Math: tensor-core on request; otherwise CUDA-core
+// with four rows per lane for M <= 3 (activations in registers) and one row
+// per lane with shared activation loads for M >= 4.  The wide layout accepts
+// more activations (M = 8 at K = 8192) and then runs with two reduction slots
+// and as few as two stages, enough for a launch that is bound by its FMAs.
 constexpr int kStepFmaMaxM = 3;
+constexpr int kWideXBytes = 136 * 1024;
+
+int step_math(int M, bool tensor_cores) {
+  return tensor_cores ? kMathMma : (M <= kStepFmaMaxM ? kMathFma : kMathWide);
+}
 
 bool step_shape(int M, int K, bool tensor_cores) {
-  return K % 1024 == 0 && K <= 65536 && mma_x_bytes(M, K / kBlock) <= kMmaXBytes &&
-         (tensor_cores || M <= kStepFmaMaxM);
+  const int math = step_math(M, tensor_cores);
+  const int limit = math == kMathWide ? kWideXBytes : kMmaXBytes;
+  return K % 1024 == 0 && K <= 65536 && mma_x_bytes(M, K / kBlock) <= limit;
 }
 
 bool use_step(int M, int K, int split_k, const void* scales, const void* zp,
@@ -1447,23 +1587,27 @@ bool use_step(int M, int K, int split_k, const void* scales, const void* zp,
 
 using MmaFn = void (*)(const Params, const CUtensorMap, const CUtensorMap, const CUtensorMap);
 
-MmaFn pick_step_kernel(int M, bool mma) {
-  if (mma) {
-    switch (M) {
-      case 1: return &gemv_step_kernel<1, true>;
-      case 2: return &gemv_step_kernel<2, true>;
-      case 3: return &gemv_step_kernel<3, true>;
-      case 4: return &gemv_step_kernel<4, true>;
-      case 5: return &gemv_step_kernel<5, true>;
-      case 6: return &gemv_step_kernel<6, true>;
-      case 7: return &gemv_step_kernel<7, true>;
-      default: return &gemv_step_kernel<8, true>;
-    }
-  }
+template <int kMath>
+MmaFn step_kernel_for(int M) {
   switch (M) {
-    case 1: return &gemv_step_kernel<1, false>;
-    case 2: return &gemv_step_kernel<2, false>;
-    default: return &gemv_step_kernel<3, false>;
+    case 1: return &gemv_step_kernel<1, kMath>;
+    case 2: return &gemv_step_kernel<2, kMath>;
+    case 3: return &gemv_step_kernel<3, kMath>;
+    case 4: return &gemv_step_kernel<4, kMath>;
+    case 5: return &gemv_step_kernel<5, kMath>;
+    case 6: return &gemv_step_kernel<6, kMath>;
+    case 7: return &gemv_step_kernel<7, kMath>;
+    default: return &gemv_step_kernel<8, kMath>;
+  }
+}
+
+MmaFn pick_step_kernel(int M, int math) {
+  if (math == kMathMma) return step_kernel_for<kMathMma>(M);
+  if (math == kMathWide) return step_kernel_for<kMathWide>(M);
+  switch (M) {            // four rows per lane: M <= kStepFmaMaxM
+    case 1: return &gemv_step_kernel<1, kMathFma>;
+    case 2: return &gemv_step_kernel<2, kMathFma>;
+    default: return &gemv_step_kernel<3, kMathFma>;
   }
 }
 
@@ -1485,7 +1629,6 @@ int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, Plan* plan) {
   p.split = 1;
   p.groups = 1;
   const int S = K / kMmaSeg;
-  const int nslots = kSlotsPerGroup;
   p.xp_pitch = mma_x_pitch(p.C);
   const int x_bytes = mma_x_bytes(M, p.C);
   const int budget = static_cast<int>(dev.smem_optin) - 1024;   // 1 KB for the alignment
@@ -1527,9 +1670,16 @@ int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, Plan* plan) {
   p.zp_offset = p.q_bytes + p.sc_bytes;
   p.tx_bytes = R * (wk * 128 + p.sc_sb * 16 + p.zp_zb * 16);
   p.stage_bytes = round_up(p.q_bytes + p.sc_bytes + p.zp_bytes, 1024);
-  const int red_bytes = round_up(nslots * wk * R * M * 4, 16);
-  const int fixed = x_bytes + red_bytes + 8 * 2 * nslots + 16;
-  p.stages = std::min(kMaxStages, (budget - fixed) / (p.stage_bytes + 16));
+  // four reduction slots, or two when four would leave fewer than three stages
+  int nslots = kSlotsPerGroup, red_bytes = 0;
+  for (;;) {
+    red_bytes = round_up(nslots * wk * R * M * 4, 16);
+    const int fixed = x_bytes + red_bytes + 8 * 2 * nslots + 16;
+    p.stages = std::min(kMaxStages, (budget - fixed) / (p.stage_bytes + 16));
+    if (p.stages >= 3 || nslots == 2) break;
+    nslots = 2;
+  }
+  p.nslots = nslots;
   if (p.stages < 2) return fail(MNB_ERR_SHAPE, "shape needs more shared memory than one SM has");
   int off = p.stages * p.stage_bytes;
   p.xp_offset = off;
@@ -1741,13 +1891,14 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   DeviceInfo dev;
   if ((st = device_info(&dev)) != MNB_OK) return st;
   const bool tc = (flags & MNB_FLAG_TENSOR_CORES) != 0;
+  const int math = step_math(M, tc);
   bool step = use_step(M, K, split_k, scales, zp, tc);
   Plan plan{};
   if (step && make_mma_plan(dev, M, N, K, &plan) != MNB_OK) {
     step = false;                                 // no stage layout fits: row-tile kernel
     plan = Plan{};
   }
-  const bool mma = step && tc;
+  const bool mma = step && math == kMathMma;
   const int split = step ? 1 : (split_k == 0 ? auto_split(M, N, K, dev.sms) : split_k);
   const KernelShape ks = pick_shape(M, K / kBlock, split, scales);
   if (!step && (st = make_plan(dev, M, N, K, split, ks, &plan)) != MNB_OK) return st;
@@ -1767,7 +1918,7 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
         (st = tensor_map(kMapZeros, zp, p, &maps[2])) != MNB_OK)
       return st;
   }
-  const void* fn = step ? reinterpret_cast<const void*>(pick_step_kernel(M, mma))
+  const void* fn = step ? reinterpret_cast<const void*>(pick_step_kernel(M, math))
                         : reinterpret_cast<const void*>(pick_kernel(M, ks));
   cudaError_t e = cudaFuncSetAttribute(fn,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,

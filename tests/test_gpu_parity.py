@@ -117,12 +117,13 @@ def test_tensor_core_kernel_only_on_request():
 
 
 def test_step_kernel_takes_default_launches():
-    """Without a K split, K a multiple of 1024 and M <= 3 run the step kernel
-    (TMA tensor copies, CUDA-core math); other launches run the row-tile
-    kernel.  No default launch uses tensor-core math."""
-    for M, N, K, split, want in ((1, 4096, 4096, 0, 1), (2, 300, 8192, 1, 1), (4, 130, 4096, 0, 0),
-                                 (3, 77, 1024, 1, 1), (5, 130, 4096, 0, 0), (2, 130, 4096, 2, 0),
-                                 (1, 75, 288, 0, 0)):
+    """Without a K split, with K a multiple of 1024 and activations that fit,
+    launches run the step kernel (TMA tensor copies, CUDA-core math: four rows
+    per lane for M <= 3, one row per lane for M >= 4); other launches run the
+    row-tile kernel.  No default launch uses tensor-core math."""
+    for M, N, K, split, want in ((1, 4096, 4096, 0, 1), (2, 300, 8192, 1, 1), (4, 130, 4096, 0, 1),
+                                 (3, 77, 1024, 1, 1), (5, 130, 4096, 0, 1), (8, 300, 8192, 0, 1),
+                                 (7, 40, 2048, 1, 1), (2, 130, 4096, 2, 0), (1, 75, 288, 0, 0)):
         inp = make_inputs(M, N, K, seed=M * 3 + split + K)
         dev = _gpu.to_device(inp)
         c0 = mnb.counters()

@@ -116,10 +116,30 @@ def test_tensor_core_kernel_only_on_request():
         _gpu.compare(inp, y16, ybf, cols=cols)
 
 
+def test_mixed_shape_chain_matches_plain_calls():
+    """A chain of differently shaped launches, each reading the previous
+    output, with the early-weights promise gives the bits of plain calls."""
+    shapes = [(4096, 4096), (24576, 4096), (4096, 24576), (1024, 4096)]
+    layers = [_gpu.to_device(make_inputs(1, N, K, seed=40 + i))[1:]
+              for i, (N, K) in enumerate(shapes)]
+    x = _gpu.to_device(make_inputs(1, 4096, 4096, seed=39))[0]
+    ref = [x]
+    for q, sc, z in layers:
+        ref.append(mnb.gemv(ref[-1], q, sc, z, "f16"))
+    torch.cuda.synchronize()
+    got = [x]
+    for q, sc, z in layers:
+        got.append(mnb.gemv(got[-1], q, sc, z, "f16", weights_ready=True))
+    torch.cuda.synchronize()
+    for a, b in zip(ref[1:], got[1:]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert torch.isfinite(a.float()).all()
+
+
 def test_step_kernel_takes_default_launches():
     """Without a K split, with K a multiple of 1024 and activations that fit,
     launches run the step kernel (TMA tensor copies, CUDA-core math: four rows
-    per lane for M <= 3, one row per lane for M >= 4); other launches run the
+    per lane for M <= 3, two rows per lane for M >= 4); other launches run the
     row-tile kernel.  No default launch uses tensor-core math."""
     for M, N, K, split, want in ((1, 4096, 4096, 0, 1), (2, 300, 8192, 1, 1), (4, 130, 4096, 0, 1),
                                  (3, 77, 1024, 1, 1), (5, 130, 4096, 0, 1), (8, 300, 8192, 0, 1),
@@ -256,11 +276,11 @@ def test_weights_ready_chain_matches_plain_calls(tc):
     inp = make_inputs(1, 4096, 4096, seed=17)
     x, q, s, z = _gpu.to_device(inp)
     ref = [x]
-    for i in range(4):
+    for i in range(8):
         ref.append(mnb.gemv(ref[-1], q, s, z, "f16", tensor_cores=tc))
     torch.cuda.synchronize()
     got = [x]
-    for i in range(4):
+    for i in range(8):
         got.append(mnb.gemv(got[-1], q, s, z, "f16", weights_ready=True, tensor_cores=tc))
     torch.cuda.synchronize()
     for a, b in zip(ref[1:], got[1:]):

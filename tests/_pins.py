@@ -69,7 +69,7 @@ def numpy_reference(inp, block=32, zp="inputs"):
     """f64 dense reference: dequantize with numpy, then one matmul."""
     K, N = inp.K, inp.N
     blocks = K // block
-    z = inp.zp if zp == "inputs" else zp
+    z = inp.zp if isinstance(zp, str) else zp
     w = (dense_codes(inp.qweight, K) - np.repeat(dense_zero_points(z, N, blocks), block, axis=1)) \
         * np.repeat(numpy_f16_to_f64(inp.scales), block, axis=1)
     x = numpy_f16_to_f64(inp.x)
@@ -97,7 +97,7 @@ def golden_arrays(case):
     s = np.array(case["scales"], dtype=np.float64)
     sh = s.astype(np.float16)
     assert np.array_equal(sh.astype(np.float64), s), "fixture scale not exact in binary16"
-    return xh.view(np.uint16), q, sh.view(np.uint16), zp
+    return xh.view(np.uint16), q, sh.view(np.uint16), (None if case.get("symmetric") else zp)
 
 
 # ------------------------------------------------------------ conversions --
@@ -267,6 +267,56 @@ def check_brute_force_tiny(o) -> None:
             assert r["y_exact"][0, 0] == 1.5 * (qc - zc) * 0.25
 
 
+def check_block_sizes_numpy_dense(o) -> None:
+    """Block sizes 16, 64 and 128, with and without zero-points, against the
+    dense f64 numpy matmul of the same definition."""
+    for (M, N, K, B, seed) in ((1, 5, 256, 16, 31), (2, 3, 256, 64, 32), (3, 4, 512, 128, 33),
+                               (1, 6, 96, 16, 34), (2, 2, 384, 128, 35)):
+        inp = make_inputs(M, N, K, seed=seed, block=B)
+        for zp in (inp.zp, None):
+            r = o.gemv(inp.x, inp.qweight, inp.scales, zp, M, N, K, block=B)
+            y, a = numpy_reference(inp, block=B, zp=zp)
+            assert np.allclose(r["y_exact"], y, rtol=0, atol=1e-12 * (1 + a.max())), (B, zp is None)
+            assert np.allclose(r["abs_sum"], a, rtol=1e-12, atol=0), (B, zp is None)
+
+
+def check_block_refinement(o) -> None:
+    """A block of B is two blocks of B/2 with the same scale and zero-point:
+    the exact sums are equal (same products, same order)."""
+    for (M, N, K, B, seed) in ((2, 3, 256, 32, 41), (1, 4, 256, 64, 42), (2, 2, 512, 128, 43)):
+        inp = make_inputs(M, N, K, seed=seed, block=B)
+        blocks = K // B
+        s_half = np.ascontiguousarray(np.repeat(inp.scales, 2, axis=1))
+        z = dense_zero_points(inp.zp, N, blocks)
+        z2 = np.repeat(z, 2, axis=1)
+        zp_half = (z2[:, 0::2] | (z2[:, 1::2] << 4)).astype(np.uint8)
+        for zp, zp2 in ((inp.zp, zp_half), (None, None)):
+            r = o.gemv(inp.x, inp.qweight, inp.scales, zp, M, N, K, block=B)
+            r2 = o.gemv(inp.x, inp.qweight, s_half, zp2, M, N, K, block=B // 2)
+            assert np.array_equal(r["y_exact"], r2["y_exact"]), (B, zp is None)
+            assert np.array_equal(r["y_f16"], r2["y_f16"])
+
+
+def check_closed_form_block_sizes(o) -> None:
+    """All-equal codes, zero-points and scales give (q - zp) * s * sum_k x at
+    every block size; without zero-points zp is 8."""
+    for (M, N, K, B, qc, zc, seed) in ((1, 3, 256, 16, 13, 2, 51), (2, 2, 256, 64, 1, 9, 52),
+                                       (1, 2, 512, 128, 6, None, 53), (2, 1, 64, 16, 15, None, 54)):
+        inp = make_inputs(M, N, K, seed=seed, block=B)
+        q = np.full_like(inp.qweight, qc | (qc << 4))
+        zp = None if zc is None else np.full_like(inp.zp, zc | (zc << 4))
+        sh = np.float16(0.015625)
+        s = np.full(inp.scales.shape, sh).view(np.uint16)
+        r = o.gemv(inp.x, q, s, zp, M, N, K, block=B)
+        xs = numpy_f16_to_f64(inp.x)
+        z = 8 if zc is None else zc
+        for m in range(M):
+            exact = Fraction(qc - z) * Fraction(float(sh)) * sum(Fraction(float(v)) for v in xs[m])
+            assert float(Fraction(float(exact))) == exact, "closed form not exact in f64"
+            assert np.all(r["y_exact"][m] == float(exact)), (B, m)
+
+
 ALL_CHECKS = (check_f16_to_f64, check_bf16_to_f64, check_f64_to_f16, check_f16_to_bf16,
               check_unpack, check_golden, check_closed_form, check_numpy_dense,
-              check_invariants, check_brute_force_tiny)
+              check_invariants, check_brute_force_tiny, check_block_sizes_numpy_dense,
+              check_block_refinement, check_closed_form_block_sizes)

@@ -34,6 +34,11 @@ MUTANTS = [
     ("zp-row-stride", "int stride = (blocks + 1) / 2;", "int stride = blocks / 2;"),
     ("bf16-significand", "double m = round_half_even(ldexp(a, 7 - E));",
      "double m = round_half_even(ldexp(a, 8 - E)) / 2.0;"),
+    ("block-fixed-at-32", "int b = k / block;", "int b = k / 32;"),
+    ("zp-stride-fixed-at-32", "int blocks = K / block;\n    int stride", "int blocks = K / 32;\n    int stride"),
+    ("symmetric-zero-point-0", "return 8;", "return 0;"),
+    ("scale-stride-fixed-at-32", "scales[(size_t)n * (size_t)blocks + (size_t)b]",
+     "scales[(size_t)n * (size_t)(K / 32) + (size_t)b]"),
 ]
 
 # The bf16 single-rounding mutant needs its narrowing to read the unrounded sum.

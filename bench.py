@@ -60,6 +60,10 @@ def parse():
     ap.add_argument("--ab-staged", action="store_true",
                     help="time a synthetic decode step of bf16 GEMVs: fp16 GEMV + separate "
                          "narrowing launch (staged route) against the direct bf16 store")
+    ap.add_argument("--block", type=int, default=32, choices=[16, 32, 64, 128],
+                    help="quantization block size of the synthetic weights")
+    ap.add_argument("--symmetric", action="store_true",
+                    help="weights without zero-points (every zero-point 8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -206,6 +210,29 @@ def cpu_model():
     return f"{platform.machine()} ({', '.join(parts)})" if parts else platform.machine()
 
 
+class FormatWorkload:
+    """A workload's shape with another weight format: block size and whether
+    zero-points are stored (the symmetric format moves none)."""
+
+    def __init__(self, base, block, symmetric):
+        self.M, self.N, self.K, self.out_dtypes = base.M, base.N, base.K, base.out_dtypes
+        self.block, self.symmetric = block, symmetric
+        self.name = f"{base.name}-b{block}" + ("-sym" if symmetric else "")
+
+    def algorithmic_bytes(self) -> int:
+        from int4_block_quantized_mnb_gb300.synth import bytes_per_call
+        zp = self.N * ((self.K // self.block + 1) // 2) if self.symmetric else 0
+        return bytes_per_call(self.M, self.N, self.K, self.block) - zp
+
+
+def w_block(w):
+    return getattr(w, "block", 32)
+
+
+def w_zp(w, inp):
+    return None if getattr(w, "symmetric", False) else inp.zp
+
+
 def oracle_sample(w, inp, seconds, threads):
     """Times the CPU oracle on about `seconds` of work: a sample of output
     columns of the workload.  Returns (GB/s, description, threads used)."""
@@ -215,7 +242,7 @@ def oracle_sample(w, inp, seconds, threads):
     rng = np.random.default_rng(0)
     probe = rng.choice(w.N, size=min(w.N, max(threads, 16)), replace=False).astype(np.int64)
     t0 = time.perf_counter()
-    o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=probe, threads=threads)
+    o.gemv(inp.x, inp.qweight, inp.scales, w_zp(w, inp), w.M, w.N, w.K, block=w_block(w), cols=probe, threads=threads)
     rate = probe.size / max(time.perf_counter() - t0, 1e-6)          # columns per second
     ncols = int(max(threads, min(w.N, rate * seconds)))
     cols = rng.choice(w.N, size=ncols, replace=False).astype(np.int64)
@@ -223,7 +250,7 @@ def oracle_sample(w, inp, seconds, threads):
     passes = 0
     t0 = time.perf_counter()
     while True:
-        o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=cols, threads=threads)
+        o.gemv(inp.x, inp.qweight, inp.scales, w_zp(w, inp), w.M, w.N, w.K, block=w_block(w), cols=cols, threads=threads)
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= 0.9 * seconds:
@@ -242,7 +269,7 @@ def run_reference(args, w):
         return 0
     from int4_block_quantized_mnb_gb300.synth import make_inputs
     from oracle import Oracle
-    inp = make_inputs(w.M, w.N, w.K, seed=0)
+    inp = make_inputs(w.M, w.N, w.K, seed=0, block=w_block(w))
     o = Oracle()
     threads = os.cpu_count() or 1
     n_calls = len(w.out_dtypes)
@@ -250,18 +277,18 @@ def run_reference(args, w):
     # calibrate: columns per second on all host threads
     probe = rng.choice(w.N, size=min(w.N, max(threads, 16)), replace=False).astype(np.int64)
     t0 = time.perf_counter()
-    o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=probe, threads=threads)
+    o.gemv(inp.x, inp.qweight, inp.scales, w_zp(w, inp), w.M, w.N, w.K, block=w_block(w), cols=probe, threads=threads)
     rate = probe.size / max(time.perf_counter() - t0, 1e-6)
     budget = 120.0
     per_step = int(max(1, min(w.N, rate * budget / max(1, args.steps + args.warmup))))
     cols = [rng.choice(w.N, size=per_step, replace=False).astype(np.int64)
             for _ in range(min(args.steps + args.warmup, 64))]
     for i in range(args.warmup):
-        o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=cols[i % len(cols)],
+        o.gemv(inp.x, inp.qweight, inp.scales, w_zp(w, inp), w.M, w.N, w.K, block=w_block(w), cols=cols[i % len(cols)],
                threads=threads)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, w.M, w.N, w.K, cols=cols[i % len(cols)],
+        o.gemv(inp.x, inp.qweight, inp.scales, w_zp(w, inp), w.M, w.N, w.K, block=w_block(w), cols=cols[i % len(cols)],
                threads=threads)
     dt = time.perf_counter() - t0
     step_bytes = w.algorithmic_bytes() * n_calls * per_step / w.N
@@ -396,12 +423,14 @@ def main():
     if args.workload not in WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {list(WORKLOADS)}")
     w = WORKLOADS[args.workload]
+    if args.block != 32 or args.symmetric:
+        w = FormatWorkload(w, args.block, args.symmetric)
     if args.impl == "reference":
         return run_reference(args, w)
 
     rank, local_rank, world = dist_env()
     # The CPU oracle's thread pool is created before the first GPU call.
-    inp = make_inputs(w.M, w.N, w.K, seed=0)
+    inp = make_inputs(w.M, w.N, w.K, seed=0, block=w_block(w))
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
@@ -425,17 +454,18 @@ def main():
     x = to_dev(inp.x, torch.float16)
     q0 = to_dev(inp.qweight, torch.uint8)
     s0 = to_dev(inp.scales, torch.float16)
-    z0 = to_dev(inp.zp, torch.uint8)
+    z0 = None if w_zp(w, inp) is None else to_dev(inp.zp, torch.uint8)
     outs = list(w.out_dtypes)
     L = len(outs)
     ys = {o: torch.empty((w.M, w.N), dtype=torch.float16 if o == "f16" else torch.bfloat16,
                          device=dev) for o in outs}
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    wbytes = q0.numel() + 2 * s0.numel() + z0.numel()
+    wbytes = q0.numel() + 2 * s0.numel() + (0 if z0 is None else z0.numel())
     R = max(L, math.ceil(4 * l2 / wbytes))
     R = int(math.ceil(R / L) * L)
-    copies = [(q0, s0, z0)] + [(q0.clone(), s0.clone(), z0.clone()) for _ in range(R - 1)]
+    copies = [(q0, s0, z0)] + [(q0.clone(), s0.clone(), None if z0 is None else z0.clone())
+                               for _ in range(R - 1)]
     split_k = args.split_k
     tc = bool(args.tensor_cores)
     stream = torch.cuda.Stream(dev)
@@ -445,7 +475,7 @@ def main():
         for i, o in enumerate(outs):
             q, s, z = copies[(j * L + i) % R]
             mnb.gemv(x, q, s, z, out_dtype=o, split_k=split_k, y=ys[o], stream=stream,
-                     weights_ready=True, tensor_cores=tc)
+                     weights_ready=True, tensor_cores=tc, block=w_block(w))
 
     # Warm-up: W eager steps.
     with torch.cuda.stream(stream):
@@ -512,10 +542,11 @@ def main():
         hx = torch.from_numpy(inp.x.view(np.int16).copy()).view(torch.float16).pin_memory()
         hq = torch.from_numpy(inp.qweight).pin_memory()
         hs = torch.from_numpy(inp.scales.view(np.int16).copy()).view(torch.float16).pin_memory()
-        hz = torch.from_numpy(inp.zp).pin_memory()
+        hz = None if z0 is None else torch.from_numpy(inp.zp).pin_memory()
         hy = {o: torch.empty(ys[o].shape, dtype=ys[o].dtype).pin_memory() for o in outs}
-        dq, ds, dz, dx = torch.empty_like(q0), torch.empty_like(s0), torch.empty_like(z0), torch.empty_like(x)
-        h2d = hx.numel() * 2 + hq.numel() + hs.numel() * 2 + hz.numel()
+        dq, ds, dx = torch.empty_like(q0), torch.empty_like(s0), torch.empty_like(x)
+        dz = None if z0 is None else torch.empty_like(z0)
+        h2d = hx.numel() * 2 + hq.numel() + hs.numel() * 2 + (0 if hz is None else hz.numel())
         d2h = sum(hy[o].numel() * 2 for o in outs)
         E = max(3, min(args.steps, int(4e9 / h2d)))
 
@@ -523,10 +554,11 @@ def main():
             dx.copy_(hx, non_blocking=True)
             dq.copy_(hq, non_blocking=True)
             ds.copy_(hs, non_blocking=True)
-            dz.copy_(hz, non_blocking=True)
+            if dz is not None:
+                dz.copy_(hz, non_blocking=True)
             for o in outs:
                 mnb.gemv(dx, dq, ds, dz, out_dtype=o, split_k=split_k, y=ys[o], stream=stream,
-                         tensor_cores=tc)
+                         tensor_cores=tc, block=w_block(w))
                 hy[o].copy_(ys[o], non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -557,6 +589,7 @@ def main():
                                     if per_call_us else None),
         "pct_of_hbm_peak": 100.0 * achieved / peak,
         "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "out_dtypes": outs,
+                   "block": w_block(w), "zero_points": w_zp(w, inp) is not None,
                    "split_k": split_k if split_k else "auto", "tensor_cores": tc,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"inputs larger than L2: {R} rotating weight copies, "

@@ -4,10 +4,12 @@
  *
  * The operation (one launch computes every output element):
  *
- *     y[m,n] = round( sum_k x[m,k] * (q[n,k] - zp[n, k/32]) * scale[n, k/32] )
+ *     y[m,n] = round( sum_k x[m,k] * (q[n,k] - zp[n, k/B]) * scale[n, k/B] )
  *
  * with 4-bit weight codes q and 4-bit asymmetric zero-points zp at block size
- * 32, fp16 activations x and fp16 scales, fp32 accumulation, and a result
+ * B = 32 (also 16, 64 and 128, and the symmetric form without zero-points,
+ * where every zp is 8), fp16 activations x and fp16 scales, fp32
+ * accumulation, and a result
  * rounded to fp16; on request the fp16 result is narrowed to bf16 in the same
  * epilogue (fp32 -> fp16 -> bf16, two round-to-nearest-even steps).
  *
@@ -19,7 +21,9 @@
  *     element of its output; here one call always writes all M*N elements.
  *   - "PORT-1 (offline bias+interleave) -- measured NO-GO on the multicol
  *     asymmetric-zp GEMV" (onnx-genai PR 1002), "Why the premise fails
- *     here" point 1: 4-bit weights with a per-block asymmetric zero-point.
+ *     here" point 1: 4-bit weights with a per-block asymmetric zero-point,
+ *     and without one the symmetric dequant with a +8 bias.  Block sizes
+ *     other than 32 keep the same layout with the block size as a parameter.
  *
  * Conventions shared by every entry point:
  *   - Memory: all array arguments are device pointers owned by the caller
@@ -55,7 +59,7 @@ typedef enum mnb_status {
     MNB_OK = 0,
     MNB_ERR_NULL = 1,    /* a required pointer is NULL */
     MNB_ERR_SHAPE = 2,   /* M, N or K outside the supported range */
-    MNB_ERR_BLOCK = 3,   /* block size other than 32 */
+    MNB_ERR_BLOCK = 3,   /* block size other than 16, 32, 64 or 128 */
     MNB_ERR_DTYPE = 4,   /* out_dtype not an mnb_out_dtype */
     MNB_ERR_SPLITK = 5,  /* split_k outside [0, mnb_max_split_k] or too small for K */
     MNB_ERR_ALIGN = 6,   /* a pointer is misaligned for its element type (see mnb_gemv) */
@@ -78,16 +82,21 @@ typedef enum mnb_status {
  *   qweight  [N][K/2] uint8, row-major, 16-byte aligned.  Byte k/2 of row n
  *            holds code q[n,k] in its low nibble for even k and in its high
  *            nibble for odd k.
- *   scales   [N][K/32] fp16, row-major, 2-byte aligned.
- *   zp       [N][ceil(K/64)] uint8, row-major, any alignment.  Byte b/2 of
- *            row n holds zero-point zp[n,b] in its low nibble for even block
- *            index b and in its high nibble for odd b; when K/32 is odd the
- *            last high nibble of each row is ignored.
+ *   scales   [N][K/block] fp16, row-major, 2-byte aligned.
+ *   zp       [N][ceil(K/block/2)] uint8, row-major, any alignment.  Byte b/2
+ *            of row n holds zero-point zp[n,b] in its low nibble for even
+ *            block index b and in its high nibble for odd b; when K/block is
+ *            odd the last high nibble of each row is ignored.  NULL selects
+ *            the symmetric format: every zero-point is 8.
  *   y        [M][N] fp16 (out_dtype MNB_OUT_F16) or bf16 (MNB_OUT_BF16),
  *            row-major, 2-byte aligned, must not overlap any input.  Every
  *            one of its M*N elements is written by this call.
- *   M        1..MNB_MAX_M.   N >= 1.   K >= 32 and a multiple of 32.
- *   block    must be MNB_BLOCK (32).
+ *   M        1..MNB_MAX_M.   N >= 1.   K >= 32, a multiple of 32 and of block.
+ *   block    16, 32 (MNB_BLOCK), 64 or 128.  Block 32 with zero-points runs
+ *            the kernels tuned for it; the other formats run one CUDA-core
+ *            kernel of the same exact arithmetic, where split_k (0 = chosen
+ *            by the library) is the number of warps that split each row's K
+ *            range inside one CTA, at most 8.
  *   out_dtype  an mnb_out_dtype.  It changes only the final store: for the
  *            same inputs and split_k the bf16 result equals the
  *            round-to-nearest-even bf16 narrowing of the fp16 result, bit
@@ -192,9 +201,10 @@ int mnb_device_error(void *stream, unsigned int *code, int clear);
  *   with M rows (M = 1..8), [12] launches with tensor-core math (only with
  *   MNB_FLAG_TENSOR_CORES), [13] launches of the step kernel (either math:
  *   tiles streamed in K steps by TMA tensor copies, no K split), [14]
- *   launches of mnb_cast_f16_to_bf16.
+ *   launches of mnb_cast_f16_to_bf16, [15] launches of the general-format
+ *   kernel (block size other than 32, or no zero-points).
  * Copies min(n, MNB_NUM_COUNTERS) counters to out; returns how many. */
-#define MNB_NUM_COUNTERS 15
+#define MNB_NUM_COUNTERS 16
 int mnb_debug_counters(uint64_t *out, int n);
 void mnb_debug_counters_reset(void);
 

@@ -47,11 +47,12 @@ def gemv_ptr(x: int, qweight: int, scales: int, zp: int, y: int, M: int, N: int,
 
 
 def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stream=None,
-         weights_ready: bool = False, tensor_cores: bool = False):
+         weights_ready: bool = False, tensor_cores: bool = False, block: int = BLOCK):
     """y = MatMulNBits(x, qweight, scales, zp) on the current CUDA device.
 
-    x [M][K] float16, qweight [N][K/2] uint8, scales [N][K/32] float16,
-    zp [N][ceil(K/64)] uint8, all contiguous CUDA tensors.  Returns y [M][N]
+    x [M][K] float16, qweight [N][K/2] uint8, scales [N][K/block] float16,
+    zp [N][ceil(K/block/2)] uint8 or None (symmetric: every zero-point 8), all
+    contiguous CUDA tensors; block is 16, 32, 64 or 128.  Returns y [M][N]
     float16 or bfloat16 (or writes the given ``y``).  ``weights_ready=True``
     promises that the kernel launched just before on the stream does not
     write qweight, scales or zp (static weights), so the call may start
@@ -60,18 +61,21 @@ def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stre
     """
     import torch
     code = _out_code(out_dtype)
-    if x.dim() != 2 or qweight.dim() != 2 or scales.dim() != 2 or zp.dim() != 2:
+    if x.dim() != 2 or qweight.dim() != 2 or scales.dim() != 2 or (zp is not None and zp.dim() != 2):
         raise ValueError("x, qweight, scales and zp must be 2-D")
     M, K = x.shape
     N = qweight.shape[0]
-    if qweight.shape[1] * 2 != K or scales.shape != (N, K // BLOCK) or \
-            zp.shape != (N, (K // BLOCK + 1) // 2):
-        raise ValueError("shapes do not match x [M][K], qweight [N][K/2], scales [N][K/32], "
-                         "zp [N][ceil(K/64)]")
+    if block <= 0 or K % block != 0:
+        raise ValueError("K must be a multiple of the block size")
+    blocks = K // block
+    if qweight.shape[1] * 2 != K or scales.shape != (N, blocks) or \
+            (zp is not None and zp.shape != (N, (blocks + 1) // 2)):
+        raise ValueError("shapes do not match x [M][K], qweight [N][K/2], scales [N][K/block], "
+                         "zp [N][ceil(K/block/2)]")
     if x.dtype != torch.float16 or scales.dtype != torch.float16 or \
-            qweight.dtype != torch.uint8 or zp.dtype != torch.uint8:
+            qweight.dtype != torch.uint8 or (zp is not None and zp.dtype != torch.uint8):
         raise TypeError("x and scales must be float16; qweight and zp uint8")
-    for t in (x, qweight, scales, zp):
+    for t in (x, qweight, scales) + (() if zp is None else (zp,)):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("inputs must be contiguous CUDA tensors")
     ydt = torch.float16 if code == OUT_F16 else torch.bfloat16
@@ -82,8 +86,9 @@ def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stre
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
     with torch.cuda.device(x.device):
-        gemv_ptr(x.data_ptr(), qweight.data_ptr(), scales.data_ptr(), zp.data_ptr(),
-                 y.data_ptr(), M, N, K, BLOCK, code, int(split_k), stream.cuda_stream,
+        gemv_ptr(x.data_ptr(), qweight.data_ptr(), scales.data_ptr(),
+                 0 if zp is None else zp.data_ptr(), y.data_ptr(), M, N, K, int(block), code,
+                 int(split_k), stream.cuda_stream,
                  (FLAG_WEIGHTS_READY if weights_ready else 0) |
                  (FLAG_TENSOR_CORES if tensor_cores else 0))
     return y

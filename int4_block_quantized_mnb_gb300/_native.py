@@ -21,7 +21,7 @@ FLAG_TENSOR_CORES = 2
 MAX_M = 8
 BLOCK = 32
 MAX_SPLIT_K = 8
-NUM_COUNTERS = 15
+NUM_COUNTERS = 16
 
 # Every symbol the header declares, with (restype, argtypes).
 _vp, _u8p, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)

@@ -7,12 +7,13 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "mnb_gemv.cu"), os.path.join(PKG, "csrc", "mnb_cast.cu")]
+SOURCES = [os.path.join(PKG, "csrc", "mnb_gemv.cu"), os.path.join(PKG, "csrc", "mnb_general.cu"),
+           os.path.join(PKG, "csrc", "mnb_cast.cu")]
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(PKG, "libmnb.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-              "--expt-relaxed-constexpr"]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
+OBJDIR = os.path.join(PKG, "_build")
 
 
 def nvcc() -> str:
@@ -22,22 +23,43 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA 13 toolkit is required to build libmnb.so")
 
 
-def command(out: str = LIBRARY) -> list:
-    return [nvcc(), *ARCH, *NVCC_FLAGS, "-I" + INCLUDE, "-o", out, *SOURCES]
+def compile_command(src: str, obj: str) -> list:
+    csrc = os.path.join(PKG, "csrc")
+    return [nvcc(), *ARCH, *NVCC_FLAGS, "-I" + INCLUDE, "-I" + csrc, "-c", "-o", obj, src]
+
+
+def link_command(objs: list, out: str) -> list:
+    return [nvcc(), *ARCH, "-shared", "-o", out, *objs]
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile libmnb.so unless it is newer than every source and the header."""
-    deps = SOURCES + [os.path.join(INCLUDE, "mnb.h"), os.path.join(PKG, "csrc", "mnb_narrow.cuh")]
+    """Compile libmnb.so unless it is newer than every source and header; the
+    translation units compile in parallel, then link."""
+    deps = SOURCES + [os.path.join(INCLUDE, "mnb.h"), os.path.join(PKG, "csrc", "mnb_narrow.cuh"),
+                      os.path.join(PKG, "csrc", "mnb_dequant.cuh")]
     if not force and os.path.exists(LIBRARY) and \
             all(os.path.getmtime(LIBRARY) >= os.path.getmtime(d) for d in deps):
         return LIBRARY
-    tmp = LIBRARY + f".tmp{os.getpid()}"
-    cmd = command(tmp)
+    os.makedirs(OBJDIR, exist_ok=True)
+    tag = f"{os.getpid()}"
+    objs = [os.path.join(OBJDIR, os.path.basename(src) + f".{tag}.o") for src in SOURCES]
+    procs = []
+    for src, obj in zip(SOURCES, objs):
+        cmd = compile_command(src, obj)
+        if verbose:
+            print(" ".join(cmd))
+        procs.append((cmd, subprocess.Popen(cmd)))
+    failed = [cmd for cmd, pr in procs if pr.wait() != 0]
+    if failed:
+        raise subprocess.CalledProcessError(1, failed[0])
+    tmp = LIBRARY + f".tmp{tag}"
+    cmd = link_command(objs, tmp)
     if verbose:
         print(" ".join(cmd))
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIBRARY)
+    for obj in objs:
+        os.remove(obj)
     return LIBRARY
 
 

@@ -40,6 +40,7 @@
 //     stop, lets in-flight copies land and returns.
 
 #include "mnb.h"
+#include "mnb_dequant.cuh"
 #include "mnb_narrow.cuh"
 
 #include <cuda_bf16.h>
@@ -247,31 +248,6 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank
   return v;
 }
 
-// (a & mask) | magic in one LOP3 (the compiler splits it in two when both
-// constants are immediates).
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t magic) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(magic));
-  return d;
-}
-
-// (q - zp) for two codes: packed fp16 subtraction of magic-biased values.
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// c + a.lo*b.lo + a.hi*b.hi; f16 sources, f32 accumulation, exact products.
-__device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float c) {
-  float d;
-  asm("{\n .reg .f16 a0, a1, b0, b1;\n .reg .f32 t;\n"
-      " mov.b32 {a0, a1}, %1;\n mov.b32 {b0, b1}, %2;\n"
-      " fma.rn.f32.f16 t, a0, b0, %3;\n fma.rn.f32.f16 %0, a1, b1, t;\n}\n"
-      : "=f"(d)
-      : "r"(a), "r"(b), "f"(c));
-  return d;
-}
 
 // D = A * B + C for one m16n8k16 tile, fp16 operands, fp32 accumulators.
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -324,16 +300,6 @@ __device__ __forceinline__ ZpPairs zp_pairs(uint32_t zw) {
   return z;
 }
 
-// Eight activations k0..k7 (packed two per word) regrouped into the B
-// fragment pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7).
-__device__ __forceinline__ uint4 pair_k4(uint4 v) {
-  uint4 o;
-  o.x = __byte_perm(v.x, v.z, 0x5410);
-  o.y = __byte_perm(v.x, v.z, 0x7632);
-  o.z = __byte_perm(v.y, v.w, 0x5410);
-  o.w = __byte_perm(v.y, v.w, 0x7632);
-  return o;
-}
 
 // D = A * B for one m16n8k16 tile (zero accumulator input).
 __device__ __forceinline__ void mma_16816_zero(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -1417,6 +1383,11 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 std::atomic<unsigned long long> g_counters[MNB_NUM_COUNTERS];
 
+// mnb_general.cu: block sizes other than 32 and the symmetric format.
+int launch_general(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
+                   void* y, int M, int N, int K, int block, int out_bf16, int split_k, int sms,
+                   cudaStream_t stream);
+
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
@@ -1865,10 +1836,12 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
                    unsigned int flags, void* stream) {
   if (flags & ~static_cast<unsigned int>(MNB_FLAG_WEIGHTS_READY | MNB_FLAG_TENSOR_CORES))
     return fail(MNB_ERR_FLAGS, "unknown flag bits");
-  if (!x || !qweight || !scales || !zp || !y) return fail(MNB_ERR_NULL, "x, qweight, scales, zp and y are required");
-  if (block != kBlock) return fail(MNB_ERR_BLOCK, "only block size 32 is supported");
+  if (!x || !qweight || !scales || !y) return fail(MNB_ERR_NULL, "x, qweight, scales and y are required");
+  if (block != 16 && block != 32 && block != 64 && block != 128)
+    return fail(MNB_ERR_BLOCK, "block size must be 16, 32, 64 or 128");
   int st = check_shape(M, N, K);
   if (st != MNB_OK) return st;
+  if (K % block != 0) return fail(MNB_ERR_SHAPE, "K must be a multiple of the block size");
   if (out_dtype != MNB_OUT_F16 && out_dtype != MNB_OUT_BF16)
     return fail(MNB_ERR_DTYPE, "out_dtype must be MNB_OUT_F16 or MNB_OUT_BF16");
   if ((reinterpret_cast<uintptr_t>(qweight) & 15u) != 0)
@@ -1876,12 +1849,12 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   if ((reinterpret_cast<uintptr_t>(x) & 1u) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
       (reinterpret_cast<uintptr_t>(y) & 1u))
     return fail(MNB_ERR_ALIGN, "x, scales and y must be 2-byte aligned");
-  const size_t C = static_cast<size_t>(K) / kBlock;
+  const size_t C = static_cast<size_t>(K) / block;
   const size_t ybytes = static_cast<size_t>(M) * N * 2;
   if (overlaps(y, ybytes, x, static_cast<size_t>(M) * K * 2) ||
       overlaps(y, ybytes, qweight, static_cast<size_t>(N) * K / 2) ||
       overlaps(y, ybytes, scales, static_cast<size_t>(N) * C * 2) ||
-      overlaps(y, ybytes, zp, static_cast<size_t>(N) * ((C + 1) / 2)))
+      (zp && overlaps(y, ybytes, zp, static_cast<size_t>(N) * ((C + 1) / 2))))
     return fail(MNB_ERR_ALIAS, "y overlaps an input array");
   const int lo = min_split(M, K);
   const int hi = std::min(kMaxSplit, K / kBlock);
@@ -1890,6 +1863,16 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
                                     std::to_string(hi) + "] for this M and K");
   DeviceInfo dev;
   if ((st = device_info(&dev)) != MNB_OK) return st;
+  if (block != kBlock || zp == nullptr) {
+    // the other formats of the family: one CUDA-core kernel for all of them
+    if ((st = launch_general(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
+                             split_k, dev.sms, static_cast<cudaStream_t>(stream))) != MNB_OK)
+      return st;
+    g_counters[0].fetch_add(1, std::memory_order_relaxed);
+    g_counters[out_dtype == MNB_OUT_BF16 ? 2 : 1].fetch_add(1, std::memory_order_relaxed);
+    g_counters[4 + M - 1].fetch_add(1, std::memory_order_relaxed);
+    return MNB_OK;
+  }
   const bool tc = (flags & MNB_FLAG_TENSOR_CORES) != 0;
   const int math = step_math(M, tc);
   bool step = use_step(M, K, split_k, scales, zp, tc);

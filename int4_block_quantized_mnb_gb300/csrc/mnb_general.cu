@@ -1,0 +1,320 @@
+// mnb_general.cu -- the MatMulNBits decode GEMV for the other formats of the
+// family: block sizes 16, 32, 64 and 128, with per-block zero-points or
+// without them (symmetric: every zero-point is 8).
+//
+// Sources: the dequantized dot product y[m,n] = sum_k x[m,k] (q[n,k] -
+// zp[n,k/B]) s[n,k/B], rounded once to fp16 and, on the bf16 arm, narrowed
+// by a second rounding ("perf(cuda): let the split-K decode GEMV store bf16
+// directly", first two paragraphs); the symmetric dequant with the +8 bias
+// when a weight has no zero-point ("PORT-1 (offline bias+interleave) --
+// measured NO-GO on the multicol asymmetric-zp GEMV", "Why the premise fails
+// here", point 1).  Block sizes other than 32 take the same packed layout
+// with the block size as a parameter: scales [N][K/B], zero-points
+// [N][ceil(K/B/2)] with the low nibble holding the even block.
+//
+// Kernel shape.  A CTA of W = P * S warps takes P row pairs; the S warps of a
+// pair split K into S contiguous ranges of 32-k chunks, and lane l of a warp
+// takes chunks l, l + 32, ... of its range.  A chunk of one row is 16 bytes of
+// codes (one vector load), its block's scale and zero-point (two for block
+// 16, where a chunk spans two blocks) and 64 bytes of activations per batch
+// row, read through the read-only cache (every warp of the SM reads the same
+// activations).  Dequant is the exact one of mnb_dequant.cuh; each lane keeps
+// fp32 sums per (row, m), reduced across lanes by a fixed shuffle tree and
+// across the S warps through shared memory in warp order.
+#include "mnb.h"
+#include "mnb_dequant.cuh"
+#include "mnb_narrow.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <string>
+
+namespace mnb {
+
+int fail(int status, const std::string& detail);
+int cuda_fail(cudaError_t e, const char* what);
+extern std::atomic<unsigned long long> g_counters[MNB_NUM_COUNTERS];
+
+namespace {
+
+constexpr int kGenWarps = 8;                 // warps per CTA at most
+constexpr int kGenRows = 2;                  // rows per warp
+
+struct GenParams {
+  const uint16_t* x;
+  const uint8_t* q;
+  const uint16_t* scales;
+  const uint8_t* zp;                         // nullptr: symmetric
+  void* y;
+  int N, K;
+  int chunks;                                // K / 32
+  int blocks;                                // K / B
+  int zstride;                               // zero-point bytes per row
+  int bshift;                                // log2(B / 32) for B >= 32
+  int split;                                 // S: warps per row pair
+  int pairs;                                 // P: row pairs per CTA
+  int out_bf16;
+  int x_aligned;                             // x is 16-byte aligned
+};
+
+__device__ __forceinline__ void gen_store(void* y, size_t idx, float v, int out_bf16) {
+  const __half h = __float2half_rn(v);
+  if (out_bf16)
+    static_cast<uint16_t*>(y)[idx] = narrow_f16_bits_to_bf16(__half_as_ushort(h));
+  else
+    static_cast<__half*>(y)[idx] = h;
+}
+
+__device__ __forceinline__ float f16_bits_to_float(uint16_t h) {
+  return __half2float(__ushort_as_half(h));
+}
+
+// (1024 + z, 64 + z) in both halves: the bias words of zero-point z.
+__device__ __forceinline__ void zp_bias(uint32_t z, uint32_t& lo, uint32_t& hi) {
+  lo = z * 0x00010001u + 0x64006400u;
+  hi = z * 0x00100010u + 0x54005400u;
+}
+
+// 64 bytes of activations x[m][32c .. 32c + 32), as four 8-k groups already
+// regrouped into the (k, k + 4) pairs the dequant produces.
+__device__ __forceinline__ void load_x_chunk(const GenParams& p, int m, int c, uint4 (&xr)[4]) {
+  const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + 32 * c;
+  if (p.x_aligned) {
+    const uint4* v = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) xr[g] = pair_k4(__ldg(v + g));
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint16_t* e = src + 8 * g;
+      uint4 v;
+      v.x = __ldg(e + 0) | (static_cast<uint32_t>(__ldg(e + 1)) << 16);
+      v.y = __ldg(e + 2) | (static_cast<uint32_t>(__ldg(e + 3)) << 16);
+      v.z = __ldg(e + 4) | (static_cast<uint32_t>(__ldg(e + 5)) << 16);
+      v.w = __ldg(e + 6) | (static_cast<uint32_t>(__ldg(e + 7)) << 16);
+      xr[g] = pair_k4(v);
+    }
+  }
+}
+
+// Block sum of one 8-k group word against one activation group.
+__device__ __forceinline__ float group_dot(uint32_t word, uint32_t zl, uint32_t zh, uint4 xv,
+                                           float acc) {
+  const uint32_t w8 = word >> 8;
+  acc = fma2_f16_f32(xv.x, hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl), acc);
+  acc = fma2_f16_f32(xv.y, hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh), acc);
+  acc = fma2_f16_f32(xv.z, hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl), acc);
+  acc = fma2_f16_f32(xv.w, hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh), acc);
+  return acc;
+}
+
+template <int M, bool kB16>
+__global__ void __launch_bounds__(kGenWarps * 32) gemv_general_kernel(const GenParams p) {
+  __shared__ float red[kGenWarps][kGenRows][M];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int pair = warp / p.split;
+  const int part = warp - pair * p.split;
+  const int row0 = (blockIdx.x * p.pairs + pair) * kGenRows;
+  const int c_begin = static_cast<int>(static_cast<long long>(part) * p.chunks / p.split);
+  const int c_end = static_cast<int>(static_cast<long long>(part + 1) * p.chunks / p.split);
+  const int nrows = max(0, min(kGenRows, p.N - row0));
+
+  // programmatic dependent launch: let the next grid launch, then wait for
+  // the preceding grid's writes before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  float acc[kGenRows][M];
+#pragma unroll
+  for (int i = 0; i < kGenRows; ++i)
+#pragma unroll
+    for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
+
+  if (nrows > 0) {
+#pragma unroll 2
+    for (int c = c_begin + lane; c < c_end; c += 32) {
+      uint4 w[kGenRows];
+      float s0[kGenRows], s1[kGenRows];
+      uint32_t zl0[kGenRows], zh0[kGenRows], zl1[kGenRows], zh1[kGenRows];
+#pragma unroll
+      for (int i = 0; i < kGenRows; ++i) {
+        const int r = min(row0 + i, p.N - 1);       // a missing second row repeats the first
+        w[i] = __ldg(reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(r) * (p.K / 2)) + c);
+        const uint16_t* srow = p.scales + static_cast<size_t>(r) * p.blocks;
+        uint32_t z0 = 8, z1 = 8;
+        if (kB16) {                                   // blocks 2c and 2c + 1
+          s0[i] = f16_bits_to_float(__ldg(srow + 2 * c));
+          s1[i] = f16_bits_to_float(__ldg(srow + 2 * c + 1));
+          if (p.zp) {
+            const uint32_t zb = __ldg(p.zp + static_cast<size_t>(r) * p.zstride + c);
+            z0 = zb & 0xFu;
+            z1 = zb >> 4;
+          }
+        } else {                                      // block c >> bshift
+          const int b = c >> p.bshift;
+          s0[i] = f16_bits_to_float(__ldg(srow + b));
+          s1[i] = 0.f;
+          if (p.zp) {
+            const uint32_t zb = __ldg(p.zp + static_cast<size_t>(r) * p.zstride + (b >> 1));
+            z0 = (b & 1) ? (zb >> 4) : (zb & 0xFu);
+          }
+          z1 = z0;
+        }
+        zp_bias(z0, zl0[i], zh0[i]);
+        zp_bias(z1, zl1[i], zh1[i]);
+      }
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        uint4 xr[4];
+        load_x_chunk(p, m, c, xr);
+#pragma unroll
+        for (int i = 0; i < kGenRows; ++i) {
+          if (kB16) {
+            float b0 = group_dot(w[i].x, zl0[i], zh0[i], xr[0], 0.f);
+            b0 = group_dot(w[i].y, zl0[i], zh0[i], xr[1], b0);
+            float b1 = group_dot(w[i].z, zl1[i], zh1[i], xr[2], 0.f);
+            b1 = group_dot(w[i].w, zl1[i], zh1[i], xr[3], b1);
+            acc[i][m] = fmaf(b0, s0[i], acc[i][m]);
+            acc[i][m] = fmaf(b1, s1[i], acc[i][m]);
+          } else {
+            float b = group_dot(w[i].x, zl0[i], zh0[i], xr[0], 0.f);
+            b = group_dot(w[i].y, zl0[i], zh0[i], xr[1], b);
+            b = group_dot(w[i].z, zl0[i], zh0[i], xr[2], b);
+            b = group_dot(w[i].w, zl0[i], zh0[i], xr[3], b);
+            acc[i][m] = fmaf(b, s0[i], acc[i][m]);
+          }
+        }
+      }
+    }
+  }
+
+  // lanes, in a fixed butterfly order
+#pragma unroll
+  for (int i = 0; i < kGenRows; ++i)
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      float v = acc[i][m];
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+      acc[i][m] = v;
+    }
+  if (p.split > 1) {
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < kGenRows; ++i)
+#pragma unroll
+        for (int m = 0; m < M; ++m) red[warp][i][m] = acc[i][m];
+    }
+    __syncthreads();
+    if (part != 0) return;
+    // the K ranges of the pair, in range order
+#pragma unroll
+    for (int i = 0; i < kGenRows; ++i)
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        float v = red[warp][i][m];
+        for (int j = 1; j < p.split; ++j) v += red[warp + j][i][m];
+        acc[i][m] = v;
+      }
+  }
+  // lane e < rows * M stores output (row e / M, batch row e % M)
+#pragma unroll
+  for (int i = 0; i < kGenRows; ++i)
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+      if (lane == i * M + m && i < nrows)
+        gen_store(p.y, static_cast<size_t>(m) * p.N + row0 + i, acc[i][m], p.out_bf16);
+}
+
+using GenFn = void (*)(const GenParams);
+
+template <bool kB16>
+GenFn general_kernel_for(int M) {
+  switch (M) {
+    case 1: return &gemv_general_kernel<1, kB16>;
+    case 2: return &gemv_general_kernel<2, kB16>;
+    case 3: return &gemv_general_kernel<3, kB16>;
+    case 4: return &gemv_general_kernel<4, kB16>;
+    case 5: return &gemv_general_kernel<5, kB16>;
+    case 6: return &gemv_general_kernel<6, kB16>;
+    case 7: return &gemv_general_kernel<7, kB16>;
+    default: return &gemv_general_kernel<8, kB16>;
+  }
+}
+
+int log2_exact(int v) {
+  int s = 0;
+  while ((1 << s) < v) ++s;
+  return s;
+}
+
+}  // namespace
+
+// Warps per row pair (S) without a requested split: the fewest of 1, 2, 4, 8
+// that give at least two CTAs per SM, and no more than leave every lane of a
+// warp at least one chunk.  A requested split_k becomes S (at most 8).
+int general_split(int N, int K, int split_k, int sms) {
+  if (split_k > 0) return std::min(split_k, kGenWarps);
+  const int chunks = K / 32;
+  int s = 1;
+  while (s < kGenWarps && s * 2 * 32 <= chunks) {
+    const long long ctas = (static_cast<long long>(N) * s + 2 * kGenWarps - 1) / (2 * kGenWarps);
+    if (ctas >= 2LL * sms) break;
+    s *= 2;
+  }
+  return s;
+}
+
+// Launches the general-format kernel; arguments are validated by the caller
+// (block in {16, 32, 64, 128}, K a multiple of 32 and of the block size).
+int launch_general(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
+                   void* y, int M, int N, int K, int block, int out_bf16, int split_k, int sms,
+                   cudaStream_t stream) {
+  GenParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.q = qweight;
+  p.scales = static_cast<const uint16_t*>(scales);
+  p.zp = zp;
+  p.y = y;
+  p.N = N;
+  p.K = K;
+  p.chunks = K / 32;
+  p.blocks = K / block;
+  p.zstride = (p.blocks + 1) / 2;
+  p.bshift = block >= 32 ? log2_exact(block / 32) : 0;
+  p.split = general_split(N, K, split_k, sms);
+  p.pairs = kGenWarps / p.split;
+  p.out_bf16 = out_bf16;
+  p.x_aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  const long long rows_cta = static_cast<long long>(kGenRows) * p.pairs;
+  const long long grid = (N + rows_cta - 1) / rows_cta;
+  if (grid > 0x7FFFFFFFLL) return fail(MNB_ERR_SHAPE, "N too large");
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(p.pairs * p.split * 32));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const GenFn fn = block == 16 ? general_kernel_for<true>(M) : general_kernel_for<false>(M);
+  void* args[1] = {&p};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC(general format)");
+  g_counters[15].fetch_add(1, std::memory_order_relaxed);
+  return MNB_OK;
+}
+
+}  // namespace mnb

@@ -29,11 +29,12 @@ def oracle() -> Oracle:
     return _oracle
 
 
-def to_device(inp, device="cuda"):
+def to_device(inp, device="cuda", symmetric=False):
+    """(x, qweight, scales, zp) on the device; zp is None for the symmetric format."""
     x = torch.from_numpy(inp.x.view(np.int16).copy()).view(torch.float16).to(device)
     q = torch.from_numpy(inp.qweight).to(device)
     s = torch.from_numpy(inp.scales.view(np.int16).copy()).view(torch.float16).to(device)
-    z = torch.from_numpy(inp.zp).to(device)
+    z = None if symmetric else torch.from_numpy(inp.zp).to(device)
     return x, q, s, z
 
 
@@ -47,21 +48,25 @@ def sentinel(M, N, out, device="cuda") -> torch.Tensor:
     return torch.full((M, N), float("nan"), dtype=dt, device=device)
 
 
-def run(dev, out="f16", split_k=0, y=None, tensor_cores=False):
+def run(dev, out="f16", split_k=0, y=None, tensor_cores=False, block=32):
     x, q, s, z = dev
     M, N = x.shape[0], q.shape[0]
     if y is None:
         y = sentinel(M, N, out, x.device)
-    mnb.gemv(x, q, s, z, out_dtype=out, split_k=split_k, y=y, tensor_cores=tensor_cores)
+    mnb.gemv(x, q, s, z, out_dtype=out, split_k=split_k, y=y, tensor_cores=tensor_cores,
+             block=block)
     torch.cuda.synchronize()
     return y
 
 
-def compare(inp, y16_bits, ybf_bits=None, cols=None, threads=8):
-    """Assert the bound and the bf16 invariant on columns ``cols`` (all if None)."""
+def compare(inp, y16_bits, ybf_bits=None, cols=None, threads=8, symmetric=False):
+    """Assert the bound and the bf16 invariant on columns ``cols`` (all if None);
+    the oracle runs at the inputs' block size, without zero-points when
+    ``symmetric``."""
     o = oracle()
     M, N, K = inp.M, inp.N, inp.K
-    ref = o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, M, N, K, cols=cols, threads=threads)
+    ref = o.gemv(inp.x, inp.qweight, inp.scales, None if symmetric else inp.zp, M, N, K,
+                 block=inp.block, cols=cols, threads=threads)
     if cols is not None:
         y16_bits = y16_bits[:, cols]
         ybf_bits = None if ybf_bits is None else ybf_bits[:, cols]

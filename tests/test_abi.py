@@ -54,8 +54,9 @@ def call(lib, x=X, q=Q, s=S, z=Z, y=Y, M=1, N=64, K=256, block=32, out=0, split=
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(x=0), 1), (dict(q=0), 1), (dict(s=0), 1), (dict(z=0), 1), (dict(y=0), 1),
-    (dict(block=64), 3), (dict(block=16), 3),
+    (dict(x=0), 1), (dict(q=0), 1), (dict(s=0), 1), (dict(y=0), 1),
+    (dict(block=48), 3), (dict(block=256), 3), (dict(block=8), 3), (dict(block=0), 3),
+    (dict(K=64, block=128), 2), (dict(K=96, block=64), 2), (dict(K=160, block=64, z=0), 2),
     (dict(M=0), 2), (dict(M=9), 2), (dict(N=0), 2), (dict(N=-3), 2),
     (dict(K=0), 2), (dict(K=48), 2), (dict(K=31), 2),
     (dict(out=2), 4), (dict(out=-1), 4),

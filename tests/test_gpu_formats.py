@@ -1,0 +1,130 @@
+"""GPU parity of the other formats of the family -- block sizes 16, 64 and 128
+and the symmetric (no zero-point, every zp 8) dequant -- against the CPU
+oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+import int4_block_quantized_mnb_gb300 as mnb
+from int4_block_quantized_mnb_gb300.synth import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = [(16, False), (16, True), (32, True), (64, False), (64, True), (128, False), (128, True)]
+FORMAT_IDS = [f"b{b}-{'sym' if s else 'zp'}" for b, s in FORMATS]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    mnb.load()
+
+
+def _run_both(inp, symmetric, split=0, cols=None):
+    dev = _gpu.to_device(inp, symmetric=symmetric)
+    y16 = _gpu.bits(_gpu.run(dev, "f16", split, block=inp.block))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16", split, block=inp.block))
+    return _gpu.compare(inp, y16, ybf, cols=cols, symmetric=symmetric)
+
+
+@pytest.mark.parametrize("block,symmetric", FORMATS, ids=FORMAT_IDS)
+@pytest.mark.parametrize("M", [1, 2, 5, 8])
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 256), (33, 512), (130, 1024), (257, 384)])
+def test_small_shapes(block, symmetric, M, N, K):
+    if K % block:
+        pytest.skip("K not a multiple of the block size")
+    inp = make_inputs(M, N, K, seed=M * 7 + N + K + block, block=block)
+    c0 = mnb.counters()
+    _run_both(inp, symmetric)
+    assert mnb.counters()[15] - c0[15] == 2
+
+
+@pytest.mark.parametrize("block,symmetric", FORMATS, ids=FORMAT_IDS)
+@pytest.mark.parametrize("split", [1, 2, 3, 8])
+def test_every_split(block, symmetric, split):
+    """Each requested split (warps per row pair) meets the bound."""
+    inp = make_inputs(3, 45, 1024, seed=split + block, block=block)
+    _run_both(inp, symmetric, split=split)
+
+
+@pytest.mark.parametrize("M,N,K,block,symmetric", [
+    (1, 4096, 4096, 16, False), (1, 4096, 4096, 64, True), (1, 4096, 4096, 128, False),
+    (1, 4096, 4096, 32, True), (1, 27648, 5120, 64, False), (8, 8192, 8192, 16, True),
+    (4, 8192, 8192, 128, True),
+])
+def test_full_size(M, N, K, block, symmetric):
+    """Decode-layer sizes, compared on sampled output columns."""
+    inp = make_inputs(M, N, K, seed=N + block, block=block)
+    cols = np.random.default_rng(block).choice(N, size=min(N, 384), replace=False)
+    cols.sort()
+    _run_both(inp, symmetric, cols=cols)
+
+
+@pytest.mark.parametrize("block", [16, 64, 128])
+def test_exact_zero_rows(block):
+    """Codes equal to their zero-point (asymmetric) or to 8 (symmetric) give an
+    exact 0 whatever the activations and scales."""
+    M, N, K = 2, 40, 512
+    inp = make_inputs(M, N, K, seed=block, block=block)
+    q = inp.qweight.copy()
+    q[::3] = 0x88                                      # rows 0, 3, ...: every code 8
+    x, qd, s, _ = _gpu.to_device(inp, symmetric=True)
+    qd = torch.from_numpy(q).cuda()
+    y = _gpu.bits(mnb.gemv(x, qd, s, None, "f16", block=block))
+    assert np.all(y[:, ::3] == 0)
+    z = inp.zp.copy()
+    z[::3] = 0x88
+    zd = torch.from_numpy(z).cuda()
+    y2 = _gpu.bits(mnb.gemv(x, qd, s, zd, "f16", block=block))
+    assert np.all(y2[:, ::3] == 0)
+
+
+@pytest.mark.parametrize("block,symmetric", [(16, True), (64, False)])
+def test_misaligned_activations(block, symmetric):
+    """x only 2-byte aligned: the scalar activation loads give the same bits."""
+    M, N, K = 2, 70, 512
+    inp = make_inputs(M, N, K, seed=9, block=block)
+    x, q, s, z = _gpu.to_device(inp, symmetric=symmetric)
+    buf = torch.empty(M * K + 8, dtype=torch.float16, device="cuda")
+    xm = buf[1:1 + M * K].view(M, K)
+    xm.copy_(x)
+    assert xm.data_ptr() % 16 != 0
+    a = _gpu.bits(mnb.gemv(x, q, s, z, "f16", block=block))
+    b = _gpu.bits(mnb.gemv(xm, q, s, z, "f16", block=block))
+    assert np.array_equal(a, b)
+    _gpu.compare(inp, b, None, symmetric=symmetric)
+
+
+def test_weights_ready_chain_matches_plain_calls():
+    """Back-to-back general-format calls, each reading the previous output,
+    with the early-weights promise give the bits of plain calls."""
+    layers = [(64, True), (16, False), (128, True), (32, True)]
+    devs = [_gpu.to_device(make_inputs(1, 2048, 2048, seed=60 + i, block=b), symmetric=sym)
+            for i, (b, sym) in enumerate(layers)]
+    x = devs[0][0]
+    ref, got = [x], [x]
+    for (b, _), (_, q, s, z) in zip(layers, devs):
+        ref.append(mnb.gemv(ref[-1], q, s, z, "f16", block=b))
+    torch.cuda.synchronize()
+    for (b, _), (_, q, s, z) in zip(layers, devs):
+        got.append(mnb.gemv(got[-1], q, s, z, "f16", block=b, weights_ready=True))
+    torch.cuda.synchronize()
+    for a, c in zip(ref[1:], got[1:]):
+        assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+        assert torch.isfinite(a.float()).all()
+
+
+def test_block32_with_zero_points_keeps_its_kernels():
+    """The tuned block-32 asymmetric path never takes the general kernel."""
+    inp = make_inputs(1, 4096, 4096, seed=3)
+    dev = _gpu.to_device(inp)
+    c0 = mnb.counters()
+    _gpu.run(dev, "f16", 0)
+    c1 = mnb.counters()
+    assert c1[15] == c0[15] and c1[13] - c0[13] == 1
+
+
+def test_no_device_error_recorded():
+    assert mnb.device_error() == 0

@@ -12,13 +12,15 @@
 // with the block size as a parameter: scales [N][K/B], zero-points
 // [N][ceil(K/B/2)] with the low nibble holding the even block.
 //
-// Kernel shape.  A CTA of W = P * S warps takes P row pairs; the S warps of a
-// pair split K into S contiguous ranges of 32-k chunks, and lane l of a warp
-// takes chunks l, l + 32, ... of its range.  A chunk of one row is 16 bytes of
-// codes (one vector load), its block's scale and zero-point (two for block
-// 16, where a chunk spans two blocks) and 64 bytes of activations per batch
-// row, read through the read-only cache (every warp of the SM reads the same
-// activations).  Dequant is the exact one of mnb_dequant.cuh; each lane keeps
+// Kernel shape.  A CTA of W = P * S warps takes P row groups (four rows for
+// M <= 2, two above); the S warps of a group split K into S contiguous ranges
+// of 32-k chunks, and lane l of a warp takes chunks l, l + 32, ... of its
+// range.  A chunk of one row is 16 bytes of codes (one vector load) and its
+// block's scale and zero-point (two for block 16, where a chunk spans two
+// blocks), dequantized once into registers for all M batch rows.  Where each
+// lane has at least four chunks, the activations (up to 96 KB) are staged
+// once per CTA in shared memory, already regrouped into the pairs the
+// dequant produces; otherwise they are read through the read-only cache.  Dequant is the exact one of mnb_dequant.cuh; each lane keeps
 // fp32 sums per (row, m), reduced across lanes by a fixed shuffle tree and
 // across the S warps through shared memory in warp order.
 #include "mnb.h"
@@ -43,7 +45,6 @@ extern std::atomic<unsigned long long> g_counters[MNB_NUM_COUNTERS];
 namespace {
 
 constexpr int kGenWarps = 8;                 // warps per CTA at most
-constexpr int kGenRows = 2;                  // rows per warp
 
 struct GenParams {
   const uint16_t* x;
@@ -56,10 +57,11 @@ struct GenParams {
   int blocks;                                // K / B
   int zstride;                               // zero-point bytes per row
   int bshift;                                // log2(B / 32) for B >= 32
-  int split;                                 // S: warps per row pair
-  int pairs;                                 // P: row pairs per CTA
+  int split;                                 // S: warps per row group
+  int pairs;                                 // P: row groups per CTA
   int out_bf16;
   int x_aligned;                             // x is 16-byte aligned
+  int x_smem;                                // activations staged in shared memory
 };
 
 __device__ __forceinline__ void gen_store(void* y, size_t idx, float v, int out_bf16) {
@@ -102,49 +104,109 @@ __device__ __forceinline__ void load_x_chunk(const GenParams& p, int m, int c, u
   }
 }
 
-// Block sum of one 8-k group word against one activation group.
-__device__ __forceinline__ float group_dot(uint32_t word, uint32_t zl, uint32_t zh, uint4 xv,
-                                           float acc) {
+// q - zp of one 8-k group word as the pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7).
+__device__ __forceinline__ void dequant_word(uint32_t word, uint32_t zl, uint32_t zh,
+                                             uint32_t* d) {
   const uint32_t w8 = word >> 8;
-  acc = fma2_f16_f32(xv.x, hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl), acc);
-  acc = fma2_f16_f32(xv.y, hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh), acc);
-  acc = fma2_f16_f32(xv.z, hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl), acc);
-  acc = fma2_f16_f32(xv.w, hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh), acc);
+  d[0] = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl);
+  d[1] = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh);
+  d[2] = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl);
+  d[3] = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh);
+}
+
+// acc + the dot product of one dequantized group with one activation group.
+__device__ __forceinline__ float group_dot(const uint32_t* d, uint4 xv, float acc) {
+  acc = fma2_f16_f32(xv.x, d[0], acc);
+  acc = fma2_f16_f32(xv.y, d[1], acc);
+  acc = fma2_f16_f32(xv.z, d[2], acc);
+  acc = fma2_f16_f32(xv.w, d[3], acc);
   return acc;
 }
 
+// acc + one row's chunk (dequantized d, four groups) against one batch row's
+// activations: one block sum times its scale, or two for block 16 (words 0-1
+// are block 2c, words 2-3 block 2c + 1).
+template <bool kB16>
+__device__ __forceinline__ void chunk_dot(const uint32_t* d, const uint4 (&xr)[4], float s0,
+                                          float s1, float& acc) {
+  if (kB16) {
+    const float b0 = group_dot(d + 4, xr[1], group_dot(d + 0, xr[0], 0.f));
+    const float b1 = group_dot(d + 12, xr[3], group_dot(d + 8, xr[2], 0.f));
+    acc = fmaf(b0, s0, acc);
+    acc = fmaf(b1, s1, acc);
+  } else {
+    float b = group_dot(d + 0, xr[0], 0.f);
+    b = group_dot(d + 4, xr[1], b);
+    b = group_dot(d + 8, xr[2], b);
+    b = group_dot(d + 12, xr[3], b);
+    acc = fmaf(b, s0, acc);
+  }
+}
+
+// Rows per warp: four while the batch is small, two for M > 2 (registers,
+// with two CTAs per SM).
+constexpr int gen_rows(int M) { return M <= 2 ? 4 : 2; }
+
+// Staged activations at most; larger batches read them from global memory.
+constexpr int kGenXSmemMax = 96 * 1024;
+
 template <int M, bool kB16>
-__global__ void __launch_bounds__(kGenWarps * 32) gemv_general_kernel(const GenParams p) {
-  __shared__ float red[kGenWarps][kGenRows][M];
+__global__ void __launch_bounds__(kGenWarps * 32, 2) gemv_general_kernel(const GenParams p) {
+  constexpr int RW = gen_rows(M);
+  // staged activations, [m][group g][chunk c] of regrouped 8-k groups, so the
+  // 32 lanes of a warp (consecutive chunks) read consecutive 16-byte words
+  extern __shared__ uint4 xs[];
+  __shared__ float red[kGenWarps][RW][M];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int pair = warp / p.split;
-  const int part = warp - pair * p.split;
-  const int row0 = (blockIdx.x * p.pairs + pair) * kGenRows;
+  const int grp = warp / p.split;
+  const int part = warp - grp * p.split;
+  const int row0 = (blockIdx.x * p.pairs + grp) * RW;
   const int c_begin = static_cast<int>(static_cast<long long>(part) * p.chunks / p.split);
   const int c_end = static_cast<int>(static_cast<long long>(part + 1) * p.chunks / p.split);
-  const int nrows = max(0, min(kGenRows, p.N - row0));
+  const int nrows = max(0, min(RW, p.N - row0));
 
   // programmatic dependent launch: let the next grid launch, then wait for
   // the preceding grid's writes before reading anything
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  float acc[kGenRows][M];
+  if (p.x_smem) {
+    const int per_m = 4 * p.chunks;
+    for (int e = threadIdx.x; e < M * per_m; e += blockDim.x) {
+      const int m = e / per_m;
+      const int rem = e - m * per_m;
+      const int c = rem >> 2, g = rem & 3;
+      const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + 32 * c + 8 * g;
+      uint4 v;
+      if (p.x_aligned) {
+        v = __ldg(reinterpret_cast<const uint4*>(src));
+      } else {
+        v.x = __ldg(src + 0) | (static_cast<uint32_t>(__ldg(src + 1)) << 16);
+        v.y = __ldg(src + 2) | (static_cast<uint32_t>(__ldg(src + 3)) << 16);
+        v.z = __ldg(src + 4) | (static_cast<uint32_t>(__ldg(src + 5)) << 16);
+        v.w = __ldg(src + 6) | (static_cast<uint32_t>(__ldg(src + 7)) << 16);
+      }
+      xs[(m * 4 + g) * p.chunks + c] = pair_k4(v);
+    }
+    __syncthreads();
+  }
+
+  float acc[RW][M];
 #pragma unroll
-  for (int i = 0; i < kGenRows; ++i)
+  for (int i = 0; i < RW; ++i)
 #pragma unroll
     for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
 
   if (nrows > 0) {
 #pragma unroll 2
     for (int c = c_begin + lane; c < c_end; c += 32) {
-      uint4 w[kGenRows];
-      float s0[kGenRows], s1[kGenRows];
-      uint32_t zl0[kGenRows], zh0[kGenRows], zl1[kGenRows], zh1[kGenRows];
+      uint4 w[RW];
+      float s0[RW], s1[RW];
+      uint32_t zl0[RW], zh0[RW], zl1[RW], zh1[RW];
 #pragma unroll
-      for (int i = 0; i < kGenRows; ++i) {
-        const int r = min(row0 + i, p.N - 1);       // a missing second row repeats the first
+      for (int i = 0; i < RW; ++i) {
+        const int r = min(row0 + i, p.N - 1);       // missing rows repeat the last one
         w[i] = __ldg(reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(r) * (p.K / 2)) + c);
         const uint16_t* srow = p.scales + static_cast<size_t>(r) * p.blocks;
         uint32_t z0 = 8, z1 = 8;
@@ -169,26 +231,50 @@ __global__ void __launch_bounds__(kGenWarps * 32) gemv_general_kernel(const GenP
         zp_bias(z0, zl0[i], zh0[i]);
         zp_bias(z1, zl1[i], zh1[i]);
       }
+      if constexpr (M <= 2) {
+        // small batch: the activations of every batch row first, then one
+        // row at a time dequantized and used for all of them
+        uint4 xr[M][4];
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        uint4 xr[4];
-        load_x_chunk(p, m, c, xr);
+        for (int m = 0; m < M; ++m) {
+          if (p.x_smem) {
 #pragma unroll
-        for (int i = 0; i < kGenRows; ++i) {
-          if (kB16) {
-            float b0 = group_dot(w[i].x, zl0[i], zh0[i], xr[0], 0.f);
-            b0 = group_dot(w[i].y, zl0[i], zh0[i], xr[1], b0);
-            float b1 = group_dot(w[i].z, zl1[i], zh1[i], xr[2], 0.f);
-            b1 = group_dot(w[i].w, zl1[i], zh1[i], xr[3], b1);
-            acc[i][m] = fmaf(b0, s0[i], acc[i][m]);
-            acc[i][m] = fmaf(b1, s1[i], acc[i][m]);
+            for (int g = 0; g < 4; ++g) xr[m][g] = xs[(m * 4 + g) * p.chunks + c];
           } else {
-            float b = group_dot(w[i].x, zl0[i], zh0[i], xr[0], 0.f);
-            b = group_dot(w[i].y, zl0[i], zh0[i], xr[1], b);
-            b = group_dot(w[i].z, zl0[i], zh0[i], xr[2], b);
-            b = group_dot(w[i].w, zl0[i], zh0[i], xr[3], b);
-            acc[i][m] = fmaf(b, s0[i], acc[i][m]);
+            load_x_chunk(p, m, c, xr[m]);
           }
+        }
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+          uint32_t d[16];
+          dequant_word(w[i].x, zl0[i], zh0[i], d + 0);
+          dequant_word(w[i].y, zl0[i], zh0[i], d + 4);
+          dequant_word(w[i].z, zl1[i], zh1[i], d + 8);
+          dequant_word(w[i].w, zl1[i], zh1[i], d + 12);
+#pragma unroll
+          for (int m = 0; m < M; ++m) chunk_dot<kB16>(d, xr[m], s0[i], s1[i], acc[i][m]);
+        }
+      } else {
+        // each row's chunk is dequantized once and used for every batch row
+        uint32_t d[RW][16];
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+          dequant_word(w[i].x, zl0[i], zh0[i], d[i] + 0);
+          dequant_word(w[i].y, zl0[i], zh0[i], d[i] + 4);
+          dequant_word(w[i].z, zl1[i], zh1[i], d[i] + 8);
+          dequant_word(w[i].w, zl1[i], zh1[i], d[i] + 12);
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          uint4 xr[4];
+          if (p.x_smem) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) xr[g] = xs[(m * 4 + g) * p.chunks + c];
+          } else {
+            load_x_chunk(p, m, c, xr);
+          }
+#pragma unroll
+          for (int i = 0; i < RW; ++i) chunk_dot<kB16>(d[i], xr, s0[i], s1[i], acc[i][m]);
         }
       }
     }
@@ -196,7 +282,7 @@ __global__ void __launch_bounds__(kGenWarps * 32) gemv_general_kernel(const GenP
 
   // lanes, in a fixed butterfly order
 #pragma unroll
-  for (int i = 0; i < kGenRows; ++i)
+  for (int i = 0; i < RW; ++i)
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       float v = acc[i][m];
@@ -210,15 +296,15 @@ __global__ void __launch_bounds__(kGenWarps * 32) gemv_general_kernel(const GenP
   if (p.split > 1) {
     if (lane == 0) {
 #pragma unroll
-      for (int i = 0; i < kGenRows; ++i)
+      for (int i = 0; i < RW; ++i)
 #pragma unroll
         for (int m = 0; m < M; ++m) red[warp][i][m] = acc[i][m];
     }
     __syncthreads();
     if (part != 0) return;
-    // the K ranges of the pair, in range order
+    // the K ranges of the group, in range order
 #pragma unroll
-    for (int i = 0; i < kGenRows; ++i)
+    for (int i = 0; i < RW; ++i)
 #pragma unroll
       for (int m = 0; m < M; ++m) {
         float v = red[warp][i][m];
@@ -226,9 +312,9 @@ __global__ void __launch_bounds__(kGenWarps * 32) gemv_general_kernel(const GenP
         acc[i][m] = v;
       }
   }
-  // lane e < rows * M stores output (row e / M, batch row e % M)
+  // lane i * M + m stores output (row0 + i, batch row m)
 #pragma unroll
-  for (int i = 0; i < kGenRows; ++i)
+  for (int i = 0; i < RW; ++i)
 #pragma unroll
     for (int m = 0; m < M; ++m)
       if (lane == i * M + m && i < nrows)
@@ -259,16 +345,19 @@ int log2_exact(int v) {
 
 }  // namespace
 
-// Warps per row pair (S) without a requested split: the fewest of 1, 2, 4, 8
-// that give at least two CTAs per SM, and no more than leave every lane of a
-// warp at least one chunk.  A requested split_k becomes S (at most 8).
-int general_split(int N, int K, int split_k, int sms) {
+// Warps per row group (S) without a requested split: the fewest of 1, 2, 4,
+// 8 that give every SM a CTA (two are resident per SM, so this stays within
+// one wave where the rows allow), and no more than leave every lane of a warp
+// at least one chunk.  A requested split_k becomes S (at most 8).
+int general_split(int M, int N, int K, int split_k, int sms) {
   if (split_k > 0) return std::min(split_k, kGenWarps);
   const int chunks = K / 32;
+  const int rows_warp = gen_rows(M);
   int s = 1;
   while (s < kGenWarps && s * 2 * 32 <= chunks) {
-    const long long ctas = (static_cast<long long>(N) * s + 2 * kGenWarps - 1) / (2 * kGenWarps);
-    if (ctas >= 2LL * sms) break;
+    const long long rows_cta = static_cast<long long>(rows_warp) * (kGenWarps / s);
+    const long long ctas = (N + rows_cta - 1) / rows_cta;
+    if (ctas >= sms) break;
     s *= 2;
   }
   return s;
@@ -291,18 +380,21 @@ int launch_general(const void* x, const uint8_t* qweight, const void* scales, co
   p.blocks = K / block;
   p.zstride = (p.blocks + 1) / 2;
   p.bshift = block >= 32 ? log2_exact(block / 32) : 0;
-  p.split = general_split(N, K, split_k, sms);
+  p.split = general_split(M, N, K, split_k, sms);
   p.pairs = kGenWarps / p.split;
   p.out_bf16 = out_bf16;
   p.x_aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
-  const long long rows_cta = static_cast<long long>(kGenRows) * p.pairs;
+  const size_t x_bytes = static_cast<size_t>(M) * K * 2;
+  // staging pays where each lane of a warp has at least four chunks of its range
+  p.x_smem = x_bytes <= static_cast<size_t>(kGenXSmemMax) && p.chunks / p.split >= 4 * 32;
+  const long long rows_cta = static_cast<long long>(gen_rows(M)) * p.pairs;
   const long long grid = (N + rows_cta - 1) / rows_cta;
   if (grid > 0x7FFFFFFFLL) return fail(MNB_ERR_SHAPE, "N too large");
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(static_cast<unsigned>(p.pairs * p.split * 32));
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = p.x_smem ? x_bytes : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -310,8 +402,11 @@ int launch_general(const void* x, const uint8_t* qweight, const void* scales, co
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const GenFn fn = block == 16 ? general_kernel_for<true>(M) : general_kernel_for<false>(M);
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGenXSmemMax);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(general format)");
   void* args[1] = {&p};
-  const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
+  e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC(general format)");
   g_counters[15].fetch_add(1, std::memory_order_relaxed);
   return MNB_OK;

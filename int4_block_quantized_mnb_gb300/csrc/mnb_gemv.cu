@@ -1136,10 +1136,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             xr[m][g] = *reinterpret_cast<const uint4*>(xb + m * p.xp_pitch + g * kg_pitch);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint4 w = *reinterpret_cast<const uint4*>(st + qo[i]);
+          // rows i and i + 2 share their swizzle: row i + 2 is 1024 bytes on
+          const uint4 w = *reinterpret_cast<const uint4*>(st + qo[i & 1] + 1024 * (i >> 1));
           const uint32_t z = (static_cast<uint32_t>(st[zo[i] + zb]) >> zsh) & 0xFu;
-          const uint32_t zl = and_or(z * 0x00010001u, 0x000F000Fu, 0x64006400u);   // 1024 + zp
-          const uint32_t zh = and_or(z * 0x00100010u, 0x00F000F0u, 0x54005400u);   //   64 + zp
+          // the bias words need no masking: z < 16 fills bits the magic leaves clear
+          const uint32_t zl = z * 0x00010001u + 0x64006400u;                       // 1024 + zp
+          const uint32_t zh = z * 0x00100010u + 0x54005400u;                       //   64 + zp
           const float sc = half_word_to_float(*reinterpret_cast<const uint16_t*>(st + so[i]), 0);
           const uint32_t words[4] = {w.x, w.y, w.z, w.w};
           float bs[M];

@@ -106,7 +106,8 @@ def measured_peaks():
 
 
 KERNEL_SOURCES = ("int4_block_quantized_mnb_gb300/csrc/mnb_gemv.cu",
-                  "int4_block_quantized_mnb_gb300/csrc/mnb_narrow.cuh", "include/mnb.h")
+                  "int4_block_quantized_mnb_gb300/csrc/mnb_dequant.cuh",
+                  "int4_block_quantized_mnb_gb300/csrc/mnb_narrow.cuh")
 
 
 def kernel_source_hash():

@@ -70,7 +70,8 @@ typedef enum mnb_status {
 } mnb_status;
 
 /* Limits of mnb_gemv. */
-#define MNB_MAX_M 8            /* decode batch rows per call */
+#define MNB_MAX_M 8            /* decode batch rows per call (the GEMV kernels) */
+#define MNB_MAX_PREFILL_M 4194240 /* rows of the prefill path: 65535 tiles of 64 */
 #define MNB_BLOCK 32           /* quantization block along K */
 #define MNB_MAX_SPLIT_K 8      /* K-partitions reduced inside one thread-block cluster */
 
@@ -91,7 +92,11 @@ typedef enum mnb_status {
  *   y        [M][N] fp16 (out_dtype MNB_OUT_F16) or bf16 (MNB_OUT_BF16),
  *            row-major, 2-byte aligned, must not overlap any input.  Every
  *            one of its M*N elements is written by this call.
- *   M        1..MNB_MAX_M.   N >= 1.   K >= 32, a multiple of 32 and of block.
+ *   M        1..MNB_MAX_M: the decode GEMV kernels; MNB_MAX_M + 1 ..
+ *            MNB_MAX_PREFILL_M: the prefill path, a tensor-core GEMM with the
+ *            same exact products, fp32 sums and epilogue (block 32, 64 or 128;
+ *            split_k 0 or 1).   N >= 1.   K >= 32, a multiple of 32 and of
+ *            block.
  *   block    16, 32 (MNB_BLOCK), 64 or 128.  Block 32 with zero-points runs
  *            the kernels tuned for it; the other formats run one CUDA-core
  *            kernel of the same exact arithmetic, where split_k (0 = chosen
@@ -202,9 +207,10 @@ int mnb_device_error(void *stream, unsigned int *code, int clear);
  *   MNB_FLAG_TENSOR_CORES), [13] launches of the step kernel (either math:
  *   tiles streamed in K steps by TMA tensor copies, no K split), [14]
  *   launches of mnb_cast_f16_to_bf16, [15] launches of the general-format
- *   kernel (block size other than 32, or no zero-points).
+ *   kernel (block size other than 32, or no zero-points), [16] launches of the
+ *   prefill GEMM (M > MNB_MAX_M).
  * Copies min(n, MNB_NUM_COUNTERS) counters to out; returns how many. */
-#define MNB_NUM_COUNTERS 16
+#define MNB_NUM_COUNTERS 17
 int mnb_debug_counters(uint64_t *out, int n);
 void mnb_debug_counters_reset(void);
 

@@ -1,4 +1,5 @@
-// mnb_dequant.cuh -- the exact 4-bit dequant shared by the GEMV kernels.
+// mnb_dequant.cuh -- the exact 4-bit dequant shared by the GEMV kernels, and
+// the fp16 tensor-core fragment product their tensor-core math uses.
 //
 // Two codes of a 32-bit word (nibbles k and k + 4 of one 8-k group) become an
 // fp16 pair by OR-ing them into the mantissa of a power of two: low nibbles
@@ -47,6 +48,28 @@ __device__ __forceinline__ uint4 pair_k4(uint4 v) {
   o.z = __byte_perm(v.y, v.w, 0x5410);
   o.w = __byte_perm(v.y, v.w, 0x7632);
   return o;
+}
+
+// D = A * B + C for one m16n8k16 tile, fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1,
+                                          const float (&c)[4]) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
+}
+
+// D = A * B for one m16n8k16 tile (zero accumulator input).
+__device__ __forceinline__ void mma_16816_zero(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm("{\n .reg .f32 z;\n mov.f32 z, 0f00000000;\n"
+      " mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {z,z,z,z};\n}"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 }  // namespace mnb

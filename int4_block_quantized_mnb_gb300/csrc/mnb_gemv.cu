@@ -249,16 +249,6 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank
 }
 
 
-// D = A * B + C for one m16n8k16 tile, fp16 operands, fp32 accumulators.
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1,
-                                          const float (&c)[4]) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%11,%12,%13};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
-        "f"(c[3]));
-}
 
 __device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -301,16 +291,6 @@ __device__ __forceinline__ ZpPairs zp_pairs(uint32_t zw) {
 }
 
 
-// D = A * B for one m16n8k16 tile (zero accumulator input).
-__device__ __forceinline__ void mma_16816_zero(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-  asm("{\n .reg .f32 z;\n mov.f32 z, 0f00000000;\n"
-      " mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {z,z,z,z};\n}"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 // One 32-block of a 16-row tile for the lane holding fragment rows g (codes
 // w0, zero-point pairs zl0/zh0, scale s0) and g + 8 (w1, zl1/zh1, s1), k
@@ -1385,6 +1365,10 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 std::atomic<unsigned long long> g_counters[MNB_NUM_COUNTERS];
 
+// mnb_prefill.cu: more than MNB_MAX_M activation rows.
+int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
+                   void* y, int M, int N, int K, int block, int out_bf16, cudaStream_t stream);
+
 // mnb_general.cu: block sizes other than 32 and the symmetric format.
 int launch_general(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                    void* y, int M, int N, int K, int block, int out_bf16, int split_k, int sms,
@@ -1776,6 +1760,41 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x0 < y0 + nb && y0 < x0 + na;
 }
 
+// The prefill path (M > MNB_MAX_M): its own checks, then one launch.
+int gemm_prefill(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
+                 void* y, int M, int N, int K, int block, int out_dtype, int split_k,
+                 void* stream) {
+  if (block == 16) return fail(MNB_ERR_BLOCK, "the prefill path takes block 32, 64 or 128");
+  if (N < 1) return fail(MNB_ERR_SHAPE, "N must be >= 1");
+  if (K < kBlock || K % kBlock != 0 || K % block != 0)
+    return fail(MNB_ERR_SHAPE, "K must be a positive multiple of 32 and of the block size");
+  if (out_dtype != MNB_OUT_F16 && out_dtype != MNB_OUT_BF16)
+    return fail(MNB_ERR_DTYPE, "out_dtype must be MNB_OUT_F16 or MNB_OUT_BF16");
+  if ((reinterpret_cast<uintptr_t>(qweight) & 15u) != 0)
+    return fail(MNB_ERR_ALIGN, "qweight must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(x) & 1u) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
+      (reinterpret_cast<uintptr_t>(y) & 1u))
+    return fail(MNB_ERR_ALIGN, "x, scales and y must be 2-byte aligned");
+  const size_t C = static_cast<size_t>(K) / block;
+  const size_t ybytes = static_cast<size_t>(M) * N * 2;
+  if (overlaps(y, ybytes, x, static_cast<size_t>(M) * K * 2) ||
+      overlaps(y, ybytes, qweight, static_cast<size_t>(N) * K / 2) ||
+      overlaps(y, ybytes, scales, static_cast<size_t>(N) * C * 2) ||
+      (zp && overlaps(y, ybytes, zp, static_cast<size_t>(N) * ((C + 1) / 2))))
+    return fail(MNB_ERR_ALIAS, "y overlaps an input array");
+  if (split_k != 0 && split_k != 1)
+    return fail(MNB_ERR_SPLITK, "split_k must be 0 or 1 on the prefill path");
+  DeviceInfo dev;
+  int st = device_info(&dev);
+  if (st != MNB_OK) return st;
+  if ((st = launch_prefill(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
+                           static_cast<cudaStream_t>(stream))) != MNB_OK)
+    return st;
+  g_counters[0].fetch_add(1, std::memory_order_relaxed);
+  g_counters[out_dtype == MNB_OUT_BF16 ? 2 : 1].fetch_add(1, std::memory_order_relaxed);
+  return MNB_OK;
+}
+
 }  // namespace mnb
 
 using namespace mnb;
@@ -1841,6 +1860,8 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   if (!x || !qweight || !scales || !y) return fail(MNB_ERR_NULL, "x, qweight, scales and y are required");
   if (block != 16 && block != 32 && block != 64 && block != 128)
     return fail(MNB_ERR_BLOCK, "block size must be 16, 32, 64 or 128");
+  if (M > kMaxM && M <= MNB_MAX_PREFILL_M)
+    return gemm_prefill(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, stream);
   int st = check_shape(M, N, K);
   if (st != MNB_OK) return st;
   if (K % block != 0) return fail(MNB_ERR_SHAPE, "K must be a multiple of the block size");

@@ -1,0 +1,221 @@
+// mnb_prefill.cu -- the MatMulNBits GEMM for more than 8 activation rows
+// (prefill): y[m,n] = sum_k x[m,k] (q[n,k] - zp[n,k/B]) s[n,k/B], M > 8, with
+// the decode GEMV's epilogue (one rounding to fp16, and on the bf16 arm the
+// narrowing of that fp16 value) -- "perf(cuda): let the split-K decode GEMV
+// store bf16 directly", the paragraph on the prefill path, which lacked the
+// narrowing store.  Block sizes 32, 64 and 128, with or without zero-points.
+//
+// Tensor-core form.  Weight rows are the M dimension of mma.sync m16n8k16
+// and activation rows its N dimension: a CTA takes 128 weight rows (16 per
+// warp) by 64 activation rows (8 tiles of 8 per warp).  The A operand is the
+// exact fp16 q - zp of mnb_dequant.cuh: lane (g, t) holds code word t of
+// chunk c for weight rows g and g + 8, whose pairs (k0,k4) (k1,k5) feed one
+// fragment product and (k2,k6) (k3,k7) the next; the activations are staged
+// per 256-k stage in shared memory, regrouped into the same pairs, so one
+// 16-byte load gives lane (g, t) the B operand of both products for
+// activation row g of a tile.  The products are exact and the fragment sums
+// fp32; each quantization block's sum D starts from zero and is scaled into
+// fp32 accumulators when the block ends.
+#include "mnb.h"
+#include "mnb_dequant.cuh"
+#include "mnb_narrow.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <string>
+
+namespace mnb {
+
+int fail(int status, const std::string& detail);
+int cuda_fail(cudaError_t e, const char* what);
+extern std::atomic<unsigned long long> g_counters[MNB_NUM_COUNTERS];
+
+namespace {
+
+constexpr int kPfWarps = 8;
+constexpr int kPfRows = 16 * kPfWarps;         // weight rows per CTA
+constexpr int kPfTiles = 8;                    // 8-row activation tiles per CTA
+constexpr int kPfTok = 8 * kPfTiles;           // activation rows per CTA
+constexpr int kPfStage = 8;                    // 32-k chunks per stage (256 k)
+// one activation row of a stage: kPfStage chunks x 4 groups of 16 bytes, plus
+// 64 bytes so that rows g and g + 1 start 16 banks apart (conflict-free loads)
+constexpr int kPfPitch = kPfStage * 4 + 4;     // in 16-byte words
+
+struct PfParams {
+  const uint16_t* x;
+  const uint8_t* q;
+  const uint16_t* scales;
+  const uint8_t* zp;                           // nullptr: symmetric
+  void* y;
+  int M, N, K;
+  int chunks;                                  // K / 32
+  int blocks;                                  // K / B
+  int zstride;                                 // zero-point bytes per row
+  int bshift;                                  // log2(B / 32)
+  int out_bf16;
+  int x_aligned;
+};
+
+__device__ __forceinline__ void pf_store(void* y, size_t idx, float v, int out_bf16) {
+  const __half h = __float2half_rn(v);
+  if (out_bf16)
+    static_cast<uint16_t*>(y)[idx] = narrow_f16_bits_to_bf16(__half_as_ushort(h));
+  else
+    static_cast<__half*>(y)[idx] = h;
+}
+
+// q - zp pairs of code word `word` (see dequant_word in the general kernel).
+__device__ __forceinline__ void pf_dequant(uint32_t word, uint32_t z, uint32_t* d) {
+  const uint32_t zl = z * 0x00010001u + 0x64006400u;
+  const uint32_t zh = z * 0x00100010u + 0x54005400u;
+  const uint32_t w8 = word >> 8;
+  d[0] = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl);
+  d[1] = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh);
+  d[2] = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl);
+  d[3] = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh);
+}
+
+__global__ void __launch_bounds__(kPfWarps * 32, 2) gemm_prefill_kernel(const PfParams p) {
+  __shared__ uint4 xs[kPfTok * kPfPitch];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  const int n0 = blockIdx.x * kPfRows + warp * 16;
+  const int m0 = blockIdx.y * kPfTok;
+  const int r0 = n0 + g, r1 = n0 + g + 8;                   // this lane's weight rows
+  const int l0 = min(r0, p.N - 1), l1 = min(r1, p.N - 1);   // rows past N read row N - 1
+  const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.q + static_cast<size_t>(l0) * (p.K / 2));
+  const uint32_t* q1 = reinterpret_cast<const uint32_t*>(p.q + static_cast<size_t>(l1) * (p.K / 2));
+  const uint16_t* s0p = p.scales + static_cast<size_t>(l0) * p.blocks;
+  const uint16_t* s1p = p.scales + static_cast<size_t>(l1) * p.blocks;
+  const int bmask = (1 << p.bshift) - 1;
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  float acc[kPfTiles][4], D[kPfTiles][4];
+#pragma unroll
+  for (int j = 0; j < kPfTiles; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[j][e] = D[j][e] = 0.f;
+
+  for (int cs = 0; cs < p.chunks; cs += kPfStage) {
+    const int nch = min(kPfStage, p.chunks - cs);
+    __syncthreads();                                       // the last stage is read
+    // stage: activation rows m0.., chunks cs.., regrouped (zero past M)
+    for (int e = threadIdx.x; e < kPfTok * nch * 4; e += kPfWarps * 32) {
+      const int tt = e / (nch * 4);
+      const int rem = e - tt * (nch * 4);
+      const int m = m0 + tt;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (m < p.M) {
+        const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + 32 * cs + 8 * rem;
+        if (p.x_aligned) {
+          v = __ldg(reinterpret_cast<const uint4*>(src));
+        } else {
+          v.x = __ldg(src + 0) | (static_cast<uint32_t>(__ldg(src + 1)) << 16);
+          v.y = __ldg(src + 2) | (static_cast<uint32_t>(__ldg(src + 3)) << 16);
+          v.z = __ldg(src + 4) | (static_cast<uint32_t>(__ldg(src + 5)) << 16);
+          v.w = __ldg(src + 6) | (static_cast<uint32_t>(__ldg(src + 7)) << 16);
+        }
+      }
+      xs[tt * kPfPitch + rem] = pair_k4(v);
+    }
+    __syncthreads();
+    for (int cc = 0; cc < nch; ++cc) {
+      const int c = cs + cc;
+      const int b = c >> p.bshift;
+      uint32_t z0 = 8, z1 = 8;
+      if (p.zp) {
+        const uint32_t zb0 = __ldg(p.zp + static_cast<size_t>(l0) * p.zstride + (b >> 1));
+        const uint32_t zb1 = __ldg(p.zp + static_cast<size_t>(l1) * p.zstride + (b >> 1));
+        z0 = (b & 1) ? (zb0 >> 4) : (zb0 & 0xFu);
+        z1 = (b & 1) ? (zb1 >> 4) : (zb1 & 0xFu);
+      }
+      uint32_t d0[4], d1[4];
+      pf_dequant(__ldg(q0 + 4 * c + t), z0, d0);
+      pf_dequant(__ldg(q1 + 4 * c + t), z1, d1);
+      const uint4* xrow = xs + g * kPfPitch + cc * 4 + t;
+#pragma unroll
+      for (int j = 0; j < kPfTiles; ++j) {
+        const uint4 xv = xrow[j * 8 * kPfPitch];
+        mma_16816(D[j], d0[0], d1[0], d0[1], d1[1], xv.x, xv.y, D[j]);
+        mma_16816(D[j], d0[2], d1[2], d0[3], d1[3], xv.z, xv.w, D[j]);
+      }
+      if ((c & bmask) == bmask) {                           // the block ends here
+        const float s0 = __half2float(__ushort_as_half(__ldg(s0p + b)));
+        const float s1 = __half2float(__ushort_as_half(__ldg(s1p + b)));
+#pragma unroll
+        for (int j = 0; j < kPfTiles; ++j) {
+          acc[j][0] = fmaf(D[j][0], s0, acc[j][0]);
+          acc[j][1] = fmaf(D[j][1], s0, acc[j][1]);
+          acc[j][2] = fmaf(D[j][2], s1, acc[j][2]);
+          acc[j][3] = fmaf(D[j][3], s1, acc[j][3]);
+          D[j][0] = D[j][1] = D[j][2] = D[j][3] = 0.f;
+        }
+      }
+    }
+  }
+  // D element e of tile j: weight row r0 (e < 2) or r1, activation row
+  // m0 + 8 j + 2 t + (e & 1)
+#pragma unroll
+  for (int j = 0; j < kPfTiles; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int n = e < 2 ? r0 : r1;
+      const int m = m0 + 8 * j + 2 * t + (e & 1);
+      if (n < p.N && m < p.M)
+        pf_store(p.y, static_cast<size_t>(m) * p.N + n, acc[j][e], p.out_bf16);
+    }
+}
+
+}  // namespace
+
+// Launches the prefill GEMM; arguments are validated by the caller (M > 8,
+// block 32, 64 or 128, K a multiple of 32 and of the block size).
+int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
+                   void* y, int M, int N, int K, int block, int out_bf16, cudaStream_t stream) {
+  PfParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.q = qweight;
+  p.scales = static_cast<const uint16_t*>(scales);
+  p.zp = zp;
+  p.y = y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.chunks = K / 32;
+  p.blocks = K / block;
+  p.zstride = (p.blocks + 1) / 2;
+  p.bshift = block == 128 ? 2 : block == 64 ? 1 : 0;
+  p.out_bf16 = out_bf16;
+  p.x_aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  const long long gx = (static_cast<long long>(N) + kPfRows - 1) / kPfRows;
+  const long long gy = (static_cast<long long>(M) + kPfTok - 1) / kPfTok;
+  if (gx > 0x7FFFFFFFLL || gy > 65535) return fail(MNB_ERR_SHAPE, "prefill shape too large");
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  cfg.blockDim = dim3(kPfWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[1] = {&p};
+  const cudaError_t e =
+      cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&gemm_prefill_kernel), args);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC(prefill)");
+  g_counters[16].fetch_add(1, std::memory_order_relaxed);
+  return MNB_OK;
+}
+
+}  // namespace mnb

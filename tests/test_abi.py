@@ -57,7 +57,9 @@ def call(lib, x=X, q=Q, s=S, z=Z, y=Y, M=1, N=64, K=256, block=32, out=0, split=
     (dict(x=0), 1), (dict(q=0), 1), (dict(s=0), 1), (dict(y=0), 1),
     (dict(block=48), 3), (dict(block=256), 3), (dict(block=8), 3), (dict(block=0), 3),
     (dict(K=64, block=128), 2), (dict(K=96, block=64), 2), (dict(K=160, block=64, z=0), 2),
-    (dict(M=0), 2), (dict(M=9), 2), (dict(N=0), 2), (dict(N=-3), 2),
+    (dict(M=0), 2), (dict(M=4194241), 2), (dict(N=0), 2), (dict(N=-3), 2),
+    (dict(M=9, block=16), 3), (dict(M=64, split=2), 5), (dict(M=9, K=96, block=64), 2),
+    (dict(M=16, out=2), 4), (dict(M=16, q=Q + 8), 6), (dict(M=16, y=X), 7),
     (dict(K=0), 2), (dict(K=48), 2), (dict(K=31), 2),
     (dict(out=2), 4), (dict(out=-1), 4),
     (dict(q=Q + 8), 6), (dict(x=X + 1), 6), (dict(s=S + 1), 6), (dict(y=Y + 1), 6),

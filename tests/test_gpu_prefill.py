@@ -1,0 +1,114 @@
+"""GPU parity of the prefill path (M > 8: the tensor-core GEMM with the decode
+GEMV's epilogue) against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+import int4_block_quantized_mnb_gb300 as mnb
+from int4_block_quantized_mnb_gb300.synth import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = [(32, False), (32, True), (64, False), (128, True)]
+FORMAT_IDS = [f"b{b}-{'sym' if s else 'zp'}" for b, s in FORMATS]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    mnb.load()
+
+
+def _run_both(inp, symmetric, cols=None):
+    dev = _gpu.to_device(inp, symmetric=symmetric)
+    c0 = mnb.counters()
+    y16 = _gpu.bits(_gpu.run(dev, "f16", 0, block=inp.block))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16", 0, block=inp.block))
+    assert mnb.counters()[16] - c0[16] == 2
+    return _gpu.compare(inp, y16, ybf, cols=cols, symmetric=symmetric)
+
+
+@pytest.mark.parametrize("block,symmetric", FORMATS, ids=FORMAT_IDS)
+@pytest.mark.parametrize("M", [9, 16, 33, 64, 65, 130])
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 256), (130, 1024), (257, 384)])
+def test_small_shapes(block, symmetric, M, N, K):
+    if K % block:
+        pytest.skip("K not a multiple of the block size")
+    inp = make_inputs(M, N, K, seed=M * 11 + N + K + block, block=block)
+    _run_both(inp, symmetric)
+
+
+@pytest.mark.parametrize("M,N,K,block,symmetric", [
+    (512, 4096, 4096, 32, False), (128, 27648, 5120, 32, False), (257, 4096, 4096, 64, True),
+    (1000, 1024, 8192, 128, False),
+])
+def test_full_size(M, N, K, block, symmetric):
+    """Prefill-sized layers, compared on sampled output columns."""
+    inp = make_inputs(M, N, K, seed=M + N + block, block=block)
+    cols = np.random.default_rng(M).choice(N, size=min(N, 96), replace=False)
+    cols.sort()
+    _run_both(inp, symmetric, cols=cols)
+
+
+def test_exact_zero_rows():
+    """Codes equal to their zero-points give exact zeros on the prefill path."""
+    M, N, K = 40, 48, 512
+    inp = make_inputs(M, N, K, seed=5)
+    q = inp.qweight.copy()
+    z = inp.zp.copy()
+    q[::5] = 0x77
+    z[::5] = 0x77
+    x, _, s, _ = _gpu.to_device(inp)
+    y = _gpu.bits(mnb.gemv(x, torch.from_numpy(q).cuda(), s, torch.from_numpy(z).cuda(), "f16"))
+    assert np.all(y[:, ::5] == 0)
+    y2 = _gpu.bits(mnb.gemv(x, torch.from_numpy(np.full_like(q, 0x88)).cuda(), s, None, "bf16"))
+    assert np.all(y2 == 0)
+
+
+def test_misaligned_activations():
+    M, N, K = 20, 70, 512
+    inp = make_inputs(M, N, K, seed=8)
+    x, q, s, z = _gpu.to_device(inp)
+    buf = torch.empty(M * K + 8, dtype=torch.float16, device="cuda")
+    xm = buf[1:1 + M * K].view(M, K)
+    xm.copy_(x)
+    assert xm.data_ptr() % 16 != 0
+    a = _gpu.bits(mnb.gemv(x, q, s, z, "f16"))
+    b = _gpu.bits(mnb.gemv(xm, q, s, z, "f16"))
+    assert np.array_equal(a, b)
+    _gpu.compare(inp, b, None)
+
+
+def test_weights_ready_chain_matches_plain_calls():
+    """Prefill layers back to back, each reading the previous output, with the
+    early-weights promise give the bits of plain calls."""
+    M = 96
+    layers = [(2048, 2048, 32, False), (1024, 2048, 64, True), (2048, 1024, 128, False)]
+    devs = [_gpu.to_device(make_inputs(M, N, K, seed=70 + i, block=b), symmetric=sym)
+            for i, (N, K, b, sym) in enumerate(layers)]
+    x = devs[0][0]
+    ref, got = [x], [x]
+    for (_, _, b, _), (_, q, s, z) in zip(layers, devs):
+        ref.append(mnb.gemv(ref[-1], q, s, z, "f16", block=b))
+    torch.cuda.synchronize()
+    for (_, _, b, _), (_, q, s, z) in zip(layers, devs):
+        got.append(mnb.gemv(got[-1], q, s, z, "f16", block=b, weights_ready=True))
+    torch.cuda.synchronize()
+    for a, c in zip(ref[1:], got[1:]):
+        assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+        assert torch.isfinite(a.float()).all()
+
+
+def test_decode_batches_keep_their_kernels():
+    """M <= 8 never takes the prefill path."""
+    inp = make_inputs(8, 300, 8192, seed=2)
+    dev = _gpu.to_device(inp)
+    c0 = mnb.counters()
+    _gpu.run(dev, "f16", 0)
+    assert mnb.counters()[16] == c0[16]
+
+
+def test_no_device_error_recorded():
+    assert mnb.device_error() == 0

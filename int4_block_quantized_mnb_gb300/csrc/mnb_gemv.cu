@@ -1367,7 +1367,8 @@ std::atomic<unsigned long long> g_counters[MNB_NUM_COUNTERS];
 
 // mnb_prefill.cu: more than MNB_MAX_M activation rows.
 int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
-                   void* y, int M, int N, int K, int block, int out_bf16, cudaStream_t stream);
+                   void* y, int M, int N, int K, int block, int out_bf16, int sms,
+                   cudaStream_t stream);
 
 // mnb_general.cu: block sizes other than 32 and the symmetric format.
 int launch_general(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
@@ -1788,7 +1789,7 @@ int gemm_prefill(const void* x, const uint8_t* qweight, const void* scales, cons
   int st = device_info(&dev);
   if (st != MNB_OK) return st;
   if ((st = launch_prefill(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
-                           static_cast<cudaStream_t>(stream))) != MNB_OK)
+                           dev.sms, static_cast<cudaStream_t>(stream))) != MNB_OK)
     return st;
   g_counters[0].fetch_add(1, std::memory_order_relaxed);
   g_counters[out_dtype == MNB_OUT_BF16 ? 2 : 1].fetch_add(1, std::memory_order_relaxed);

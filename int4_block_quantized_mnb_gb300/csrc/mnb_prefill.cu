@@ -175,12 +175,173 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) gemm_prefill_kernel(const Pf
     }
 }
 
+
+// ---- pipelined form (16-byte-aligned activations) --------------------------
+//
+// Two stage buffers in dynamic shared memory: while a stage is multiplied, the
+// next stage's raw activations and codes arrive by async copies
+// (cp.async.cg, 16 bytes each) and its scales and zero-points by plain loads
+// held in registers until the stage's arithmetic is done.  Activations are
+// regrouped into the (k, k + 4) pairs at fragment load (four byte permutes).
+constexpr int kXPitch = kPfStage * 64 + 64;    // bytes per activation row of a stage
+constexpr int kCPitch = kPfStage * 16 + 16;    // bytes per weight row of a stage
+constexpr int kXBuf = kPfTok * kXPitch;
+constexpr int kCBuf = kPfRows * kCPitch;
+constexpr int kSBuf = kPfRows * kPfStage * 2;  // at most 8 scales per row and stage
+constexpr int kZBuf = kPfRows * 4;             // at most 4 zero-point bytes per row and stage
+constexpr int kPfSmem = 2 * (kXBuf + kCBuf + kSBuf + kZBuf);
+constexpr int kSPer = kPfRows * kPfStage / (kPfWarps * 32);   // scales per thread per stage
+constexpr int kZPer = kPfRows * 4 / (kPfWarps * 32);          // zero-point bytes per thread
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// kCtas: CTAs one SM holds (2 at 128 registers a thread, 1 above).
+template <int kCtas>
+__global__ void __launch_bounds__(kPfWarps * 32, kCtas) gemm_prefill_pipelined(const PfParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* xb = smem;                              // [2][kXBuf]
+  unsigned char* cb = xb + 2 * kXBuf;                    // [2][kCBuf]
+  uint16_t* sb = reinterpret_cast<uint16_t*>(cb + 2 * kCBuf);   // [2][rows][8]
+  uint8_t* zb = reinterpret_cast<uint8_t*>(sb + 2 * kSBuf / 2); // [2][rows][4]
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  const int nb0 = blockIdx.x * kPfRows;                  // first weight row of the CTA
+  const int m0 = blockIdx.y * kPfTok;
+  const int lr0 = warp * 16 + g, lr1 = lr0 + 8;          // this lane's rows in the CTA
+  const int bper = 1 << p.bshift;                        // chunks per block
+  const int nstages = (p.chunks + kPfStage - 1) / kPfStage;
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  uint16_t spre[kSPer];
+  uint8_t zpre[kZPer];
+  auto fill_async = [&](int st, int bi) {
+    const int cs = st * kPfStage;
+    const int nch = min(kPfStage, p.chunks - cs);
+    const uint32_t xdst = static_cast<uint32_t>(__cvta_generic_to_shared(xb + bi * kXBuf));
+    const uint32_t cdst = static_cast<uint32_t>(__cvta_generic_to_shared(cb + bi * kCBuf));
+    for (int e = threadIdx.x; e < kPfTok * nch * 4; e += kPfWarps * 32) {
+      const int tt = e / (nch * 4), rem = e - tt * (nch * 4);
+      const int m = min(m0 + tt, p.M - 1);                // rows past M repeat row M - 1
+      cp_async16(xdst + tt * kXPitch + rem * 16, p.x + static_cast<size_t>(m) * p.K + 32 * cs + 8 * rem);
+    }
+    for (int e = threadIdx.x; e < kPfRows * nch; e += kPfWarps * 32) {
+      const int r = e / nch, cc = e - r * nch;
+      const int n = min(nb0 + r, p.N - 1);                // rows past N repeat row N - 1
+      cp_async16(cdst + r * kCPitch + cc * 16, p.q + static_cast<size_t>(n) * (p.K / 2) + 16 * (cs + cc));
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  auto load_sz = [&](int st) {
+    const int b0 = (st * kPfStage) >> p.bshift;
+    const int nbk = (min(kPfStage, p.chunks - st * kPfStage) + bper - 1) >> p.bshift;
+    const int nzb = (nbk + 1) >> 1;
+#pragma unroll
+    for (int i = 0; i < kSPer; ++i) {
+      const int e = threadIdx.x + i * kPfWarps * 32;
+      const int r = e / kPfStage, bb = e - r * kPfStage;
+      const int n = min(nb0 + r, p.N - 1);
+      spre[i] = bb < nbk ? __ldg(p.scales + static_cast<size_t>(n) * p.blocks + b0 + bb) : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < kZPer; ++i) {
+      const int e = threadIdx.x + i * kPfWarps * 32;
+      const int r = e >> 2, zz = e & 3;
+      const int n = min(nb0 + r, p.N - 1);
+      zpre[i] = (p.zp && zz < nzb) ? __ldg(p.zp + static_cast<size_t>(n) * p.zstride + (b0 >> 1) + zz) : 0;
+    }
+  };
+  auto store_sz = [&](int bi) {
+#pragma unroll
+    for (int i = 0; i < kSPer; ++i) sb[bi * (kSBuf / 2) + threadIdx.x + i * kPfWarps * 32] = spre[i];
+#pragma unroll
+    for (int i = 0; i < kZPer; ++i) zb[bi * kZBuf + threadIdx.x + i * kPfWarps * 32] = zpre[i];
+  };
+
+  float acc[kPfTiles][4], D[kPfTiles][4];
+#pragma unroll
+  for (int j = 0; j < kPfTiles; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[j][e] = D[j][e] = 0.f;
+
+  fill_async(0, 0);
+  load_sz(0);
+  store_sz(0);
+  for (int st = 0; st < nstages; ++st) {
+    const int bi = st & 1;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();                 // stage st landed and is visible; buffer bi ^ 1 is free
+    const bool more = st + 1 < nstages;
+    if (more) {
+      fill_async(st + 1, bi ^ 1);
+      load_sz(st + 1);
+    }
+    const int cs = st * kPfStage;
+    const int nch = min(kPfStage, p.chunks - cs);
+    const int b0 = cs >> p.bshift;
+    const unsigned char* xs = xb + bi * kXBuf + g * kXPitch + t * 16;
+    const unsigned char* cw = cb + bi * kCBuf + 4 * t;
+    const uint16_t* ss = sb + bi * (kSBuf / 2);
+    const uint8_t* zs = zb + bi * kZBuf;
+    for (int cc = 0; cc < nch; ++cc) {
+      const int c = cs + cc;
+      const int bb = (c >> p.bshift) - b0;
+      uint32_t z0 = 8, z1 = 8;
+      if (p.zp) {
+        const uint32_t sh = (bb & 1) * 4;
+        z0 = (static_cast<uint32_t>(zs[lr0 * 4 + (bb >> 1)]) >> sh) & 0xFu;
+        z1 = (static_cast<uint32_t>(zs[lr1 * 4 + (bb >> 1)]) >> sh) & 0xFu;
+      }
+      uint32_t d0[4], d1[4];
+      pf_dequant(*reinterpret_cast<const uint32_t*>(cw + lr0 * kCPitch + cc * 16), z0, d0);
+      pf_dequant(*reinterpret_cast<const uint32_t*>(cw + lr1 * kCPitch + cc * 16), z1, d1);
+#pragma unroll
+      for (int j = 0; j < kPfTiles; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xs + j * 8 * kXPitch + cc * 64);
+        const uint32_t x04 = __byte_perm(v.x, v.z, 0x5410), x15 = __byte_perm(v.x, v.z, 0x7632);
+        const uint32_t x26 = __byte_perm(v.y, v.w, 0x5410), x37 = __byte_perm(v.y, v.w, 0x7632);
+        mma_16816(D[j], d0[0], d1[0], d0[1], d1[1], x04, x15, D[j]);
+        mma_16816(D[j], d0[2], d1[2], d0[3], d1[3], x26, x37, D[j]);
+      }
+      if ((c & (bper - 1)) == bper - 1) {                  // the block ends here
+        const float s0 = __half2float(__ushort_as_half(ss[lr0 * kPfStage + bb]));
+        const float s1 = __half2float(__ushort_as_half(ss[lr1 * kPfStage + bb]));
+#pragma unroll
+        for (int j = 0; j < kPfTiles; ++j) {
+          acc[j][0] = fmaf(D[j][0], s0, acc[j][0]);
+          acc[j][1] = fmaf(D[j][1], s0, acc[j][1]);
+          acc[j][2] = fmaf(D[j][2], s1, acc[j][2]);
+          acc[j][3] = fmaf(D[j][3], s1, acc[j][3]);
+          D[j][0] = D[j][1] = D[j][2] = D[j][3] = 0.f;
+        }
+      }
+    }
+    if (more) store_sz(bi ^ 1);
+  }
+  const int r0 = nb0 + lr0, r1 = nb0 + lr1;
+#pragma unroll
+  for (int j = 0; j < kPfTiles; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int n = e < 2 ? r0 : r1;
+      const int m = m0 + 8 * j + 2 * t + (e & 1);
+      if (n < p.N && m < p.M)
+        pf_store(p.y, static_cast<size_t>(m) * p.N + n, acc[j][e], p.out_bf16);
+    }
+}
+
 }  // namespace
 
 // Launches the prefill GEMM; arguments are validated by the caller (M > 8,
 // block 32, 64 or 128, K a multiple of 32 and of the block size).
 int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
-                   void* y, int M, int N, int K, int block, int out_bf16, cudaStream_t stream) {
+                   void* y, int M, int N, int K, int block, int out_bf16, int sms,
+                   cudaStream_t stream) {
   PfParams p{};
   p.x = static_cast<const uint16_t*>(x);
   p.q = qweight;
@@ -211,8 +372,18 @@ int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, co
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[1] = {&p};
-  const cudaError_t e =
-      cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&gemm_prefill_kernel), args);
+  const void* fn = reinterpret_cast<const void*>(&gemm_prefill_kernel);
+  if (p.x_aligned) {                 // the async copies want 16-byte-aligned rows
+    // two CTAs per SM only when the grid needs them: a small grid would be
+    // packed two to an SM and leave SMs idle
+    fn = gx * gy > sms ? reinterpret_cast<const void*>(&gemm_prefill_pipelined<2>)
+                       : reinterpret_cast<const void*>(&gemm_prefill_pipelined<1>);
+    cfg.dynamicSmemBytes = kPfSmem;
+    const cudaError_t ea =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (ea != cudaSuccess) return cuda_fail(ea, "cudaFuncSetAttribute(prefill)");
+  }
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC(prefill)");
   g_counters[16].fetch_add(1, std::memory_order_relaxed);
   return MNB_OK;

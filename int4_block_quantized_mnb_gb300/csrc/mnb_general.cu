@@ -12,8 +12,8 @@
 // with the block size as a parameter: scales [N][K/B], zero-points
 // [N][ceil(K/B/2)] with the low nibble holding the even block.
 //
-// Kernel shape.  A CTA of W = P * S warps takes P row groups (four rows for
-// M <= 2, two above); the S warps of a group split K into S contiguous ranges
+// Kernel shape.  A CTA of W = P * S warps takes P row groups (four rows per
+// warp for M <= 2; sixteen above, see gemv_general_wide); the S warps of a group split K into S contiguous ranges
 // of 32-k chunks, and lane l of a warp takes chunks l, l + 32, ... of its
 // range.  A chunk of one row is 16 bytes of codes (one vector load) and its
 // block's scale and zero-point (two for block 16, where a chunk spans two
@@ -143,9 +143,10 @@ __device__ __forceinline__ void chunk_dot(const uint32_t* d, const uint4 (&xr)[4
   }
 }
 
-// Rows per warp: four while the batch is small, two for M > 2 (registers,
-// with two CTAs per SM).
-constexpr int gen_rows(int M) { return M <= 2 ? 4 : 2; }
+// Rows per warp: four (lanes over chunks) for M <= 2; sixteen for M > 2,
+// where lane (q, rr) takes rows rr and rr + 8 and every fourth chunk, so the
+// eight lanes of a quarter warp share each activation load.
+constexpr int gen_rows(int M) { return M <= 2 ? 4 : 16; }
 
 // Staged activations at most; larger batches read them from global memory.
 constexpr int kGenXSmemMax = 96 * 1024;
@@ -321,6 +322,150 @@ __global__ void __launch_bounds__(kGenWarps * 32, 2) gemv_general_kernel(const G
         gen_store(p.y, static_cast<size_t>(m) * p.N + row0 + i, acc[i][m], p.out_bf16);
 }
 
+// M > 2: lane (q, rr) = (lane >> 3, lane & 7) takes weight rows rr and rr + 8
+// of the warp's 16 and chunks q, q + 4, ... of the warp's K range.  Each row's
+// chunk is dequantized once for all M activation rows, and one activation load
+// (the same address for the eight lanes of a quarter warp) serves both rows.
+template <int M, bool kB16>
+__global__ void __launch_bounds__(kGenWarps * 32, 2) gemv_general_wide(const GenParams p) {
+  extern __shared__ uint4 xs[];
+  __shared__ float red[kGenWarps][2][M][8];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rr = lane & 7;
+  const int q4 = lane >> 3;
+  const int grp = warp / p.split;
+  const int part = warp - grp * p.split;
+  const int row0 = (blockIdx.x * p.pairs + grp) * 16;
+  const int c_begin = static_cast<int>(static_cast<long long>(part) * p.chunks / p.split);
+  const int c_end = static_cast<int>(static_cast<long long>(part + 1) * p.chunks / p.split);
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (p.x_smem) {
+    const int per_m = 4 * p.chunks;
+    for (int e = threadIdx.x; e < M * per_m; e += blockDim.x) {
+      const int m = e / per_m;
+      const int rem = e - m * per_m;
+      const int c = rem >> 2, g = rem & 3;
+      const uint16_t* src = p.x + static_cast<size_t>(m) * p.K + 32 * c + 8 * g;
+      uint4 v;
+      if (p.x_aligned) {
+        v = __ldg(reinterpret_cast<const uint4*>(src));
+      } else {
+        v.x = __ldg(src + 0) | (static_cast<uint32_t>(__ldg(src + 1)) << 16);
+        v.y = __ldg(src + 2) | (static_cast<uint32_t>(__ldg(src + 3)) << 16);
+        v.z = __ldg(src + 4) | (static_cast<uint32_t>(__ldg(src + 5)) << 16);
+        v.w = __ldg(src + 6) | (static_cast<uint32_t>(__ldg(src + 7)) << 16);
+      }
+      xs[(m * 4 + g) * p.chunks + c] = pair_k4(v);
+    }
+    __syncthreads();
+  }
+
+  float acc[2][M];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
+  const int ra = min(row0 + rr, p.N - 1), rb = min(row0 + rr + 8, p.N - 1);
+  if (row0 < p.N) {
+#pragma unroll 2
+    for (int c = c_begin + q4; c < c_end; c += 4) {
+      uint4 w[2];
+      float s0[2], s1[2];
+      uint32_t zl0[2], zh0[2], zl1[2], zh1[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int r = i ? rb : ra;
+        w[i] = __ldg(reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(r) * (p.K / 2)) + c);
+        const uint16_t* srow = p.scales + static_cast<size_t>(r) * p.blocks;
+        uint32_t z0 = 8, z1 = 8;
+        if (kB16) {
+          s0[i] = f16_bits_to_float(__ldg(srow + 2 * c));
+          s1[i] = f16_bits_to_float(__ldg(srow + 2 * c + 1));
+          if (p.zp) {
+            const uint32_t zb = __ldg(p.zp + static_cast<size_t>(r) * p.zstride + c);
+            z0 = zb & 0xFu;
+            z1 = zb >> 4;
+          }
+        } else {
+          const int b = c >> p.bshift;
+          s0[i] = f16_bits_to_float(__ldg(srow + b));
+          s1[i] = 0.f;
+          if (p.zp) {
+            const uint32_t zb = __ldg(p.zp + static_cast<size_t>(r) * p.zstride + (b >> 1));
+            z0 = (b & 1) ? (zb >> 4) : (zb & 0xFu);
+          }
+          z1 = z0;
+        }
+        zp_bias(z0, zl0[i], zh0[i]);
+        zp_bias(z1, zl1[i], zh1[i]);
+      }
+      uint32_t d[2][16];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        dequant_word(w[i].x, zl0[i], zh0[i], d[i] + 0);
+        dequant_word(w[i].y, zl0[i], zh0[i], d[i] + 4);
+        dequant_word(w[i].z, zl1[i], zh1[i], d[i] + 8);
+        dequant_word(w[i].w, zl1[i], zh1[i], d[i] + 12);
+      }
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        uint4 xr[4];
+        if (p.x_smem) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) xr[g] = xs[(m * 4 + g) * p.chunks + c];
+        } else {
+          load_x_chunk(p, m, c, xr);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) chunk_dot<kB16>(d[i], xr, s0[i], s1[i], acc[i][m]);
+      }
+    }
+  }
+  // the four chunk lanes of each row, in a fixed order
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      float v = acc[i][m];
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+      acc[i][m] = v;
+    }
+  if (p.split > 1) {
+    if (q4 == 0) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int m = 0; m < M; ++m) red[warp][i][m][rr] = acc[i][m];
+    }
+    __syncthreads();
+    if (part != 0) return;
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        float v = red[warp][i][m][rr];
+        for (int j = 1; j < p.split; ++j) v += red[warp + j][i][m][rr];
+        acc[i][m] = v;
+      }
+  }
+  if (q4 == 0) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = row0 + rr + 8 * i;
+      if (r < p.N) {
+#pragma unroll
+        for (int m = 0; m < M; ++m)
+          gen_store(p.y, static_cast<size_t>(m) * p.N + r, acc[i][m], p.out_bf16);
+      }
+    }
+  }
+}
+
 using GenFn = void (*)(const GenParams);
 
 template <bool kB16>
@@ -328,12 +473,12 @@ GenFn general_kernel_for(int M) {
   switch (M) {
     case 1: return &gemv_general_kernel<1, kB16>;
     case 2: return &gemv_general_kernel<2, kB16>;
-    case 3: return &gemv_general_kernel<3, kB16>;
-    case 4: return &gemv_general_kernel<4, kB16>;
-    case 5: return &gemv_general_kernel<5, kB16>;
-    case 6: return &gemv_general_kernel<6, kB16>;
-    case 7: return &gemv_general_kernel<7, kB16>;
-    default: return &gemv_general_kernel<8, kB16>;
+    case 3: return &gemv_general_wide<3, kB16>;
+    case 4: return &gemv_general_wide<4, kB16>;
+    case 5: return &gemv_general_wide<5, kB16>;
+    case 6: return &gemv_general_wide<6, kB16>;
+    case 7: return &gemv_general_wide<7, kB16>;
+    default: return &gemv_general_wide<8, kB16>;
   }
 }
 
@@ -347,14 +492,15 @@ int log2_exact(int v) {
 
 // Warps per row group (S) without a requested split: the fewest of 1, 2, 4,
 // 8 that give every SM a CTA (two are resident per SM, so this stays within
-// one wave where the rows allow), and no more than leave every lane of a warp
-// at least one chunk.  A requested split_k becomes S (at most 8).
+// one wave where the rows allow), and no more than leave every chunk lane of a
+// warp (32 for M <= 2, 4 above) at least one chunk.  A requested split_k becomes S (at most 8).
 int general_split(int M, int N, int K, int split_k, int sms) {
   if (split_k > 0) return std::min(split_k, kGenWarps);
   const int chunks = K / 32;
   const int rows_warp = gen_rows(M);
+  const int chunk_lanes = M <= 2 ? 32 : 4;      // lanes of a warp that split its chunks
   int s = 1;
-  while (s < kGenWarps && s * 2 * 32 <= chunks) {
+  while (s < kGenWarps && s * 2 * chunk_lanes <= chunks) {
     const long long rows_cta = static_cast<long long>(rows_warp) * (kGenWarps / s);
     const long long ctas = (N + rows_cta - 1) / rows_cta;
     if (ctas >= sms) break;
@@ -385,8 +531,9 @@ int launch_general(const void* x, const uint8_t* qweight, const void* scales, co
   p.out_bf16 = out_bf16;
   p.x_aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   const size_t x_bytes = static_cast<size_t>(M) * K * 2;
-  // staging pays where each lane of a warp has at least four chunks of its range
-  p.x_smem = x_bytes <= static_cast<size_t>(kGenXSmemMax) && p.chunks / p.split >= 4 * 32;
+  // staging pays where each chunk lane of a warp has at least four chunks
+  p.x_smem = x_bytes <= static_cast<size_t>(kGenXSmemMax) &&
+             p.chunks / p.split >= 4 * (M <= 2 ? 32 : 4);
   const long long rows_cta = static_cast<long long>(gen_rows(M)) * p.pairs;
   const long long grid = (N + rows_cta - 1) / rows_cta;
   if (grid > 0x7FFFFFFFLL) return fail(MNB_ERR_SHAPE, "N too large");

@@ -8,7 +8,8 @@ import subprocess
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SOURCES = [os.path.join(PKG, "csrc", "mnb_gemv.cu"), os.path.join(PKG, "csrc", "mnb_general.cu"),
-           os.path.join(PKG, "csrc", "mnb_prefill.cu"), os.path.join(PKG, "csrc", "mnb_cast.cu")]
+           os.path.join(PKG, "csrc", "mnb_prefill.cu"), os.path.join(PKG, "csrc", "mnb_prefill_tc.cu"),
+           os.path.join(PKG, "csrc", "mnb_cast.cu")]
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(PKG, "libmnb.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

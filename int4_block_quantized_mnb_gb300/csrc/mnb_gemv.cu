@@ -1365,6 +1365,11 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 std::atomic<unsigned long long> g_counters[MNB_NUM_COUNTERS];
 
+// mnb_prefill_tc.cu: the prefill GEMM on tcgen05 (MNB_FLAG_TENSOR_CORES).
+int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
+                      void* y, int M, int N, int K, int block, int out_bf16, unsigned int* err,
+                      int sms, cudaStream_t stream);
+
 // mnb_prefill.cu: more than MNB_MAX_M activation rows.
 int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                    void* y, int M, int N, int K, int block, int out_bf16, int sms,
@@ -1380,6 +1385,7 @@ struct DeviceInfo {
   int sms = 0;
   int major = 0, minor = 0;
   size_t smem_optin = 0;
+  unsigned int* err = nullptr;   // this device's g_device_error
 };
 
 constexpr int kMaxDevices = 64;
@@ -1404,6 +1410,10 @@ int device_info(DeviceInfo* out) {
     if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute(smem)");
     d.smem_optin = static_cast<size_t>(v);
+    void* err = nullptr;
+    if ((e = cudaGetSymbolAddress(&err, g_device_error)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(device error)");
+    d.err = static_cast<unsigned int*>(err);
     d.ready = true;
   }
   if (d.major != 10 || d.minor != 3)
@@ -1764,7 +1774,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // The prefill path (M > MNB_MAX_M): its own checks, then one launch.
 int gemm_prefill(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                  void* y, int M, int N, int K, int block, int out_dtype, int split_k,
-                 void* stream) {
+                 unsigned int flags, void* stream) {
   if (block == 16) return fail(MNB_ERR_BLOCK, "the prefill path takes block 32, 64 or 128");
   if (N < 1) return fail(MNB_ERR_SHAPE, "N must be >= 1");
   if (K < kBlock || K % kBlock != 0 || K % block != 0)
@@ -1788,9 +1798,19 @@ int gemm_prefill(const void* x, const uint8_t* qweight, const void* scales, cons
   DeviceInfo dev;
   int st = device_info(&dev);
   if (st != MNB_OK) return st;
-  if ((st = launch_prefill(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
-                           dev.sms, static_cast<cudaStream_t>(stream))) != MNB_OK)
-    return st;
+  // tcgen05 form on request, where the activations are 16-byte aligned
+  const bool tc = (flags & MNB_FLAG_TENSOR_CORES) && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  if (tc)
+    st = launch_prefill_tc(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
+                           dev.err, dev.sms, static_cast<cudaStream_t>(stream));
+  else
+    st = launch_prefill(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
+                        dev.sms, static_cast<cudaStream_t>(stream));
+  if (st != MNB_OK) return st;
+  if (tc) {
+    g_counters[12].fetch_add(1, std::memory_order_relaxed);
+    g_counters[16].fetch_add(1, std::memory_order_relaxed);
+  }
   g_counters[0].fetch_add(1, std::memory_order_relaxed);
   g_counters[out_dtype == MNB_OUT_BF16 ? 2 : 1].fetch_add(1, std::memory_order_relaxed);
   return MNB_OK;
@@ -1862,7 +1882,8 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   if (block != 16 && block != 32 && block != 64 && block != 128)
     return fail(MNB_ERR_BLOCK, "block size must be 16, 32, 64 or 128");
   if (M > kMaxM && M <= MNB_MAX_PREFILL_M)
-    return gemm_prefill(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, stream);
+    return gemm_prefill(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, flags,
+                        stream);
   int st = check_shape(M, N, K);
   if (st != MNB_OK) return st;
   if (K % block != 0) return fail(MNB_ERR_SHAPE, "K must be a multiple of the block size");

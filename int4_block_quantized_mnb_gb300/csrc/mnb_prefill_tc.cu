@@ -1,0 +1,455 @@
+// mnb_prefill_tc.cu -- the prefill GEMM (M > 8) on the fifth-generation tensor
+// cores: tcgen05.mma with fp32 accumulators in tensor memory (TMEM).
+//
+// Exactness.  Each dequantized weight w = (q - zp) s has at most 15
+// significant bits (4 of q - zp, 11 of the fp16 scale), so it splits exactly
+// into hi = fp16(w) and lo = w - hi, and lo' = lo 2^11 is an fp16 value as
+// well (at most 4 significant bits, at most |hi| in magnitude; normal for
+// |w| >= 2^-11).  Two fp16 GEMMs then give exact products x hi and x lo' with
+// fp32 sums: y = D_hi + 2^-11 D_lo.  No per-block scaling is needed, so both
+// accumulators stay in TMEM across the whole K loop.
+//
+// Tile.  A CTA computes 128 weight rows x 128 or 256 activation rows (UMMA
+// M = 128, N = 128 or 256) in K steps of 64.  Per step its 256 or 512 threads write, in the
+// 128-byte swizzled K-major layout the tensor core reads, the hi and lo tiles
+// of the weights (thread = one row x 32 or 16 k: one code load, its block's
+// scale and zero-point) and the activation tile, from registers loaded one
+// step ahead; both keep the dequant's (k, k + 4)
+// pairing (the same permutation of k in both operands leaves each dot product
+// unchanged).  One thread issues the eight MMAs of the step (hi and lo, four
+// K = 16 slices each) and commits them to the step buffer's mbarrier; the
+// buffer is refilled two steps later, after that barrier completes.  The
+// epilogue reads TMEM (warp w: lanes 32 (w mod 4) .. + 31, 32 columns by w / 4),
+// forms D_hi + 2^-11 D_lo, rounds once to fp16 and, on the bf16 arm, narrows.
+#include "mnb.h"
+#include "mnb_dequant.cuh"
+#include "mnb_narrow.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <string>
+
+namespace mnb {
+
+int fail(int status, const std::string& detail);
+int cuda_fail(cudaError_t e, const char* what);
+extern std::atomic<unsigned long long> g_counters[MNB_NUM_COUNTERS];
+
+namespace {
+
+constexpr int kTcRows = 128;                 // weight rows per CTA (UMMA M)
+constexpr int kTcK = 64;                     // k per step: one 128-byte swizzle row of fp16
+constexpr int kTcTile = 128 * 128;           // bytes of one 128 x 64 fp16 tile
+// Per activation-tile width kTok (UMMA N, 128 or 256): one step's buffer
+// holds the hi and lo weight tiles and kTok / 128 activation tiles; TMEM
+// holds D_hi (columns 0 .. kTok - 1) and D_lo (kTok .. 2 kTok - 1).
+constexpr int tc_buf(int kTok) { return (2 + kTok / 128) * kTcTile; }
+constexpr int tc_smem(int kTok) { return 2 * tc_buf(kTok) + 1024 + 64; }   // + alignment, barriers
+constexpr int tc_cols(int kTok) { return 2 * kTok; }
+constexpr unsigned kTcErrMma = 5;            // device error: MMA completion never arrived
+constexpr unsigned long long kTcWaitNs = 2000000000ull;
+
+struct TcParams {
+  const uint16_t* x;
+  const uint8_t* q;
+  const uint16_t* scales;
+  const uint8_t* zp;
+  void* y;
+  int M, N, K;
+  int blocks, zstride, block;
+  int out_bf16;
+  unsigned int* err;                         // the device error word (mnb_device_error)
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Byte offset of 16-byte chunk j (k = 8 j .. 8 j + 7) of row r in a 128-row,
+// 64-k fp16 tile in the 128-byte swizzled K-major layout: 8-row groups of
+// 1024 bytes, rows of 128 bytes, chunk index XOR (r mod 8).
+__device__ __forceinline__ uint32_t sw128(int r, int j) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
+}
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled tile:
+// start address >> 4 (bits 0-13), leading offset 1 (unused for this layout,
+// bits 16-29), stride between 8-row groups 1024 >> 4 (bits 32-45), descriptor
+// version 1 (bits 46-47), swizzle mode 2 = 128 bytes (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), fp16 A
+// and B (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t tc_idesc(int kTok) {
+  return (1u << 4) | (static_cast<uint32_t>(kTok >> 3) << 17) | ((kTcRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ bool tc_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long tc_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for an MMA commit; false (and the device error word set) when
+// the completion did not arrive within the limit.
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
+  if (tc_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = tc_now();
+  while (!tc_try_wait(bar, parity)) {
+    if (tc_now() - t0 > kTcWaitNs) {
+      atomicCAS(err, 0u, kTcErrMma);
+      return false;
+    }
+  }
+  return true;
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// hi = fp16(d s) and lo' = (d s - hi) 2^11, both exact fp16, for one pair.
+// For |s| <= 2 (so |hi| <= 30 and both s 2^11 and hi 2^11 stay finite) one packed fp16 FMA
+// forms lo' exactly: its exact value has at most 4 significant bits and is
+// no larger than |hi 2^11|, so the single rounding leaves it unchanged.
+// Larger scales take the fp32 form.
+__device__ __forceinline__ void split_pair(uint32_t d, float s, uint32_t s2, uint32_t s2k,
+                                           bool small, uint32_t& hi, uint32_t& lo) {
+  hi = hmul2(d, s2);
+  if (small) {
+    const uint32_t hk = hmul2(hi, 0x68006800u);                  // hi 2^11, exact
+    lo = hfma2(d, s2k, hk ^ 0x80008000u);                        // d s 2^11 - hi 2^11
+    return;
+  }
+  const __half2 dh = *reinterpret_cast<const __half2*>(&d);
+  const __half2 hh = *reinterpret_cast<const __half2*>(&hi);
+  const float l0 = fmaf(__low2float(dh), s, -__low2float(hh)) * 2048.f;    // exact in fp32
+  const float l1 = fmaf(__high2float(dh), s, -__high2float(hh)) * 2048.f;
+  const __half2 lh = __floats2half2_rn(l0, l1);                           // exact: <= 4 bits
+  lo = *reinterpret_cast<const uint32_t*>(&lh);
+}
+
+__device__ __forceinline__ void pf_out(void* y, size_t idx, float v, int out_bf16) {
+  const __half h = __float2half_rn(v);
+  if (out_bf16)
+    static_cast<uint16_t*>(y)[idx] = narrow_f16_bits_to_bf16(__half_as_ushort(h));
+  else
+    static_cast<__half*>(y)[idx] = h;
+}
+
+// kThreads: 512 (one CTA per SM, for grids no larger than the SM count) or
+// 256 (two CTAs per SM).  A thread handles one weight row x kKPer k and
+// kXPer activation chunks per step.
+template <int kThreads, int kTok>
+__global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p) {
+  constexpr int kTcThreads = kThreads;
+  constexpr int kTcTok = kTok;
+  constexpr int kTcBuf = tc_buf(kTok);
+  constexpr int kTcCols = tc_cols(kTok);
+  constexpr int kKPer = kTcRows * kTcK / kThreads;           // 16 or 32 k per thread
+  constexpr int kWords = kKPer / 8;
+  constexpr int kTcXPer = kTcTok * kTcK / 8 / kThreads;      // activation chunks per thread
+  constexpr int kParts = kTcK / kKPer;                       // threads per weight row
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kTcBuf);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 2 * kTcBuf + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 2 * kTcBuf + 32);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int n0 = blockIdx.x * kTcRows;
+  const int m0 = blockIdx.y * kTcTok;
+  const uint32_t bar0 = smem_addr(bars), bar1 = bar0 + 8;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar1) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kTcCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // this thread's weight row and 32-k half of every step
+  const int wr = tid / kParts, qk = tid % kParts;    // weight row, kKPer-k part of the step
+  const int wrow = min(n0 + wr, p.N - 1);            // rows past N repeat row N - 1
+  const uint8_t* qrow = p.q + static_cast<size_t>(wrow) * (p.K / 2);
+  const uint16_t* srow = p.scales + static_cast<size_t>(wrow) * p.blocks;
+  const uint8_t* zrow = p.zp ? p.zp + static_cast<size_t>(wrow) * p.zstride : nullptr;
+  const int nsteps = (p.K + kTcK - 1) / kTcK;
+  bool ok = true;
+
+  // Each thread's global inputs of a step (its weight row's 32 codes, scale
+  // and zero-point, four activation chunks), loaded one step ahead.
+  struct StepIn {
+    uint32_t w[kWords];
+    float s;
+    uint32_t z;
+    uint4 xv[kTcXPer];
+  };
+  auto load_step = [&](int st, StepIn& in) {
+    const int k0 = st * kTcK;
+    const int kk = k0 + kKPer * qk;
+#pragma unroll
+    for (int i = 0; i < kWords; ++i) in.w[i] = 0u;
+    in.s = 0.f;
+    in.z = 8;
+    if (kk < p.K) {                                  // zero past K (K is a multiple of 32)
+      if constexpr (kWords == 4) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow + kk / 2));
+        in.w[0] = v.x; in.w[1] = v.y; in.w[2] = v.z; in.w[3] = v.w;
+      } else {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(qrow + kk / 2));
+        in.w[0] = v.x; in.w[1] = v.y;
+      }
+      const int b = kk / p.block;
+      in.s = __half2float(__ushort_as_half(__ldg(srow + b)));
+      if (zrow) {
+        const uint32_t zb = __ldg(zrow + (b >> 1));
+        in.z = (b & 1) ? (zb >> 4) : (zb & 0xFu);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kTcXPer; ++i) {
+      const int item = tid + i * kTcThreads;
+      const int tt = item >> 3, cj = item & 7;
+      const int m = min(m0 + tt, p.M - 1);           // rows past M repeat row M - 1
+      const int kx = k0 + 8 * cj;
+      in.xv[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (kx < p.K)
+        in.xv[i] = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K + kx));
+    }
+  };
+
+  // Thread 0 alone waits on the MMA commits and publishes the outcome; every
+  // branch on it follows a barrier, so all threads take the same path.
+  StepIn cur, nxt;
+  load_step(0, cur);
+  for (int st = 0; st < nsteps && ok; ++st) {
+    const int bi = st & 1;
+    unsigned char* buf = smem + bi * kTcBuf;
+    // the buffer's MMAs of two steps ago must be done before it is rewritten
+    if (st >= 2) {
+      if (tid == 0 && !tc_wait(bi ? bar1 : bar0, ((st - 2) >> 1) & 1, p.err)) *abort_flag = 1;
+      __syncthreads();
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
+    }
+    // weights: row wr, k = kKPer qk .. + kKPer of the step, as exact hi and lo parts
+    {
+      const __half sh = __float2half_rn(cur.s);      // s is an fp16 value: exact
+      const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x00010001u;
+      const bool small = fabsf(cur.s) <= 2.f;
+      const __half shk = __float2half_rn(small ? cur.s * 2048.f : 0.f);   // exact when small
+      const uint32_t s2k = static_cast<uint32_t>(__half_as_ushort(shk)) * 0x00010001u;
+      const uint32_t zl = cur.z * 0x00010001u + 0x64006400u;
+      const uint32_t zh = cur.z * 0x00100010u + 0x54005400u;
+#pragma unroll
+      for (int g = 0; g < kWords; ++g) {
+        const uint32_t word = cur.w[g], w8 = word >> 8;
+        uint32_t d[4] = {hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl),
+                         hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh),
+                         hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl),
+                         hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh)};
+        uint4 hi, lo;
+        split_pair(d[0], cur.s, s2, s2k, small, hi.x, lo.x);
+        split_pair(d[1], cur.s, s2, s2k, small, hi.y, lo.y);
+        split_pair(d[2], cur.s, s2, s2k, small, hi.z, lo.z);
+        split_pair(d[3], cur.s, s2, s2k, small, hi.w, lo.w);
+        const uint32_t off = sw128(wr, kWords * qk + g);
+        *reinterpret_cast<uint4*>(buf + off) = hi;
+        *reinterpret_cast<uint4*>(buf + kTcTile + off) = lo;
+      }
+    }
+    // activations: 128 rows x 8 chunks of 8 k, regrouped into the same pairs
+#pragma unroll
+    for (int i = 0; i < kTcXPer; ++i) {
+      const int item = tid + i * kTcThreads;
+      const int tt = item >> 3, cj = item & 7;
+      *reinterpret_cast<uint4*>(buf + 2 * kTcTile + sw128(tt, cj)) = pair_k4(cur.xv[i]);
+    }
+    if (st + 1 < nsteps) load_step(st + 1, nxt);     // in flight while this step multiplies
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t a_hi = smem_addr(buf), a_lo = a_hi + kTcTile, bx = a_hi + 2 * kTcTile;
+#pragma unroll
+      for (int ks = 0; ks < kTcK / 16; ++ks) {       // K = 16 slices: 32 bytes apart
+        const uint32_t acc = (st > 0 || ks > 0) ? 1u : 0u;
+        tc_mma(tmem, sw128_desc(a_hi + 32 * ks), sw128_desc(bx + 32 * ks), tc_idesc(kTok), acc);
+        tc_mma(tmem + kTcTok, sw128_desc(a_lo + 32 * ks), sw128_desc(bx + 32 * ks),
+               tc_idesc(kTok), acc);
+      }
+      tc_commit(bi ? bar1 : bar0);
+    }
+    cur = nxt;
+  }
+  // wait for the last step's MMAs (and the one before, on the other buffer)
+  if (ok && tid == 0) {
+    const int last = nsteps - 1;
+    if (last >= 1 && !tc_wait(((last - 1) & 1) ? bar1 : bar0, ((last - 1) >> 1) & 1, p.err))
+      *abort_flag = 1;
+    else if (!tc_wait((last & 1) ? bar1 : bar0, (last >> 1) & 1, p.err))
+      *abort_flag = 1;
+  }
+  __syncthreads();
+  ok = *abort_flag == 0;
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (ok) {
+    // warp w: TMEM lanes 32 (w mod 4) .., a 1/(warps/4) share of the columns
+    constexpr int kColsPerWarp = kTcTok / (kThreads / 128);
+    const int lane_base = 32 * (warp & 3);
+    const int col0 = kColsPerWarp * (warp >> 2);
+    const int n = n0 + lane_base + lane;
+#pragma unroll 1
+    for (int cc = 0; cc < kColsPerWarp / 32; ++cc) {
+      const int col = col0 + 32 * cc;
+      float vh[32], vl[32];
+      tc_ld32(tmem + (static_cast<uint32_t>(lane_base) << 16) + col, vh);
+      tc_ld32(tmem + (static_cast<uint32_t>(lane_base) << 16) + kTcTok + col, vl);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int m = m0 + col + j;
+        if (n < p.N && m < p.M)
+          pf_out(p.y, static_cast<size_t>(m) * p.N + n, fmaf(vl[j], 1.f / 2048.f, vh[j]),
+                 p.out_bf16);
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcCols)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+// Launches the tensor-memory prefill GEMM; the caller has validated the
+// arguments and checked that x is 16-byte aligned.
+int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
+                      void* y, int M, int N, int K, int block, int out_bf16, unsigned int* err,
+                      int sms, cudaStream_t stream) {
+  TcParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.q = qweight;
+  p.scales = static_cast<const uint16_t*>(scales);
+  p.zp = zp;
+  p.y = y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.block = block;
+  p.blocks = K / block;
+  p.zstride = (p.blocks + 1) / 2;
+  p.out_bf16 = out_bf16;
+  p.err = err;
+  // Activation tiles of 256 rows (one 512-thread CTA per SM, all of TMEM)
+  // where that still gives every SM a CTA; else 128 rows, with 512 threads
+  // while the grid leaves SMs to spare and two 256-thread CTAs per SM above.
+  const long long gx = (static_cast<long long>(N) + kTcRows - 1) / kTcRows;
+  const bool t256 = gx * ((static_cast<long long>(M) + 255) / 256) >= sms;
+  const int tok = t256 ? 256 : 128;
+  const long long gy = (static_cast<long long>(M) + tok - 1) / tok;
+  if (gx > 0x7FFFFFFFLL || gy > 65535) return fail(MNB_ERR_SHAPE, "prefill shape too large");
+  const bool wide = t256 || gx * gy <= sms;
+  const void* fn = t256   ? reinterpret_cast<const void*>(&gemm_prefill_tc<512, 256>)
+                   : wide ? reinterpret_cast<const void*>(&gemm_prefill_tc<512, 128>)
+                          : reinterpret_cast<const void*>(&gemm_prefill_tc<256, 128>);
+  const int smem = tc_smem(tok);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill tc)");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  cfg.blockDim = dim3(wide ? 512 : 256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[1] = {&p};
+  e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC(prefill tc)");
+  return MNB_OK;
+}
+
+}  // namespace mnb

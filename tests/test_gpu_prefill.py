@@ -21,12 +21,14 @@ def built():
     mnb.load()
 
 
-def _run_both(inp, symmetric, cols=None):
+def _run_both(inp, symmetric, cols=None, tensor_cores=False):
     dev = _gpu.to_device(inp, symmetric=symmetric)
     c0 = mnb.counters()
-    y16 = _gpu.bits(_gpu.run(dev, "f16", 0, block=inp.block))
-    ybf = _gpu.bits(_gpu.run(dev, "bf16", 0, block=inp.block))
-    assert mnb.counters()[16] - c0[16] == 2
+    y16 = _gpu.bits(_gpu.run(dev, "f16", 0, block=inp.block, tensor_cores=tensor_cores))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16", 0, block=inp.block, tensor_cores=tensor_cores))
+    c1 = mnb.counters()
+    assert c1[16] - c0[16] == 2
+    assert c1[12] - c0[12] == (2 if tensor_cores else 0)      # tcgen05 form only on request
     return _gpu.compare(inp, y16, ybf, cols=cols, symmetric=symmetric)
 
 
@@ -50,6 +52,31 @@ def test_full_size(M, N, K, block, symmetric):
     cols = np.random.default_rng(M).choice(N, size=min(N, 96), replace=False)
     cols.sort()
     _run_both(inp, symmetric, cols=cols)
+
+
+@pytest.mark.parametrize("block,symmetric", FORMATS, ids=FORMAT_IDS)
+@pytest.mark.parametrize("M", [9, 64, 130, 257])
+@pytest.mark.parametrize("N,K", [(1, 128), (33, 96), (130, 1024), (257, 384)])
+def test_tensor_core_small_shapes(block, symmetric, M, N, K):
+    """The tcgen05 form (MNB_FLAG_TENSOR_CORES): each weight split exactly into
+    two fp16 parts, fp32 accumulators in tensor memory; same bound."""
+    if K % block:
+        pytest.skip("K not a multiple of the block size")
+    inp = make_inputs(M, N, K, seed=M * 13 + N + K + block, block=block)
+    _run_both(inp, symmetric, tensor_cores=True)
+
+
+@pytest.mark.parametrize("M,N,K,block,symmetric", [
+    (512, 4096, 4096, 32, False), (300, 27648, 5120, 64, True), (1000, 1024, 8192, 128, False),
+    (300, 19456, 256, 32, False), (2100, 19456, 512, 64, True),
+])
+def test_tensor_core_full_size(M, N, K, block, symmetric):
+    """Prefill-sized layers on the tcgen05 form (128- and 256-row activation
+    tiles), compared on sampled output columns."""
+    inp = make_inputs(M, N, K, seed=M + N + block + 1, block=block)
+    cols = np.random.default_rng(M + 1).choice(N, size=min(N, 96), replace=False)
+    cols.sort()
+    _run_both(inp, symmetric, cols=cols, tensor_cores=True)
 
 
 def test_exact_zero_rows():

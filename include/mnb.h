@@ -139,19 +139,20 @@ int mnb_gemv(const void *x, const uint8_t *qweight, const void *scales, const ui
 #define MNB_FLAG_WEIGHTS_READY 1u
 
 /*
- * MNB_FLAG_TENSOR_CORES: permit the tensor-core kernel where it applies (no K
- * split, K a multiple of 1024, scales and zp 16-byte aligned, M * K at most
- * 33792).  It forms the same exact fp16 products (q - zp) * x and accumulates
- * them in fp32 with mma.sync m16n8k16 instead of fp32 FMAs; results meet the
- * same error bound and bf16 invariant, but their bits may differ from the
- * default kernels'.  Without the flag no decode launch (M <= MNB_MAX_M) uses a
- * tensor-core instruction.  On the prefill path (M > MNB_MAX_M, which by
- * default runs mma.sync on the same exact products) the flag selects the
- * tcgen05 form when x is 16-byte aligned: every dequantized weight (q - zp) s
- * is split exactly into two fp16 parts, so the products stay exact and the
- * sums fp32 (in tensor memory); it differs from the default only where an
- * infinite activation meets a weight whose low part is zero (NaN instead of
- * +-inf) and for weights below 2^-11 in magnitude (the low part is rounded).
+ * MNB_FLAG_TENSOR_CORES: permit tensor-core math in the step kernel where it
+ * applies (no K split, K a multiple of 1024, scales and zp 16-byte aligned, M
+ * * K at most 33792). It forms the same exact fp16 products (q - zp) * x and
+ * accumulates them in fp32 with mma.sync m16n8k16 instead of fp32 FMAs;
+ * results meet the same error bound and bf16 invariant, but their bits may
+ * differ from the default kernels'. Without the flag no decode launch (M <=
+ * MNB_MAX_M) uses a tensor-core instruction. On the prefill path (M >
+ * MNB_MAX_M, which by default runs mma.sync on the same exact products) the
+ * flag selects the tcgen05 form when x is 16-byte aligned: every dequantized
+ * weight (q - zp) s is split exactly into two fp16 parts, so the products
+ * stay exact and the sums fp32 (in tensor memory); it differs from the
+ * default only where an infinite activation meets a weight whose low part is
+ * zero (NaN instead of +-inf) and for weights below 2^-11 in magnitude (the
+ * low part is rounded).
  */
 #define MNB_FLAG_TENSOR_CORES 2u
 

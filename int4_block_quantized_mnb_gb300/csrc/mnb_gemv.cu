@@ -108,7 +108,7 @@ struct Params {
   int stages;
   int rows_stage;   // rows of the weight matrix per stage (a multiple of the chunk rows)
   int q_pitch;      // bytes per row inside a stage's weight area
-  // tensor-core kernel only
+  // step kernel only
   int tr;           // 16-row sub-tiles per tile
   int wk;           // K slices = 256-k segments per stage
   int steps;        // stages per tile (K / 256 / wk)
@@ -123,7 +123,7 @@ struct Params {
   int bar_offset;   // shared-memory offset of the mbarrier array
   int red_offset;   // offset of the cross-warp reduction slots
   int part_offset;  // offset of the cluster partial sums
-  int xp_offset;    // offset of the tensor-core kernel's activation fragments
+  int xp_offset;    // offset of the step kernel's staged activations
   int xp_pitch;     // bytes per activation row of those fragments
   int flag_offset;  // offset of the CTA abort flag
 };
@@ -769,10 +769,11 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
 }
 
 
-// ------------------------------------------------------ tensor-core kernel --
+// ------------------------------------------------------------- step kernel --
 //
-// The multiply-accumulate of small batches runs on the tensor cores
-// (mma.sync m16n8k16, fp16 operands, fp32 accumulation):
+// Weight tiles stream in through TMA tensor copies; the multiply-accumulate
+// runs on CUDA cores by default (see gemv_step_kernel) or, on request, on the
+// tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation):
 //   A = 16 weight rows x 16 k: lane (g, t) holds code word t (k = 8t..8t+7 of
 //       the block) of rows g and g+8, dequantized exactly to q - zp by the same
 //       lop3 + packed subtraction as the CUDA-core kernel; the word's pairs
@@ -825,8 +826,8 @@ __device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// Producer of the tensor-core kernel (one thread): one stage per (tile, part),
-// three tensor copies completing on the stage's mbarrier.
+// Producer of the step kernel (one thread): one stage per (tile, part), three
+// tensor copies completing on the stage's mbarrier.
 __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* smem,
                                                 uint32_t full0, uint32_t empty0,
                                                 volatile int* abort_flag, int t_begin,
@@ -880,7 +881,7 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
 }
 
 // Math of the step kernel: CUDA-core with four rows per lane (small M),
-// CUDA-core with one row per lane and broadcast activations (larger M), or
+// CUDA-core with two rows per lane and shared activation loads (larger M), or
 // tensor-core (on request).
 enum StepMath : int { kMathFma = 0, kMathWide = 1, kMathMma = 2 };
 
@@ -1424,7 +1425,7 @@ int device_info(DeviceInfo* out) {
 }
 
 int check_shape(int M, int N, int K) {
-  if (M < 1 || M > kMaxM) return fail(MNB_ERR_SHAPE, "M must be in 1..8");
+  if (M < 1 || M > kMaxM) return fail(MNB_ERR_SHAPE, "M must be in 1..4194240");
   if (N < 1) return fail(MNB_ERR_SHAPE, "N must be >= 1");
   if (K < kBlock || K % kBlock != 0) return fail(MNB_ERR_SHAPE, "K must be a positive multiple of 32");
   const int min_split = (K + max_k_per_cta(M) - 1) / max_k_per_cta(M);
@@ -1582,7 +1583,7 @@ MmaFn pick_step_kernel(int M, int math) {
 int round_up(int v, int a) { return (v + a - 1) / a * a; }
 int odd_at_least(int v) { return v | 1; }
 
-// Tile shape and stage layout of the tensor-core kernel.  Sub-tiles per tile
+// Tile shape and stage layout of the step kernel.  Sub-tiles per tile
 // (tr): the largest whose makespan, in 16-row tiles per CTA, is within 5% of
 // the best and that keeps as many SMs busy; K slices: the largest divisor of
 // K / 256 up to 16 / tr (at least 4 where K allows, so a stage's zero-point
@@ -1668,7 +1669,7 @@ int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, Plan* plan) {
 
 // ---------------------------------------------------------- tensor maps --
 //
-// The three views the tensor-core kernel copies from (see its layout notes),
+// The three views the step kernel copies from (see its layout notes),
 // encoded with the driver's cuTensorMapEncodeTiled (fetched once through the
 // runtime, no link-time dependence on libcuda).  A map depends only on the
 // array's address, N, K and the tile shape (tr, wk), so encoded maps are kept in a

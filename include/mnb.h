@@ -140,8 +140,8 @@ int mnb_gemv(const void *x, const uint8_t *qweight, const void *scales, const ui
 
 /*
  * MNB_FLAG_TENSOR_CORES: permit tensor-core math in the step kernel where it
- * applies (no K split, K a multiple of 1024, scales and zp 16-byte aligned, M
- * * K at most 33792). It forms the same exact fp16 products (q - zp) * x and
+ * applies (no K split, K a multiple of 1024, scales and zp 16-byte aligned,
+ * M times K at most 33792). It forms the same exact fp16 products (q - zp) * x and
  * accumulates them in fp32 with mma.sync m16n8k16 instead of fp32 FMAs;
  * results meet the same error bound and bf16 invariant, but their bits may
  * differ from the default kernels'. Without the flag no decode launch (M <=

@@ -59,6 +59,7 @@ struct PfParams {
   int bshift;                                  // log2(B / 32)
   int out_bf16;
   int x_aligned;
+  int ksplit;                                  // CTAs of a cluster that split K (grid z)
 };
 
 __device__ __forceinline__ void pf_store(void* y, size_t idx, float v, int out_bf16) {
@@ -213,7 +214,11 @@ __global__ void __launch_bounds__(kPfWarps * 32, kCtas) gemm_prefill_pipelined(c
   const int m0 = blockIdx.y * kPfTok;
   const int lr0 = warp * 16 + g, lr1 = lr0 + 8;          // this lane's rows in the CTA
   const int bper = 1 << p.bshift;                        // chunks per block
-  const int nstages = (p.chunks + kPfStage - 1) / kPfStage;
+  // this CTA's stages: a contiguous share of the K stages (whole stages, so
+  // every quantization block stays inside one CTA)
+  const int nstages_all = (p.chunks + kPfStage - 1) / kPfStage;
+  const int st_begin = static_cast<int>(blockIdx.z) * nstages_all / p.ksplit;
+  const int st_end = (static_cast<int>(blockIdx.z) + 1) * nstages_all / p.ksplit;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -269,14 +274,14 @@ __global__ void __launch_bounds__(kPfWarps * 32, kCtas) gemm_prefill_pipelined(c
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[j][e] = D[j][e] = 0.f;
 
-  fill_async(0, 0);
-  load_sz(0);
+  fill_async(st_begin, 0);
+  load_sz(st_begin);
   store_sz(0);
-  for (int st = 0; st < nstages; ++st) {
-    const int bi = st & 1;
+  for (int st = st_begin; st < st_end; ++st) {
+    const int bi = (st - st_begin) & 1;
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();                 // stage st landed and is visible; buffer bi ^ 1 is free
-    const bool more = st + 1 < nstages;
+    const bool more = st + 1 < st_end;
     if (more) {
       fill_async(st + 1, bi ^ 1);
       load_sz(st + 1);
@@ -324,15 +329,51 @@ __global__ void __launch_bounds__(kPfWarps * 32, kCtas) gemm_prefill_pipelined(c
     if (more) store_sz(bi ^ 1);
   }
   const int r0 = nb0 + lr0, r1 = nb0 + lr1;
+  if (p.ksplit == 1) {
+#pragma unroll
+    for (int j = 0; j < kPfTiles; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int n = e < 2 ? r0 : r1;
+        const int m = m0 + 8 * j + 2 * t + (e & 1);
+        if (n < p.N && m < p.M)
+          pf_store(p.y, static_cast<size_t>(m) * p.N + n, acc[j][e], p.out_bf16);
+      }
+    return;
+  }
+  // K split over the cluster: each CTA leaves its fp32 tile [row][activation
+  // row] in its shared memory; after the cluster barrier, rank r sums the
+  // r-th 1/S of the tile over the ranks in rank order (distributed shared
+  // memory) and stores it; a second barrier keeps every tile readable until
+  // all ranks are done.
+  __syncthreads();                                          // stage buffers are free
+  float* part = reinterpret_cast<float*>(xb);               // 128 x 64 fp32
 #pragma unroll
   for (int j = 0; j < kPfTiles; ++j)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int n = e < 2 ? r0 : r1;
-      const int m = m0 + 8 * j + 2 * t + (e & 1);
-      if (n < p.N && m < p.M)
-        pf_store(p.y, static_cast<size_t>(m) * p.N + n, acc[j][e], p.out_bf16);
+    for (int e = 0; e < 4; ++e)
+      part[(e < 2 ? lr0 : lr1) * kPfTok + 8 * j + 2 * t + (e & 1)] = acc[j][e];
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  const int share = kPfRows * kPfTok / p.ksplit;
+  const uint32_t part_addr = static_cast<uint32_t>(__cvta_generic_to_shared(part));
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  for (int e = threadIdx.x; e < share; e += kPfWarps * 32) {
+    const int gidx = static_cast<int>(rank) * share + e;
+    const int row = gidx / kPfTok, tok = gidx - row * kPfTok;
+    const uint32_t local = part_addr + 4u * static_cast<uint32_t>(gidx);
+    float sum = 0.f;
+    for (int r = 0; r < p.ksplit; ++r) {
+      uint32_t remote;
+      float v;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(r));
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+      sum += v;
     }
+    const int n = nb0 + row, m = m0 + tok;
+    if (n < p.N && m < p.M) pf_store(p.y, static_cast<size_t>(m) * p.N + n, sum, p.out_bf16);
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace
@@ -357,26 +398,40 @@ int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, co
   p.bshift = block == 128 ? 2 : block == 64 ? 1 : 0;
   p.out_bf16 = out_bf16;
   p.x_aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  p.ksplit = 1;
   const long long gx = (static_cast<long long>(N) + kPfRows - 1) / kPfRows;
   const long long gy = (static_cast<long long>(M) + kPfTok - 1) / kPfTok;
   if (gx > 0x7FFFFFFFLL || gy > 65535) return fail(MNB_ERR_SHAPE, "prefill shape too large");
+  // A grid smaller than the SM count splits K over a cluster of up to 8 CTAs
+  // (each keeping at least two stages), pipelined form only.
+  const int nstages = (p.chunks + kPfStage - 1) / kPfStage;
+  if (p.x_aligned)
+    while (p.ksplit < 8 && gx * gy * p.ksplit < sms && nstages >= 4 * p.ksplit) p.ksplit *= 2;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
+                     static_cast<unsigned>(p.ksplit));
   cfg.blockDim = dim3(kPfWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.ksplit > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = static_cast<unsigned>(p.ksplit);
+    cfg.numAttrs = 2;
+  }
   void* args[1] = {&p};
   const void* fn = reinterpret_cast<const void*>(&gemm_prefill_kernel);
   if (p.x_aligned) {                 // the async copies want 16-byte-aligned rows
     // two CTAs per SM only when the grid needs them: a small grid would be
     // packed two to an SM and leave SMs idle
-    fn = gx * gy > sms ? reinterpret_cast<const void*>(&gemm_prefill_pipelined<2>)
+    fn = gx * gy * p.ksplit > sms ? reinterpret_cast<const void*>(&gemm_prefill_pipelined<2>)
                        : reinterpret_cast<const void*>(&gemm_prefill_pipelined<1>);
     cfg.dynamicSmemBytes = kPfSmem;
     const cudaError_t ea =

@@ -402,11 +402,13 @@ int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, co
   const long long gx = (static_cast<long long>(N) + kPfRows - 1) / kPfRows;
   const long long gy = (static_cast<long long>(M) + kPfTok - 1) / kPfTok;
   if (gx > 0x7FFFFFFFLL || gy > 65535) return fail(MNB_ERR_SHAPE, "prefill shape too large");
-  // A grid smaller than the SM count splits K over a cluster of up to 8 CTAs
-  // (each keeping at least two stages), pipelined form only.
+  // A grid of at most half the SM count splits K over a cluster of up to 8
+  // CTAs, doubling while the grid is below the SM count (each keeps two
+  // stages); pipelined form only.
   const int nstages = (p.chunks + kPfStage - 1) / kPfStage;
   if (p.x_aligned)
-    while (p.ksplit < 8 && gx * gy * p.ksplit < sms && nstages >= 4 * p.ksplit) p.ksplit *= 2;
+    if (gx * gy * 2 <= sms)
+      while (p.ksplit < 8 && gx * gy * p.ksplit < sms && nstages >= 4 * p.ksplit) p.ksplit *= 2;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),

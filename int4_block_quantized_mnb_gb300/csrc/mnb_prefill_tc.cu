@@ -21,6 +21,8 @@
 // buffer is refilled two steps later, after that barrier completes.  The
 // epilogue reads TMEM (warp w: lanes 32 (w mod 4) .. + 31, 32 columns by w / 4),
 // forms D_hi + 2^-11 D_lo, rounds once to fp16 and, on the bf16 arm, narrows.
+// A grid smaller than the SM count splits K over a cluster of up to 8 CTAs;
+// their fp32 tiles are summed in rank order through distributed shared memory.
 #include "mnb.h"
 #include "mnb_dequant.cuh"
 #include "mnb_narrow.cuh"
@@ -63,6 +65,7 @@ struct TcParams {
   int blocks, zstride, block;
   int out_bf16;
   unsigned int* err;                         // the device error word (mnb_device_error)
+  int ksplit;                                // CTAs of a cluster that split K (grid z)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -248,7 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
   const uint8_t* qrow = p.q + static_cast<size_t>(wrow) * (p.K / 2);
   const uint16_t* srow = p.scales + static_cast<size_t>(wrow) * p.blocks;
   const uint8_t* zrow = p.zp ? p.zp + static_cast<size_t>(wrow) * p.zstride : nullptr;
-  const int nsteps = (p.K + kTcK - 1) / kTcK;
+  // this CTA's K steps: a contiguous share of all of them (grid z, cluster rank)
+  const int nsteps_all = (p.K + kTcK - 1) / kTcK;
+  const int st_begin = static_cast<int>(blockIdx.z) * nsteps_all / p.ksplit;
+  const int nsteps = (static_cast<int>(blockIdx.z) + 1) * nsteps_all / p.ksplit - st_begin;
   bool ok = true;
 
   // Each thread's global inputs of a step (its weight row's 32 codes, scale
@@ -296,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
   // Thread 0 alone waits on the MMA commits and publishes the outcome; every
   // branch on it follows a barrier, so all threads take the same path.
   StepIn cur, nxt;
-  load_step(0, cur);
-  for (int st = 0; st < nsteps && ok; ++st) {
+  load_step(st_begin, cur);
+  for (int st = 0; st < nsteps && ok; ++st) {       // st counts this CTA's steps
     const int bi = st & 1;
     unsigned char* buf = smem + bi * kTcBuf;
     // the buffer's MMAs of two steps ago must be done before it is rewritten
@@ -342,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
       const int tt = item >> 3, cj = item & 7;
       *reinterpret_cast<uint4*>(buf + 2 * kTcTile + sw128(tt, cj)) = pair_k4(cur.xv[i]);
     }
-    if (st + 1 < nsteps) load_step(st + 1, nxt);     // in flight while this step multiplies
+    if (st + 1 < nsteps) load_step(st_begin + st + 1, nxt);   // in flight during this step
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     if (tid == 0) {
@@ -370,12 +376,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
   __syncthreads();
   ok = *abort_flag == 0;
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  // warp w: TMEM lanes 32 (w mod 4) .., a 1/(warps/4) share of the columns
+  constexpr int kColsPerWarp = kTcTok / (kThreads / 128);
+  const int lane_base = 32 * (warp & 3);
+  const int col0 = kColsPerWarp * (warp >> 2);
+  const int n = n0 + lane_base + lane;
+  // with a K split, the fp32 tile [row][activation row] goes to this CTA's
+  // shared memory (the stage buffers are free) instead of to y
+  float* part = reinterpret_cast<float*>(smem);
   if (ok) {
-    // warp w: TMEM lanes 32 (w mod 4) .., a 1/(warps/4) share of the columns
-    constexpr int kColsPerWarp = kTcTok / (kThreads / 128);
-    const int lane_base = 32 * (warp & 3);
-    const int col0 = kColsPerWarp * (warp >> 2);
-    const int n = n0 + lane_base + lane;
 #pragma unroll 1
     for (int cc = 0; cc < kColsPerWarp / 32; ++cc) {
       const int col = col0 + 32 * cc;
@@ -384,12 +393,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
       tc_ld32(tmem + (static_cast<uint32_t>(lane_base) << 16) + kTcTok + col, vl);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const int m = m0 + col + j;
-        if (n < p.N && m < p.M)
-          pf_out(p.y, static_cast<size_t>(m) * p.N + n, fmaf(vl[j], 1.f / 2048.f, vh[j]),
-                 p.out_bf16);
+        const float v = fmaf(vl[j], 1.f / 2048.f, vh[j]);
+        if (p.ksplit > 1) {
+          part[(lane_base + lane) * kTcTok + col + j] = v;
+        } else {
+          const int m = m0 + col + j;
+          if (n < p.N && m < p.M) pf_out(p.y, static_cast<size_t>(m) * p.N + n, v, p.out_bf16);
+        }
       }
     }
+  }
+  if (p.ksplit > 1) {
+    // rank r sums the r-th 1/S of the tile over the ranks in rank order
+    // (distributed shared memory); the second barrier keeps every tile
+    // readable until all ranks are done.  Every CTA takes both barriers.
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int share = kTcRows * kTcTok / p.ksplit;
+    const uint32_t part_addr = smem_addr(part);
+    if (ok) {
+      for (int e = tid; e < share; e += kThreads) {
+        const int gidx = static_cast<int>(rank) * share + e;
+        const int row = gidx / kTcTok, tok = gidx - row * kTcTok;
+        const uint32_t local = part_addr + 4u * static_cast<uint32_t>(gidx);
+        float sum = 0.f;
+        for (int r = 0; r < p.ksplit; ++r) {
+          uint32_t remote;
+          float v;
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(r));
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+          sum += v;
+        }
+        const int nn = n0 + row, m = m0 + tok;
+        if (nn < p.N && m < p.M) pf_out(p.y, static_cast<size_t>(m) * p.N + nn, sum, p.out_bf16);
+      }
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -429,7 +469,13 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
   const int tok = t256 ? 256 : 128;
   const long long gy = (static_cast<long long>(M) + tok - 1) / tok;
   if (gx > 0x7FFFFFFFLL || gy > 65535) return fail(MNB_ERR_SHAPE, "prefill shape too large");
-  const bool wide = t256 || gx * gy <= sms;
+  // a grid of at most half the SM count splits K over a cluster of up to 8
+  // CTAs, doubling while the grid is below the SM count (each keeps two steps)
+  const int nsteps = (K + kTcK - 1) / kTcK;
+  p.ksplit = 1;
+  if (gx * gy * 2 <= sms)
+    while (p.ksplit < 8 && gx * gy * p.ksplit < sms && nsteps >= 4 * p.ksplit) p.ksplit *= 2;
+  const bool wide = t256 || gx * gy * p.ksplit <= sms;
   const void* fn = t256   ? reinterpret_cast<const void*>(&gemm_prefill_tc<512, 256>)
                    : wide ? reinterpret_cast<const void*>(&gemm_prefill_tc<512, 128>)
                           : reinterpret_cast<const void*>(&gemm_prefill_tc<256, 128>);
@@ -437,15 +483,23 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill tc)");
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
+                     static_cast<unsigned>(p.ksplit));
   cfg.blockDim = dim3(wide ? 512 : 256);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.ksplit > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = static_cast<unsigned>(p.ksplit);
+    cfg.numAttrs = 2;
+  }
   void* args[1] = {&p};
   e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC(prefill tc)");

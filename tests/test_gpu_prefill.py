@@ -79,20 +79,21 @@ def test_tensor_core_full_size(M, N, K, block, symmetric):
     _run_both(inp, symmetric, cols=cols, tensor_cores=True)
 
 
+@pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
 @pytest.mark.parametrize("M,N,K,block,symmetric", [
     (16, 512, 4096, 32, False), (9, 300, 8192, 64, True), (64, 4096, 4096, 128, False),
     (33, 1000, 2048, 32, True),
 ])
-def test_k_split_over_a_cluster(M, N, K, block, symmetric):
+def test_k_split_over_a_cluster(M, N, K, block, symmetric, tc):
     """Small grids split K over a thread-block cluster (up to 8 CTAs, partial
-    tiles summed in rank order through distributed shared memory): within the
-    bound, and the same bits on every run."""
+    tiles summed in rank order through distributed shared memory), in both
+    forms: within the bound, and the same bits on every run."""
     inp = make_inputs(M, N, K, seed=M + K + block, block=block)
     cols = None if N <= 512 else np.arange(0, N, 9)
-    _run_both(inp, symmetric, cols=cols)
+    _run_both(inp, symmetric, cols=cols, tensor_cores=tc)
     dev = _gpu.to_device(inp, symmetric=symmetric)
-    a = _gpu.bits(_gpu.run(dev, "f16", 0, block=block))
-    b = _gpu.bits(_gpu.run(dev, "f16", 0, block=block))
+    a = _gpu.bits(_gpu.run(dev, "f16", 0, block=block, tensor_cores=tc))
+    b = _gpu.bits(_gpu.run(dev, "f16", 0, block=block, tensor_cores=tc))
     assert np.array_equal(a, b)
 
 

@@ -64,6 +64,8 @@ def parse():
                     help="quantization block size of the synthetic weights")
     ap.add_argument("--symmetric", action="store_true",
                     help="weights without zero-points (every zero-point 8)")
+    ap.add_argument("--m", type=int, default=0,
+                    help="activation rows instead of the workload's (M > 8: the prefill GEMM)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -93,6 +95,32 @@ def fma_bound(w, props, clk):
     fmas = w.M * w.N * w.K
     return {"fmas_per_launch": fmas, "tfma_per_s": rate / 1e12, "us": fmas / rate * 1e6,
             "rate_source": f"{props.multi_processor_count} SMs x 128 FP32 lanes x {mhz:.0f} MHz"}
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor TFLOP/s (burst) from MEASURED_PEAKS.json; fp16 runs at
+    the same nominal rate."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def tensor_roofline(w, per_launch_s, gbs, hbm_peak):
+    """The prefill GEMM (M > 8) against the dense tensor peak: 2 M N K flops per
+    launch over its average duration; the HBM fraction beside it."""
+    flops = 2.0 * w.M * w.N * w.K
+    tf = flops / per_launch_s / 1e12
+    peak, kind = measured_tensor_peak()
+    return {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+            "peak_kind": kind + " bf16 (fp16 operands run at the same nominal rate)",
+            "traffic": None, "flops_per_launch": flops,
+            "hbm_achieved_gbs": gbs, "hbm_frac": gbs / hbm_peak}
 
 
 def measured_peaks():
@@ -215,10 +243,14 @@ class FormatWorkload:
     """A workload's shape with another weight format: block size and whether
     zero-points are stored (the symmetric format moves none)."""
 
-    def __init__(self, base, block, symmetric):
+    def __init__(self, base, block, symmetric, M=0):
         self.M, self.N, self.K, self.out_dtypes = base.M, base.N, base.K, base.out_dtypes
         self.block, self.symmetric = block, symmetric
-        self.name = f"{base.name}-b{block}" + ("-sym" if symmetric else "")
+        name = base.name
+        if M:
+            self.M = M
+            name = f"{'prefill' if M > 8 else 'batch'}-m{M}-k{self.K}-n{self.N}"
+        self.name = name + (f"-b{block}" if block != 32 else "") + ("-sym" if symmetric else "")
 
     def algorithmic_bytes(self) -> int:
         from int4_block_quantized_mnb_gb300.synth import bytes_per_call
@@ -424,8 +456,8 @@ def main():
     if args.workload not in WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {list(WORKLOADS)}")
     w = WORKLOADS[args.workload]
-    if args.block != 32 or args.symmetric:
-        w = FormatWorkload(w, args.block, args.symmetric)
+    if args.block != 32 or args.symmetric or args.m:
+        w = FormatWorkload(w, args.block, args.symmetric, args.m)
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -598,13 +630,14 @@ def main():
                    "timing": f"CUDA events around {full} replays of a {G}-step graph"
                              + (f" + 1 replay of a {rem}-step graph" if rem else "")
                              + "; warm-up: W eager steps, then one untimed replay per graph"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": None if tc else recorded_traffic(w.name),
-                     "algorithmic_bytes_per_launch": bytes_call,
-                     "peak_datasheet": DATASHEET_HBM_GBS,
-                     "frac_datasheet": achieved / DATASHEET_HBM_GBS,
-                     "fma_bound": fma_bound(w, props, clk) if w.M > 1 else None},
+        "roofline": ({"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                      "frac": achieved / peak, "peak_kind": peak_kind,
+                      "traffic": None if tc else recorded_traffic(w.name),
+                      "algorithmic_bytes_per_launch": bytes_call,
+                      "peak_datasheet": DATASHEET_HBM_GBS,
+                      "frac_datasheet": achieved / DATASHEET_HBM_GBS,
+                      "fma_bound": fma_bound(w, props, clk) if w.M > 1 else None}
+                     if w.M <= 8 else tensor_roofline(w, per_launch_s, achieved, peak)),
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,

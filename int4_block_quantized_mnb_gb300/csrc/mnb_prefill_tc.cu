@@ -10,15 +10,16 @@
 // accumulators stay in TMEM across the whole K loop.
 //
 // Tile.  A CTA computes 128 weight rows x 128 or 256 activation rows (UMMA
-// M = 128, N = 128 or 256) in K steps of 64.  Per step its 256 or 512 threads write, in the
-// 128-byte swizzled K-major layout the tensor core reads, the hi and lo tiles
-// of the weights (thread = one row x 32 or 16 k: one code load, its block's
-// scale and zero-point) and the activation tile, from registers loaded one
-// step ahead; both keep the dequant's (k, k + 4)
-// pairing (the same permutation of k in both operands leaves each dot product
-// unchanged).  One thread issues the eight MMAs of the step (hi and lo, four
-// K = 16 slices each) and commits them to the step buffer's mbarrier; the
-// buffer is refilled two steps later, after that barrier completes.  The
+// M = 128, N = 128 or 256) in K steps of 64, through a ring of three stage
+// buffers.  Its 512 dequant threads write, per step, the hi and lo tiles of the
+// weights (thread = one row x 16 k: one code load, its block's scale and
+// zero-point) and the activation tile in the 128-byte swizzled K-major layout
+// the tensor core reads, from registers loaded one step ahead; both keep the
+// dequant's (k, k + 4) pairing (the same permutation of k in both operands
+// leaves each dot product unchanged).  Each dequant warp marks a stage full on
+// its mbarrier; one more warp waits for it, issues the step's eight MMAs (hi
+// and lo, four K = 16 slices each) and commits them to the stage's empty
+// barrier, which the dequant warps wait on before they refill it.  The
 // epilogue reads TMEM (warp w: lanes 32 (w mod 4) .. + 31, 32 columns by w / 4),
 // forms D_hi + 2^-11 D_lo, rounds once to fp16 and, on the bf16 arm, narrows.
 // A grid smaller than the SM count splits K over a cluster of up to 8 CTAs;
@@ -50,7 +51,9 @@ constexpr int kTcTile = 128 * 128;           // bytes of one 128 x 64 fp16 tile
 // holds the hi and lo weight tiles and kTok / 128 activation tiles; TMEM
 // holds D_hi (columns 0 .. kTok - 1) and D_lo (kTok .. 2 kTok - 1).
 constexpr int tc_buf(int kTok) { return (2 + kTok / 128) * kTcTile; }
-constexpr int tc_smem(int kTok) { return 2 * tc_buf(kTok) + 1024 + 64; }   // + alignment, barriers
+constexpr int kRing = 3;                     // stages in the ring
+constexpr int kDequantThreads = 512;         // dequant and epilogue threads; one more warp issues MMAs
+constexpr int tc_smem(int kTok) { return kRing * tc_buf(kTok) + 1024 + 128; }   // + alignment, barriers
 constexpr int tc_cols(int kTok) { return 2 * kTok; }
 constexpr unsigned kTcErrMma = 5;            // device error: MMA completion never arrived
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
@@ -199,35 +202,38 @@ __device__ __forceinline__ void pf_out(void* y, size_t idx, float v, int out_bf1
     static_cast<__half*>(y)[idx] = h;
 }
 
-// kThreads: 512 (one CTA per SM, for grids no larger than the SM count) or
-// 256 (two CTAs per SM).  A thread handles one weight row x kKPer k and
-// kXPer activation chunks per step.
+// kThreads dequant threads (plus one MMA warp): a thread handles one weight
+// row x kKPer k and kXPer activation chunks per step.
 template <int kThreads, int kTok>
-__global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p) {
+__global__ void __launch_bounds__(kThreads + 32, 1) gemm_prefill_tc(const TcParams p) {
   constexpr int kTcThreads = kThreads;
   constexpr int kTcTok = kTok;
   constexpr int kTcBuf = tc_buf(kTok);
   constexpr int kTcCols = tc_cols(kTok);
-  constexpr int kKPer = kTcRows * kTcK / kThreads;           // 16 or 32 k per thread
+  constexpr int kKPer = kTcRows * kTcK / kThreads;           // k per thread and step
   constexpr int kWords = kKPer / 8;
   constexpr int kTcXPer = kTcTok * kTcK / 8 / kThreads;      // activation chunks per thread
   constexpr int kParts = kTcK / kKPer;                       // threads per weight row
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kTcBuf);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 2 * kTcBuf + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 2 * kTcBuf + 32);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing * kTcBuf);   // full[R] empty[R] done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kRing * kTcBuf + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kRing * kTcBuf + 80);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int n0 = blockIdx.x * kTcRows;
   const int m0 = blockIdx.y * kTcTok;
-  const uint32_t bar0 = smem_addr(bars), bar1 = bar0 + 8;
+  const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8 * kRing, done = full0 + 16 * kRing;
+  const bool is_mma = warp == kThreads / 32;                // the extra warp issues the MMAs
 
   if (tid == 0) {
     *abort_flag = 0;
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar1) : "memory");
+    for (int r = 0; r < kRing; ++r) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * r), "r"(kThreads / 32) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * r) : "memory");
+    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // this thread's weight row and 32-k half of every step
+  // this thread's weight row and kKPer-k part of every step
   const int wr = tid / kParts, qk = tid % kParts;    // weight row, kKPer-k part of the step
   const int wrow = min(n0 + wr, p.N - 1);            // rows past N repeat row N - 1
   const uint8_t* qrow = p.q + static_cast<size_t>(wrow) * (p.K / 2);
@@ -257,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
   const int nsteps = (static_cast<int>(blockIdx.z) + 1) * nsteps_all / p.ksplit - st_begin;
   bool ok = true;
 
-  // Each thread's global inputs of a step (its weight row's 32 codes, scale
-  // and zero-point, four activation chunks), loaded one step ahead.
+  // Each thread's global inputs of a step (its weight row's kKPer codes,
+  // scale and zero-point, kTcXPer activation chunks), loaded one step ahead.
   struct StepIn {
     uint32_t w[kWords];
     float s;
@@ -299,61 +305,72 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
     }
   };
 
-  // Thread 0 alone waits on the MMA commits and publishes the outcome; every
-  // branch on it follows a barrier, so all threads take the same path.
-  StepIn cur, nxt;
-  load_step(st_begin, cur);
-  for (int st = 0; st < nsteps && ok; ++st) {       // st counts this CTA's steps
-    const int bi = st & 1;
-    unsigned char* buf = smem + bi * kTcBuf;
-    // the buffer's MMAs of two steps ago must be done before it is rewritten
-    if (st >= 2) {
-      if (tid == 0 && !tc_wait(bi ? bar1 : bar0, ((st - 2) >> 1) & 1, p.err)) *abort_flag = 1;
-      __syncthreads();
-      if (*abort_flag) {
-        ok = false;
+  // Dequant warps fill ring stage ls % R once the MMAs of its previous use
+  // have committed (empty), then arrive on full; the MMA warp waits on full,
+  // issues the stage's MMAs and commits them to empty, and after the last
+  // stage to done.  Every wait is bounded; a wait that gives up raises the
+  // abort flag and the others then give up too.
+  if (!is_mma) {
+    StepIn cur, nxt;
+    load_step(st_begin, cur);
+    for (int st = 0; st < nsteps; ++st) {
+      const int rs = st % kRing, use = st / kRing;
+      unsigned char* buf = smem + rs * kTcBuf;
+      if (use > 0 && !tc_wait(empty0 + 8 * rs, (use - 1) & 1, p.err)) {
+        *abort_flag = 1;
         break;
       }
-    }
-    // weights: row wr, k = kKPer qk .. + kKPer of the step, as exact hi and lo parts
-    {
-      const __half sh = __float2half_rn(cur.s);      // s is an fp16 value: exact
-      const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x00010001u;
-      const bool small = fabsf(cur.s) <= 2.f;
-      const __half shk = __float2half_rn(small ? cur.s * 2048.f : 0.f);   // exact when small
-      const uint32_t s2k = static_cast<uint32_t>(__half_as_ushort(shk)) * 0x00010001u;
-      const uint32_t zl = cur.z * 0x00010001u + 0x64006400u;
-      const uint32_t zh = cur.z * 0x00100010u + 0x54005400u;
+      if (*abort_flag) break;
+      {
+        const __half sh = __float2half_rn(cur.s);      // s is an fp16 value: exact
+        const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x00010001u;
+        const bool small = fabsf(cur.s) <= 2.f;
+        const __half shk = __float2half_rn(small ? cur.s * 2048.f : 0.f);   // exact when small
+        const uint32_t s2k = static_cast<uint32_t>(__half_as_ushort(shk)) * 0x00010001u;
+        const uint32_t zl = cur.z * 0x00010001u + 0x64006400u;
+        const uint32_t zh = cur.z * 0x00100010u + 0x54005400u;
 #pragma unroll
-      for (int g = 0; g < kWords; ++g) {
-        const uint32_t word = cur.w[g], w8 = word >> 8;
-        uint32_t d[4] = {hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl),
-                         hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh),
-                         hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl),
-                         hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh)};
-        uint4 hi, lo;
-        split_pair(d[0], cur.s, s2, s2k, small, hi.x, lo.x);
-        split_pair(d[1], cur.s, s2, s2k, small, hi.y, lo.y);
-        split_pair(d[2], cur.s, s2, s2k, small, hi.z, lo.z);
-        split_pair(d[3], cur.s, s2, s2k, small, hi.w, lo.w);
-        const uint32_t off = sw128(wr, kWords * qk + g);
-        *reinterpret_cast<uint4*>(buf + off) = hi;
-        *reinterpret_cast<uint4*>(buf + kTcTile + off) = lo;
+        for (int g = 0; g < kWords; ++g) {
+          const uint32_t word = cur.w[g], w8 = word >> 8;
+          uint32_t d[4] = {hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl),
+                           hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh),
+                           hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl),
+                           hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh)};
+          uint4 hi, lo;
+          split_pair(d[0], cur.s, s2, s2k, small, hi.x, lo.x);
+          split_pair(d[1], cur.s, s2, s2k, small, hi.y, lo.y);
+          split_pair(d[2], cur.s, s2, s2k, small, hi.z, lo.z);
+          split_pair(d[3], cur.s, s2, s2k, small, hi.w, lo.w);
+          const uint32_t off = sw128(wr, kWords * qk + g);
+          *reinterpret_cast<uint4*>(buf + off) = hi;
+          *reinterpret_cast<uint4*>(buf + kTcTile + off) = lo;
+        }
       }
-    }
-    // activations: 128 rows x 8 chunks of 8 k, regrouped into the same pairs
 #pragma unroll
-    for (int i = 0; i < kTcXPer; ++i) {
-      const int item = tid + i * kTcThreads;
-      const int tt = item >> 3, cj = item & 7;
-      *reinterpret_cast<uint4*>(buf + 2 * kTcTile + sw128(tt, cj)) = pair_k4(cur.xv[i]);
+      for (int i = 0; i < kTcXPer; ++i) {
+        const int item = tid + i * kTcThreads;
+        const int tt = item >> 3, cj = item & 7;
+        *reinterpret_cast<uint4*>(buf + 2 * kTcTile + sw128(tt, cj)) = pair_k4(cur.xv[i]);
+      }
+      if (st + 1 < nsteps) load_step(st_begin + st + 1, nxt);   // in flight during this step
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(full0 + 8 * rs) : "memory");
+      cur = nxt;
     }
-    if (st + 1 < nsteps) load_step(st_begin + st + 1, nxt);   // in flight during this step
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    if (tid == 0) {
+    // the MMAs of the last stage have completed when done arrives
+    if (!*abort_flag && !tc_wait(done, 0, p.err)) *abort_flag = 1;
+  } else if (lane == 0) {
+    for (int st = 0; st < nsteps; ++st) {
+      const int rs = st % kRing, use = st / kRing;
+      if (!tc_wait(full0 + 8 * rs, use & 1, p.err) || *abort_flag) {
+        *abort_flag = 1;
+        break;
+      }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t a_hi = smem_addr(buf), a_lo = a_hi + kTcTile, bx = a_hi + 2 * kTcTile;
+      const uint32_t a_hi = smem_addr(smem + rs * kTcBuf), a_lo = a_hi + kTcTile;
+      const uint32_t bx = a_hi + 2 * kTcTile;
 #pragma unroll
       for (int ks = 0; ks < kTcK / 16; ++ks) {       // K = 16 slices: 32 bytes apart
         const uint32_t acc = (st > 0 || ks > 0) ? 1u : 0u;
@@ -361,17 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
         tc_mma(tmem + kTcTok, sw128_desc(a_lo + 32 * ks), sw128_desc(bx + 32 * ks),
                tc_idesc(kTok), acc);
       }
-      tc_commit(bi ? bar1 : bar0);
+      tc_commit(empty0 + 8 * rs);
     }
-    cur = nxt;
-  }
-  // wait for the last step's MMAs (and the one before, on the other buffer)
-  if (ok && tid == 0) {
-    const int last = nsteps - 1;
-    if (last >= 1 && !tc_wait(((last - 1) & 1) ? bar1 : bar0, ((last - 1) >> 1) & 1, p.err))
-      *abort_flag = 1;
-    else if (!tc_wait((last & 1) ? bar1 : bar0, (last >> 1) & 1, p.err))
-      *abort_flag = 1;
+    if (!*abort_flag) tc_commit(done);
   }
   __syncthreads();
   ok = *abort_flag == 0;
@@ -384,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
   // with a K split, the fp32 tile [row][activation row] goes to this CTA's
   // shared memory (the stage buffers are free) instead of to y
   float* part = reinterpret_cast<float*>(smem);
-  if (ok) {
+  if (ok && !is_mma) {
 #pragma unroll 1
     for (int cc = 0; cc < kColsPerWarp / 32; ++cc) {
       const int col = col0 + 32 * cc;
@@ -413,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_prefill_tc(const TcParams p)
     const int share = kTcRows * kTcTok / p.ksplit;
     const uint32_t part_addr = smem_addr(part);
     if (ok) {
-      for (int e = tid; e < share; e += kThreads) {
+      for (int e = tid; e < share; e += kThreads + 32) {
         const int gidx = static_cast<int>(rank) * share + e;
         const int row = gidx / kTcTok, tok = gidx - row * kTcTok;
         const uint32_t local = part_addr + 4u * static_cast<uint32_t>(gidx);
@@ -461,31 +470,28 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
   p.zstride = (p.blocks + 1) / 2;
   p.out_bf16 = out_bf16;
   p.err = err;
-  // Activation tiles of 256 rows (one 512-thread CTA per SM, all of TMEM)
-  // where that still gives every SM a CTA; else 128 rows, with 512 threads
-  // while the grid leaves SMs to spare and two 256-thread CTAs per SM above.
+  // Activation tiles of 256 rows (all of TMEM) where that still gives every
+  // SM a CTA, else 128.
   const long long gx = (static_cast<long long>(N) + kTcRows - 1) / kTcRows;
   const bool t256 = gx * ((static_cast<long long>(M) + 255) / 256) >= sms;
   const int tok = t256 ? 256 : 128;
   const long long gy = (static_cast<long long>(M) + tok - 1) / tok;
   if (gx > 0x7FFFFFFFLL || gy > 65535) return fail(MNB_ERR_SHAPE, "prefill shape too large");
-  // a grid of at most half the SM count splits K over a cluster of up to 8
-  // CTAs, doubling while the grid is below the SM count (each keeps two steps)
+  // one CTA per SM (the ring fills most of its shared memory): a grid of at
+  // most half the SM count splits K over a cluster of up to 8 CTAs, doubling
+  // while the grid still fits the SMs (each CTA keeps at least two steps)
   const int nsteps = (K + kTcK - 1) / kTcK;
   p.ksplit = 1;
-  if (gx * gy * 2 <= sms)
-    while (p.ksplit < 8 && gx * gy * p.ksplit < sms && nsteps >= 4 * p.ksplit) p.ksplit *= 2;
-  const bool wide = t256 || gx * gy * p.ksplit <= sms;
-  const void* fn = t256   ? reinterpret_cast<const void*>(&gemm_prefill_tc<512, 256>)
-                   : wide ? reinterpret_cast<const void*>(&gemm_prefill_tc<512, 128>)
-                          : reinterpret_cast<const void*>(&gemm_prefill_tc<256, 128>);
+  while (p.ksplit < 8 && gx * gy * p.ksplit * 2 <= sms && nsteps >= 4 * p.ksplit) p.ksplit *= 2;
+  const void* fn = t256 ? reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 256>)
+                        : reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 128>);
   const int smem = tc_smem(tok);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill tc)");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
                      static_cast<unsigned>(p.ksplit));
-  cfg.blockDim = dim3(wide ? 512 : 256);
+  cfg.blockDim = dim3(kDequantThreads + 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

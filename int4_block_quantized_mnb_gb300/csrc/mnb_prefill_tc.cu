@@ -30,10 +30,12 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <string>
 
 namespace mnb {
@@ -144,6 +146,28 @@ __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, unsigned 
   return true;
 }
 
+// One tiled 2-D tensor copy (global -> this CTA's shared memory) completing
+// on mbarrier bar, and the expect-tx arrival that accounts for its bytes.
+__device__ __forceinline__ void tc_tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
 // 32 consecutive TMEM columns of this warp's 32 lanes.
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -203,39 +227,44 @@ __device__ __forceinline__ void pf_out(void* y, size_t idx, float v, int out_bf1
 }
 
 // kThreads dequant threads (plus one MMA warp): a thread handles one weight
-// row x kKPer k and kXPer activation chunks per step.
+// row x kKPer k per step.
 template <int kThreads, int kTok>
-__global__ void __launch_bounds__(kThreads + 32, 1) gemm_prefill_tc(const TcParams p) {
-  constexpr int kTcThreads = kThreads;
+__global__ void __launch_bounds__(kThreads + 32, 1)
+    gemm_prefill_tc(const TcParams p, const __grid_constant__ CUtensorMap tm_x) {
   constexpr int kTcTok = kTok;
   constexpr int kTcBuf = tc_buf(kTok);
   constexpr int kTcCols = tc_cols(kTok);
   constexpr int kKPer = kTcRows * kTcK / kThreads;           // k per thread and step
   constexpr int kWords = kKPer / 8;
-  constexpr int kTcXPer = kTcTok * kTcK / 8 / kThreads;      // activation chunks per thread
   constexpr int kParts = kTcK / kKPer;                       // threads per weight row
+  constexpr uint32_t kXBytes = kTcTok * kTcK * 2;            // one activation tile
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing * kTcBuf);   // full[R] empty[R] done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kRing * kTcBuf + 64);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kRing * kTcBuf + 80);
+  // full[R] xfull[R] empty[R] done, then the TMEM address and the abort flag
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing * kTcBuf);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kRing * kTcBuf + 96);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kRing * kTcBuf + 112);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int n0 = blockIdx.x * kTcRows;
   const int m0 = blockIdx.y * kTcTok;
-  const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8 * kRing, done = full0 + 16 * kRing;
+  const uint32_t full0 = smem_addr(bars), xfull0 = full0 + 8 * kRing,
+                 empty0 = full0 + 16 * kRing, done = full0 + 24 * kRing;
   const bool is_mma = warp == kThreads / 32;                // the extra warp issues the MMAs
 
   if (tid == 0) {
     *abort_flag = 0;
     for (int r = 0; r < kRing; ++r) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * r), "r"(kThreads / 32) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(xfull0 + 8 * r) : "memory");
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * r) : "memory");
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (is_mma && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
@@ -264,21 +293,20 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gemm_prefill_tc(const TcPara
   bool ok = true;
 
   // Each thread's global inputs of a step (its weight row's kKPer codes,
-  // scale and zero-point, kTcXPer activation chunks), loaded one step ahead.
+  // scale and zero-point), loaded two steps ahead; past K they are zero
+  // (K is a multiple of 32), as the tensor copy makes the activations there.
   struct StepIn {
     uint32_t w[kWords];
     float s;
     uint32_t z;
-    uint4 xv[kTcXPer];
   };
   auto load_step = [&](int st, StepIn& in) {
-    const int k0 = st * kTcK;
-    const int kk = k0 + kKPer * qk;
+    const int kk = st * kTcK + kKPer * qk;
 #pragma unroll
     for (int i = 0; i < kWords; ++i) in.w[i] = 0u;
     in.s = 0.f;
     in.z = 8;
-    if (kk < p.K) {                                  // zero past K (K is a multiple of 32)
+    if (kk < p.K) {
       if constexpr (kWords == 4) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow + kk / 2));
         in.w[0] = v.x; in.w[1] = v.y; in.w[2] = v.z; in.w[3] = v.w;
@@ -293,77 +321,80 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gemm_prefill_tc(const TcPara
         in.z = (b & 1) ? (zb >> 4) : (zb & 0xFu);
       }
     }
-#pragma unroll
-    for (int i = 0; i < kTcXPer; ++i) {
-      const int item = tid + i * kTcThreads;
-      const int tt = item >> 3, cj = item & 7;
-      const int m = min(m0 + tt, p.M - 1);           // rows past M repeat row M - 1
-      const int kx = k0 + 8 * cj;
-      in.xv[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (kx < p.K)
-        in.xv[i] = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K + kx));
-    }
   };
 
-  // Dequant warps fill ring stage ls % R once the MMAs of its previous use
-  // have committed (empty), then arrive on full; the MMA warp waits on full,
-  // issues the stage's MMAs and commits them to empty, and after the last
-  // stage to done.  Every wait is bounded; a wait that gives up raises the
-  // abort flag and the others then give up too.
+  // Ring stage st % R.  Dequant warps write its hi and lo weight tiles once
+  // the MMAs of its previous use have committed (empty), then arrive on full;
+  // the MMA thread copies its activation tile by TMA (xfull), waits on full
+  // and xfull, issues the stage's MMAs and commits them to empty, and after
+  // the last stage to done.  Every wait is bounded; a wait that gives up
+  // raises the abort flag and the others then give up too.
   if (!is_mma) {
-    StepIn cur, nxt;
+    StepIn cur, nx1, nx2;
     load_step(st_begin, cur);
+    if (nsteps > 1) load_step(st_begin + 1, nx1);
     for (int st = 0; st < nsteps; ++st) {
       const int rs = st % kRing, use = st / kRing;
       unsigned char* buf = smem + rs * kTcBuf;
+      if (st + 2 < nsteps) load_step(st_begin + st + 2, nx2);   // in flight for two steps
       if (use > 0 && !tc_wait(empty0 + 8 * rs, (use - 1) & 1, p.err)) {
         *abort_flag = 1;
         break;
       }
       if (*abort_flag) break;
-      {
-        const __half sh = __float2half_rn(cur.s);      // s is an fp16 value: exact
-        const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x00010001u;
-        const bool small = fabsf(cur.s) <= 2.f;
-        const __half shk = __float2half_rn(small ? cur.s * 2048.f : 0.f);   // exact when small
-        const uint32_t s2k = static_cast<uint32_t>(__half_as_ushort(shk)) * 0x00010001u;
-        const uint32_t zl = cur.z * 0x00010001u + 0x64006400u;
-        const uint32_t zh = cur.z * 0x00100010u + 0x54005400u;
+      const __half sh = __float2half_rn(cur.s);      // s is an fp16 value: exact
+      const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x00010001u;
+      const bool small = fabsf(cur.s) <= 2.f;
+      const __half shk = __float2half_rn(small ? cur.s * 2048.f : 0.f);   // exact when small
+      const uint32_t s2k = static_cast<uint32_t>(__half_as_ushort(shk)) * 0x00010001u;
+      const uint32_t zl = cur.z * 0x00010001u + 0x64006400u;
+      const uint32_t zh = cur.z * 0x00100010u + 0x54005400u;
 #pragma unroll
-        for (int g = 0; g < kWords; ++g) {
-          const uint32_t word = cur.w[g], w8 = word >> 8;
-          uint32_t d[4] = {hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl),
-                           hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh),
-                           hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl),
-                           hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh)};
-          uint4 hi, lo;
-          split_pair(d[0], cur.s, s2, s2k, small, hi.x, lo.x);
-          split_pair(d[1], cur.s, s2, s2k, small, hi.y, lo.y);
-          split_pair(d[2], cur.s, s2, s2k, small, hi.z, lo.z);
-          split_pair(d[3], cur.s, s2, s2k, small, hi.w, lo.w);
-          const uint32_t off = sw128(wr, kWords * qk + g);
-          *reinterpret_cast<uint4*>(buf + off) = hi;
-          *reinterpret_cast<uint4*>(buf + kTcTile + off) = lo;
-        }
+      for (int g = 0; g < kWords; ++g) {
+        const uint32_t word = cur.w[g], w8 = word >> 8;
+        // exact q - zp of pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7), regrouped
+        // into natural k order (k0,k1) (k2,k3) (k4,k5) (k6,k7)
+        const uint32_t d0 = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl);
+        const uint32_t d1 = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh);
+        const uint32_t d2 = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl);
+        const uint32_t d3 = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh);
+        uint4 hi, lo;
+        split_pair(prmt(d0, d1, 0x5410u), cur.s, s2, s2k, small, hi.x, lo.x);
+        split_pair(prmt(d2, d3, 0x5410u), cur.s, s2, s2k, small, hi.y, lo.y);
+        split_pair(prmt(d0, d1, 0x7632u), cur.s, s2, s2k, small, hi.z, lo.z);
+        split_pair(prmt(d2, d3, 0x7632u), cur.s, s2, s2k, small, hi.w, lo.w);
+        const uint32_t off = sw128(wr, kWords * qk + g);
+        *reinterpret_cast<uint4*>(buf + off) = hi;
+        *reinterpret_cast<uint4*>(buf + kTcTile + off) = lo;
       }
-#pragma unroll
-      for (int i = 0; i < kTcXPer; ++i) {
-        const int item = tid + i * kTcThreads;
-        const int tt = item >> 3, cj = item & 7;
-        *reinterpret_cast<uint4*>(buf + 2 * kTcTile + sw128(tt, cj)) = pair_k4(cur.xv[i]);
-      }
-      if (st + 1 < nsteps) load_step(st_begin + st + 1, nxt);   // in flight during this step
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0)
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(full0 + 8 * rs) : "memory");
-      cur = nxt;
+      cur = nx1;
+      nx1 = nx2;
     }
     // the MMAs of the last stage have completed when done arrives
     if (!*abort_flag && !tc_wait(done, 0, p.err)) *abort_flag = 1;
   } else if (lane == 0) {
+    // activation tile of step st (k0 = 64 (st_begin + st), rows m0 ..) into
+    // stage st % R: 128-byte rows, 128-byte swizzle (the MMA's layout);
+    // rows past M and k past K arrive as zeros
+    auto copy_x = [&](int st) {
+      const int rs = st % kRing;
+      tc_expect_tx(xfull0 + 8 * rs, kXBytes);
+      tc_tma_2d(smem_addr(smem + rs * kTcBuf + 2 * kTcTile), &tm_x, (st_begin + st) * kTcK, m0,
+                xfull0 + 8 * rs);
+    };
+    int issued = 0, consumed = 0;
+    for (; issued < kRing && issued < nsteps; ++issued) copy_x(issued);
     for (int st = 0; st < nsteps; ++st) {
       const int rs = st % kRing, use = st / kRing;
+      if (!tc_wait(xfull0 + 8 * rs, use & 1, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      consumed = st + 1;
       if (!tc_wait(full0 + 8 * rs, use & 1, p.err) || *abort_flag) {
         *abort_flag = 1;
         break;
@@ -379,8 +410,24 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gemm_prefill_tc(const TcPara
                tc_idesc(kTok), acc);
       }
       tc_commit(empty0 + 8 * rs);
+      // refill the stage of step st - 1 once its MMAs (queued ahead of
+      // these) have completed
+      if (st >= 1 && issued < nsteps) {
+        const int ps = (st - 1) % kRing;
+        if (!tc_wait(empty0 + 8 * ps, ((st - 1) / kRing) & 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        copy_x(issued++);
+      }
     }
-    if (!*abort_flag) tc_commit(done);
+    if (!*abort_flag) {
+      tc_commit(done);
+    } else {
+      // copies still in flight land before the CTA's shared memory is released
+      for (int st = consumed; st < issued; ++st)
+        if (!tc_wait(xfull0 + 8 * (st % kRing), (st / kRing) & 1, p.err)) break;
+    }
   }
   __syncthreads();
   ok = *abort_flag == 0;
@@ -449,6 +496,27 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gemm_prefill_tc(const TcPara
   }
 }
 
+// cuTensorMapEncodeTiled from the driver, fetched once through the runtime
+// (no link-time dependence on libcuda); null when the driver lacks it.
+using TcEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+TcEncodeFn tc_encode_fn() {
+  static std::once_flag once;
+  static TcEncodeFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<TcEncodeFn>(f);
+  });
+  return fn;
+}
+
 }  // namespace
 
 // Launches the tensor-memory prefill GEMM; the caller has validated the
@@ -506,7 +574,22 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
     attr[1].val.clusterDim.z = static_cast<unsigned>(p.ksplit);
     cfg.numAttrs = 2;
   }
-  void* args[1] = {&p};
+  // the activations as (k, row) fp16 pairs of bits: boxes of 64 k (one
+  // 128-byte swizzle row) x tok rows, zero-filled past K and M
+  const TcEncodeFn encode = tc_encode_fn();
+  if (!encode) return fail(MNB_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  CUtensorMap tm_x;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcK), static_cast<cuuint32_t>(tok)};
+  const cuuint32_t ones[2] = {1, 1};
+  const CUresult r = encode(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(x), dims,
+                            strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MNB_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult " + std::to_string(r) + ")");
+  void* args[2] = {&p, &tm_x};
   e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC(prefill tc)");
   return MNB_OK;

@@ -341,18 +341,22 @@ __global__ void __launch_bounds__(kPfWarps * 32, kCtas) gemm_prefill_pipelined(c
       }
     return;
   }
-  // K split over the cluster: each CTA leaves its fp32 tile [row][activation
-  // row] in its shared memory; after the cluster barrier, rank r sums the
+  // K split over the cluster: each CTA leaves its fp32 tile [activation row]
+  // [weight row] (rows kPartPitch words apart: lanes (g, t) of a fragment
+  // store hit 32 different banks) in its shared memory; after the cluster
+  // barrier, rank r sums the
   // r-th 1/S of the tile over the ranks in rank order (distributed shared
   // memory) and stores it; a second barrier keeps every tile readable until
   // all ranks are done.
   __syncthreads();                                          // stage buffers are free
-  float* part = reinterpret_cast<float*>(xb);               // 128 x 64 fp32
+  constexpr int kPartPitch = kPfRows + 4;
+  static_assert(kPfTok * kPartPitch * 4 <= 2 * kXBuf, "partial tile exceeds the stage buffers");
+  float* part = reinterpret_cast<float*>(xb);               // 64 x 132 fp32
 #pragma unroll
   for (int j = 0; j < kPfTiles; ++j)
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      part[(e < 2 ? lr0 : lr1) * kPfTok + 8 * j + 2 * t + (e & 1)] = acc[j][e];
+      part[(8 * j + 2 * t + (e & 1)) * kPartPitch + (e < 2 ? lr0 : lr1)] = acc[j][e];
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   const int share = kPfRows * kPfTok / p.ksplit;
   const uint32_t part_addr = static_cast<uint32_t>(__cvta_generic_to_shared(part));
@@ -360,8 +364,8 @@ __global__ void __launch_bounds__(kPfWarps * 32, kCtas) gemm_prefill_pipelined(c
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
   for (int e = threadIdx.x; e < share; e += kPfWarps * 32) {
     const int gidx = static_cast<int>(rank) * share + e;
-    const int row = gidx / kPfTok, tok = gidx - row * kPfTok;
-    const uint32_t local = part_addr + 4u * static_cast<uint32_t>(gidx);
+    const int tok = gidx / kPfRows, row = gidx - tok * kPfRows;   // y row, column
+    const uint32_t local = part_addr + 4u * static_cast<uint32_t>(tok * kPartPitch + row);
     float sum = 0.f;
     for (int r = 0; r < p.ksplit; ++r) {
       uint32_t remote;

@@ -49,13 +49,20 @@ namespace {
 constexpr int kTcRows = 128;                 // weight rows per CTA (UMMA M)
 constexpr int kTcK = 64;                     // k per step: one 128-byte swizzle row of fp16
 constexpr int kTcTile = 128 * 128;           // bytes of one 128 x 64 fp16 tile
-// Per activation-tile width kTok (UMMA N, 128 or 256): one step's buffer
-// holds the hi and lo weight tiles and kTok / 128 activation tiles; TMEM
-// holds D_hi (columns 0 .. kTok - 1) and D_lo (kTok .. 2 kTok - 1).
-constexpr int tc_buf(int kTok) { return (2 + kTok / 128) * kTcTile; }
-constexpr int kRing = 3;                     // stages in the ring
+// Per activation-tile width kTok (UMMA N, 128 or 256): a weight stage holds
+// the hi and lo tiles of a step, an activation stage its kTok x 64 tile, in
+// two rings: the activation ring, filled by tensor copies, runs further
+// ahead (memory latency) than the weight ring, filled by the dequant threads
+// from codes they load kAhead steps ahead.  TMEM holds D_hi (columns
+// 0 .. kTok - 1) and D_lo (kTok .. 2 kTok - 1).
+constexpr int kWBuf = 2 * kTcTile;                                      // one weight stage
+constexpr int tc_xbuf(int kTok) { return kTok * kTcK * 2; }             // one activation stage
+constexpr int tc_wring(int kTok) { return kTok == 256 ? 2 : 3; }
+constexpr int tc_xring(int kTok) { return kTok == 256 ? 4 : 6; }
+constexpr int kAhead = 2;                    // steps of codes in flight per dequant thread
 constexpr int kDequantThreads = 512;         // dequant and epilogue threads; one more warp issues MMAs
-constexpr int tc_smem(int kTok) { return kRing * tc_buf(kTok) + 1024 + 128; }   // + alignment, barriers
+constexpr int tc_bars(int kTok) { return tc_wring(kTok) * kWBuf + tc_xring(kTok) * tc_xbuf(kTok); }
+constexpr int tc_smem(int kTok) { return tc_bars(kTok) + 1024 + 256; }   // + alignment, barriers
 constexpr int tc_cols(int kTok) { return 2 * kTok; }
 constexpr unsigned kTcErrMma = 5;            // device error: MMA completion never arrived
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
@@ -67,7 +74,7 @@ struct TcParams {
   const uint8_t* zp;
   void* y;
   int M, N, K;
-  int blocks, zstride, block;
+  int blocks, zstride, block, bshift;        // bshift = log2(block)
   int out_bf16;
   unsigned int* err;                         // the device error word (mnb_device_error)
   int ksplit;                                // CTAs of a cluster that split K (grid z)
@@ -218,6 +225,14 @@ __device__ __forceinline__ void split_pair(uint32_t d, float s, uint32_t s2, uin
   lo = *reinterpret_cast<const uint32_t*>(&lh);
 }
 
+// The same split when |s| <= 2 holds for the whole warp: -hi 2^11 by one
+// exact multiply, then the fused form above.
+__device__ __forceinline__ void split_pair_small(uint32_t d, uint32_t s2, uint32_t s2k,
+                                                 uint32_t& hi, uint32_t& lo) {
+  hi = hmul2(d, s2);
+  lo = hfma2(d, s2k, hmul2(hi, 0xE800E800u));                  // d s 2^11 + (-hi 2^11)
+}
+
 __device__ __forceinline__ void pf_out(void* y, size_t idx, float v, int out_bf16) {
   const __half h = __float2half_rn(v);
   if (out_bf16)
@@ -232,33 +247,38 @@ template <int kThreads, int kTok>
 __global__ void __launch_bounds__(kThreads + 32, 1)
     gemm_prefill_tc(const TcParams p, const __grid_constant__ CUtensorMap tm_x) {
   constexpr int kTcTok = kTok;
-  constexpr int kTcBuf = tc_buf(kTok);
+  constexpr int kWR = tc_wring(kTok), kXR = tc_xring(kTok);
   constexpr int kTcCols = tc_cols(kTok);
   constexpr int kKPer = kTcRows * kTcK / kThreads;           // k per thread and step
   constexpr int kWords = kKPer / 8;
   constexpr int kParts = kTcK / kKPer;                       // threads per weight row
-  constexpr uint32_t kXBytes = kTcTok * kTcK * 2;            // one activation tile
+  constexpr uint32_t kXBytes = tc_xbuf(kTok);               // one activation tile
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  // full[R] xfull[R] empty[R] done, then the TMEM address and the abort flag
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing * kTcBuf);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kRing * kTcBuf + 96);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kRing * kTcBuf + 112);
+  // weight stages, activation stages, then full[WR] empty[WR] xfull[XR]
+  // xempty[XR] done, the TMEM address and the abort flag
+  unsigned char* xstages = smem + kWR * kWBuf;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + tc_bars(kTok));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + tc_bars(kTok) + 224);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + tc_bars(kTok) + 240);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int n0 = blockIdx.x * kTcRows;
   const int m0 = blockIdx.y * kTcTok;
-  const uint32_t full0 = smem_addr(bars), xfull0 = full0 + 8 * kRing,
-                 empty0 = full0 + 16 * kRing, done = full0 + 24 * kRing;
+  const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8 * kWR, xfull0 = empty0 + 8 * kWR,
+                 xempty0 = xfull0 + 8 * kXR, done = xempty0 + 8 * kXR;
   const bool is_mma = warp == kThreads / 32;                // the extra warp issues the MMAs
 
   if (tid == 0) {
     *abort_flag = 0;
-    for (int r = 0; r < kRing; ++r) {
+    for (int r = 0; r < kWR; ++r) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * r), "r"(kThreads / 32) : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(xfull0 + 8 * r) : "memory");
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * r) : "memory");
+    }
+    for (int r = 0; r < kXR; ++r) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(xfull0 + 8 * r) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(xempty0 + 8 * r) : "memory");
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -293,7 +313,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   bool ok = true;
 
   // Each thread's global inputs of a step (its weight row's kKPer codes,
-  // scale and zero-point), loaded two steps ahead; past K they are zero
+  // scale and zero-point), loaded kAhead steps ahead; past K they are zero
   // (K is a multiple of 32), as the tensor copy makes the activations there.
   struct StepIn {
     uint32_t w[kWords];
@@ -314,7 +334,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         const uint2 v = __ldg(reinterpret_cast<const uint2*>(qrow + kk / 2));
         in.w[0] = v.x; in.w[1] = v.y;
       }
-      const int b = kk / p.block;
+      const int b = kk >> p.bshift;
       in.s = __half2float(__ushort_as_half(__ldg(srow + b)));
       if (zrow) {
         const uint32_t zb = __ldg(zrow + (b >> 1));
@@ -323,21 +343,28 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     }
   };
 
-  // Ring stage st % R.  Dequant warps write its hi and lo weight tiles once
-  // the MMAs of its previous use have committed (empty), then arrive on full;
-  // the MMA thread copies its activation tile by TMA (xfull), waits on full
-  // and xfull, issues the stage's MMAs and commits them to empty, and after
-  // the last stage to done.  Every wait is bounded; a wait that gives up
-  // raises the abort flag and the others then give up too.
+  // Step st uses weight stage st % WR and activation stage st % XR.  Dequant
+  // warps write the weight stage's hi and lo tiles once the MMAs of its
+  // previous use have committed (empty), then arrive on full; the MMA thread
+  // copies the activation tile by TMA (xfull) once the MMAs of that stage's
+  // previous use have committed (xempty), waits on full and xfull, issues the
+  // step's MMAs and commits them to empty and xempty, and after the last step
+  // to done.  Every wait is bounded; a wait that gives up raises the abort
+  // flag and the others then give up too.
   if (!is_mma) {
-    StepIn cur, nx1, nx2;
-    load_step(st_begin, cur);
-    if (nsteps > 1) load_step(st_begin + 1, nx1);
+    StepIn fifo[kAhead];                             // steps st .. st + kAhead - 1
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i)
+      if (i < nsteps) load_step(st_begin + i, fifo[i]);
+    int rs = 0;                                      // weight stage st % WR
+    uint32_t ph = 0;                                 // parity of (st / WR)
     for (int st = 0; st < nsteps; ++st) {
-      const int rs = st % kRing, use = st / kRing;
-      unsigned char* buf = smem + rs * kTcBuf;
-      if (st + 2 < nsteps) load_step(st_begin + st + 2, nx2);   // in flight for two steps
-      if (use > 0 && !tc_wait(empty0 + 8 * rs, (use - 1) & 1, p.err)) {
+      unsigned char* buf = smem + rs * kWBuf;
+      const StepIn cur = fifo[0];
+#pragma unroll
+      for (int i = 0; i + 1 < kAhead; ++i) fifo[i] = fifo[i + 1];
+      if (st + kAhead < nsteps) load_step(st_begin + st + kAhead, fifo[kAhead - 1]);
+      if (st >= kWR && !tc_wait(empty0 + 8 * rs, ph ^ 1u, p.err)) {
         *abort_flag = 1;
         break;
       }
@@ -349,59 +376,86 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
       const uint32_t s2k = static_cast<uint32_t>(__half_as_ushort(shk)) * 0x00010001u;
       const uint32_t zl = cur.z * 0x00010001u + 0x64006400u;
       const uint32_t zh = cur.z * 0x00100010u + 0x54005400u;
-#pragma unroll
-      for (int g = 0; g < kWords; ++g) {
+      // exact q - zp of pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7) of word g,
+      // regrouped into natural k order (k0,k1) (k2,k3) (k4,k5) (k6,k7)
+      auto pairs = [&](int g, uint32_t (&n)[4]) {
         const uint32_t word = cur.w[g], w8 = word >> 8;
-        // exact q - zp of pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7), regrouped
-        // into natural k order (k0,k1) (k2,k3) (k4,k5) (k6,k7)
         const uint32_t d0 = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl);
         const uint32_t d1 = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh);
         const uint32_t d2 = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl);
         const uint32_t d3 = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh);
-        uint4 hi, lo;
-        split_pair(prmt(d0, d1, 0x5410u), cur.s, s2, s2k, small, hi.x, lo.x);
-        split_pair(prmt(d2, d3, 0x5410u), cur.s, s2, s2k, small, hi.y, lo.y);
-        split_pair(prmt(d0, d1, 0x7632u), cur.s, s2, s2k, small, hi.z, lo.z);
-        split_pair(prmt(d2, d3, 0x7632u), cur.s, s2, s2k, small, hi.w, lo.w);
+        n[0] = prmt(d0, d1, 0x5410u);
+        n[1] = prmt(d2, d3, 0x5410u);
+        n[2] = prmt(d0, d1, 0x7632u);
+        n[3] = prmt(d2, d3, 0x7632u);
+      };
+      auto store = [&](int g, const uint4& hi, const uint4& lo) {
         const uint32_t off = sw128(wr, kWords * qk + g);
         *reinterpret_cast<uint4*>(buf + off) = hi;
         *reinterpret_cast<uint4*>(buf + kTcTile + off) = lo;
+      };
+      if (__all_sync(0xFFFFFFFFu, small)) {          // the usual case: fp16 split only
+#pragma unroll
+        for (int g = 0; g < kWords; ++g) {
+          uint32_t n[4];
+          pairs(g, n);
+          uint4 hi, lo;
+          split_pair_small(n[0], s2, s2k, hi.x, lo.x);
+          split_pair_small(n[1], s2, s2k, hi.y, lo.y);
+          split_pair_small(n[2], s2, s2k, hi.z, lo.z);
+          split_pair_small(n[3], s2, s2k, hi.w, lo.w);
+          store(g, hi, lo);
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < kWords; ++g) {
+          uint32_t n[4];
+          pairs(g, n);
+          uint4 hi, lo;
+          split_pair(n[0], cur.s, s2, s2k, small, hi.x, lo.x);
+          split_pair(n[1], cur.s, s2, s2k, small, hi.y, lo.y);
+          split_pair(n[2], cur.s, s2, s2k, small, hi.z, lo.z);
+          split_pair(n[3], cur.s, s2, s2k, small, hi.w, lo.w);
+          store(g, hi, lo);
+        }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0)
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(full0 + 8 * rs) : "memory");
-      cur = nx1;
-      nx1 = nx2;
+      if (++rs == kWR) {
+        rs = 0;
+        ph ^= 1u;
+      }
     }
     // the MMAs of the last stage have completed when done arrives
     if (!*abort_flag && !tc_wait(done, 0, p.err)) *abort_flag = 1;
   } else if (lane == 0) {
     // activation tile of step st (k0 = 64 (st_begin + st), rows m0 ..) into
-    // stage st % R: 128-byte rows, 128-byte swizzle (the MMA's layout);
+    // stage st % XR: 128-byte rows, 128-byte swizzle (the MMA's layout);
     // rows past M and k past K arrive as zeros
     auto copy_x = [&](int st) {
-      const int rs = st % kRing;
-      tc_expect_tx(xfull0 + 8 * rs, kXBytes);
-      tc_tma_2d(smem_addr(smem + rs * kTcBuf + 2 * kTcTile), &tm_x, (st_begin + st) * kTcK, m0,
-                xfull0 + 8 * rs);
+      const int xs = st % kXR;
+      tc_expect_tx(xfull0 + 8 * xs, kXBytes);
+      tc_tma_2d(smem_addr(xstages + xs * kXBytes), &tm_x, (st_begin + st) * kTcK, m0,
+                xfull0 + 8 * xs);
     };
     int issued = 0, consumed = 0;
-    for (; issued < kRing && issued < nsteps; ++issued) copy_x(issued);
+    for (; issued < kXR && issued < nsteps; ++issued) copy_x(issued);
     for (int st = 0; st < nsteps; ++st) {
-      const int rs = st % kRing, use = st / kRing;
-      if (!tc_wait(xfull0 + 8 * rs, use & 1, p.err)) {
+      const int rs = st % kWR, xs = st % kXR;
+      if (!tc_wait(xfull0 + 8 * xs, (st / kXR) & 1, p.err)) {
         *abort_flag = 1;
         break;
       }
       consumed = st + 1;
-      if (!tc_wait(full0 + 8 * rs, use & 1, p.err) || *abort_flag) {
+      if (!tc_wait(full0 + 8 * rs, (st / kWR) & 1, p.err) || *abort_flag) {
         *abort_flag = 1;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t a_hi = smem_addr(smem + rs * kTcBuf), a_lo = a_hi + kTcTile;
-      const uint32_t bx = a_hi + 2 * kTcTile;
+      const uint32_t a_hi = smem_addr(smem + rs * kWBuf), a_lo = a_hi + kTcTile;
+      const uint32_t bx = smem_addr(xstages + xs * kXBytes);
 #pragma unroll
       for (int ks = 0; ks < kTcK / 16; ++ks) {       // K = 16 slices: 32 bytes apart
         const uint32_t acc = (st > 0 || ks > 0) ? 1u : 0u;
@@ -410,11 +464,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                tc_idesc(kTok), acc);
       }
       tc_commit(empty0 + 8 * rs);
-      // refill the stage of step st - 1 once its MMAs (queued ahead of
-      // these) have completed
+      tc_commit(xempty0 + 8 * xs);
+      // refill the activation stage of step st - 1 once its MMAs (queued
+      // ahead of these) have completed
       if (st >= 1 && issued < nsteps) {
-        const int ps = (st - 1) % kRing;
-        if (!tc_wait(empty0 + 8 * ps, ((st - 1) / kRing) & 1, p.err)) {
+        const int ps = (st - 1) % kXR;
+        if (!tc_wait(xempty0 + 8 * ps, ((st - 1) / kXR) & 1, p.err)) {
           *abort_flag = 1;
           break;
         }
@@ -426,7 +481,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     } else {
       // copies still in flight land before the CTA's shared memory is released
       for (int st = consumed; st < issued; ++st)
-        if (!tc_wait(xfull0 + 8 * (st % kRing), (st / kRing) & 1, p.err)) break;
+        if (!tc_wait(xfull0 + 8 * (st % kXR), (st / kXR) & 1, p.err)) break;
     }
   }
   __syncthreads();
@@ -437,8 +492,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   const int lane_base = 32 * (warp & 3);
   const int col0 = kColsPerWarp * (warp >> 2);
   const int n = n0 + lane_base + lane;
-  // with a K split, the fp32 tile [row][activation row] goes to this CTA's
-  // shared memory (the stage buffers are free) instead of to y
+  // with a K split, the fp32 tile [activation row][weight row] goes to this
+  // CTA's shared memory (the stage buffers are free) instead of to y: a
+  // warp's lanes store consecutive words
   float* part = reinterpret_cast<float*>(smem);
   if (ok && !is_mma) {
 #pragma unroll 1
@@ -451,7 +507,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
       for (int j = 0; j < 32; ++j) {
         const float v = fmaf(vl[j], 1.f / 2048.f, vh[j]);
         if (p.ksplit > 1) {
-          part[(lane_base + lane) * kTcTok + col + j] = v;
+          part[(col + j) * kTcRows + lane_base + lane] = v;
         } else {
           const int m = m0 + col + j;
           if (n < p.N && m < p.M) pf_out(p.y, static_cast<size_t>(m) * p.N + n, v, p.out_bf16);
@@ -471,7 +527,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     if (ok) {
       for (int e = tid; e < share; e += kThreads + 32) {
         const int gidx = static_cast<int>(rank) * share + e;
-        const int row = gidx / kTcTok, tok = gidx - row * kTcTok;
+        const int tok = gidx / kTcRows, row = gidx - tok * kTcRows;   // y row, column
         const uint32_t local = part_addr + 4u * static_cast<uint32_t>(gidx);
         float sum = 0.f;
         for (int r = 0; r < p.ksplit; ++r) {
@@ -534,14 +590,16 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
   p.N = N;
   p.K = K;
   p.block = block;
+  p.bshift = block == 128 ? 7 : block == 64 ? 6 : 5;     // block 32, 64 or 128 here
   p.blocks = K / block;
   p.zstride = (p.blocks + 1) / 2;
   p.out_bf16 = out_bf16;
   p.err = err;
-  // Activation tiles of 256 rows (all of TMEM) where that still gives every
-  // SM a CTA, else 128.
+  // Activation tiles of 256 rows (all of TMEM) for M > 128: a CTA's dequant
+  // work per step does not depend on the tile width, so the wider tile does
+  // twice the products per dequantized weight (small grids split K below).
   const long long gx = (static_cast<long long>(N) + kTcRows - 1) / kTcRows;
-  const bool t256 = gx * ((static_cast<long long>(M) + 255) / 256) >= sms;
+  const bool t256 = M > 128;
   const int tok = t256 ? 256 : 128;
   const long long gy = (static_cast<long long>(M) + tok - 1) / tok;
   if (gx > 0x7FFFFFFFLL || gy > 65535) return fail(MNB_ERR_SHAPE, "prefill shape too large");

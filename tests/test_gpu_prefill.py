@@ -81,8 +81,28 @@ def test_tensor_core_full_size(M, N, K, block, symmetric):
 
 @pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
 @pytest.mark.parametrize("M,N,K,block,symmetric", [
+    (130, 257, 1024, 32, False), (300, 520, 2048, 64, True), (40, 1000, 512, 128, False),
+])
+def test_scale_ranges(M, N, K, block, symmetric, tc):
+    """Scales above 2 (the tcgen05 form's fp32 split), exactly 2 and just above,
+    and subnormal ones, mixed with the usual range within one warp's rows."""
+    inp = make_inputs(M, N, K, seed=M + N + 3, block=block)
+    sc = inp.scales.view(np.float16).astype(np.float32)
+    r = np.arange(N)
+    sc[r % 5 == 0] *= 900.0                              # up to 18
+    sc[r % 7 == 0] = 2.0
+    sc[r % 9 == 0] = np.float32(np.float16(2.0) + np.float16(2.0 ** -9))
+    sc[r % 11 == 0] = 2.0 ** -18                        # subnormal
+    sc[(r % 13 == 0)[:, None] & (np.arange(sc.shape[1]) % 3 == 0)[None, :]] *= -1.0
+    inp.scales[...] = sc.astype(np.float16).view(np.uint16)
+    cols = None if N <= 520 else np.arange(0, N, 3)
+    _run_both(inp, symmetric, cols=cols, tensor_cores=tc)
+
+
+@pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
+@pytest.mark.parametrize("M,N,K,block,symmetric", [
     (16, 512, 4096, 32, False), (9, 300, 8192, 64, True), (64, 4096, 4096, 128, False),
-    (33, 1000, 2048, 32, True),
+    (33, 1000, 2048, 32, True), (300, 1024, 4096, 32, False), (200, 2000, 2048, 64, True),
 ])
 def test_k_split_over_a_cluster(M, N, K, block, symmetric, tc):
     """Small grids split K over a thread-block cluster (up to 8 CTAs, partial

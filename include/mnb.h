@@ -203,7 +203,8 @@ const char *mnb_last_error_detail(void);
 /* Device-side error word of the current device: 0, or the first code a
  * kernel recorded when one of its bounded waits gave up (1 = stage data never
  * arrived, 2 = a stage was never released, 3 = copies still in flight at exit,
- * 4 = a reduction slot was never filled or freed).  Enqueues a read on
+ * 4 = a reduction slot was never filled or freed, 5 = a stage, activation copy
+ * or MMA completion of the tensor-memory prefill GEMM never arrived).  Enqueues a read on
  * `stream`, synchronises that stream and writes the word to *code; clears it
  * when `clear` is non-zero.  Returns MNB_ERR_CUDA if the read fails. */
 int mnb_device_error(void *stream, unsigned int *code, int clear);

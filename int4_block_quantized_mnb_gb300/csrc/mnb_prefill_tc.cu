@@ -10,19 +10,22 @@
 // accumulators stay in TMEM across the whole K loop.
 //
 // Tile.  A CTA computes 128 weight rows x 128 or 256 activation rows (UMMA
-// M = 128, N = 128 or 256) in K steps of 64, through a ring of three stage
-// buffers.  Its 512 dequant threads write, per step, the hi and lo tiles of the
-// weights (thread = one row x 16 k: one code load, its block's scale and
-// zero-point) and the activation tile in the 128-byte swizzled K-major layout
-// the tensor core reads, from registers loaded one step ahead; both keep the
-// dequant's (k, k + 4) pairing (the same permutation of k in both operands
-// leaves each dot product unchanged).  Each dequant warp marks a stage full on
-// its mbarrier; one more warp waits for it, issues the step's eight MMAs (hi
-// and lo, four K = 16 slices each) and commits them to the stage's empty
-// barrier, which the dequant warps wait on before they refill it.  The
-// epilogue reads TMEM (warp w: lanes 32 (w mod 4) .. + 31, 32 columns by w / 4),
-// forms D_hi + 2^-11 D_lo, rounds once to fp16 and, on the bf16 arm, narrows.
-// A grid smaller than the SM count splits K over a cluster of up to 8 CTAs;
+// M = 128, N = 128 or 256) in K steps of 64, through two rings of stage
+// buffers in the 128-byte swizzled K-major layout the tensor core reads:
+//   weights      512 dequant threads write each step's hi and lo tiles
+//                (thread = one row x 16 k: its codes, scale and zero-point,
+//                loaded two steps ahead), regrouping the dequant's exact
+//                (k, k + 4) pairs into natural k order; each warp then
+//                arrives on the stage's "full" mbarrier;
+//   activations  one more warp copies each step's tile with a tiled tensor
+//                copy (zero fill past K and M) onto the stage's "xfull"
+//                barrier, a few steps ahead.
+// That warp waits on both, issues the step's eight MMAs (hi and lo, four
+// K = 16 slices each) and commits them to the stages' "empty" and "xempty"
+// barriers, which gate their refills.  The epilogue reads TMEM (warp w:
+// lanes 32 (w mod 4) .. + 31, a quarter of the columns by w / 4), forms
+// D_hi + 2^-11 D_lo, rounds once to fp16 and, on the bf16 arm, narrows.  A
+// grid of at most half the SM count splits K over a cluster of up to 8 CTAs;
 // their fp32 tiles are summed in rank order through distributed shared memory.
 #include "mnb.h"
 #include "mnb_dequant.cuh"
@@ -61,10 +64,10 @@ constexpr int tc_wring(int kTok) { return kTok == 256 ? 2 : 3; }
 constexpr int tc_xring(int kTok) { return kTok == 256 ? 4 : 6; }
 constexpr int kAhead = 2;                    // steps of codes in flight per dequant thread
 constexpr int kDequantThreads = 512;         // dequant and epilogue threads; one more warp issues MMAs
-constexpr int tc_bars(int kTok) { return tc_wring(kTok) * kWBuf + tc_xring(kTok) * tc_xbuf(kTok); }
-constexpr int tc_smem(int kTok) { return tc_bars(kTok) + 1024 + 256; }   // + alignment, barriers
+constexpr int tc_ring_bytes(int kTok) { return tc_wring(kTok) * kWBuf + tc_xring(kTok) * tc_xbuf(kTok); }
+constexpr int tc_smem(int kTok) { return tc_ring_bytes(kTok) + 1024 + 256; }   // + alignment, barriers
 constexpr int tc_cols(int kTok) { return 2 * kTok; }
-constexpr unsigned kTcErrMma = 5;            // device error: MMA completion never arrived
+constexpr unsigned kTcErrMma = 5;            // device error: a pipeline wait gave up
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
 
 struct TcParams {
@@ -139,8 +142,9 @@ __device__ __forceinline__ unsigned long long tc_now() {
   return t;
 }
 
-// Bounded wait for an MMA commit; false (and the device error word set) when
-// the completion did not arrive within the limit.
+// Bounded wait for a phase of one of the pipeline's mbarriers (stage full,
+// copy landed, MMAs committed); false (and the device error word set) when it
+// did not complete within the limit.
 __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
   if (tc_try_wait(bar, parity)) return true;
   const unsigned long long t0 = tc_now();
@@ -258,9 +262,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   // weight stages, activation stages, then full[WR] empty[WR] xfull[XR]
   // xempty[XR] done, the TMEM address and the abort flag
   unsigned char* xstages = smem + kWR * kWBuf;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + tc_bars(kTok));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + tc_bars(kTok) + 224);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + tc_bars(kTok) + 240);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + tc_ring_bytes(kTok));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + tc_ring_bytes(kTok) + 224);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + tc_ring_bytes(kTok) + 240);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;

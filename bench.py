@@ -56,7 +56,10 @@ def parse():
     ap.add_argument("--split-k", type=int, default=0,
                     help="0 = the library's choice (as a user calling with split_k=0 gets)")
     ap.add_argument("--tensor-cores", action="store_true",
-                    help="permit the tensor-core kernel (MNB_FLAG_TENSOR_CORES)")
+                    help="permit the decode step kernel's tensor-core math (MNB_FLAG_TENSOR_CORES)")
+    ap.add_argument("--prefill-mma-sync", action="store_true",
+                    help="M > 8: the mma.sync form of the prefill GEMM instead of its tcgen05 form "
+                         "(MNB_FLAG_PREFILL_MMA_SYNC)")
     ap.add_argument("--ab-staged", action="store_true",
                     help="time a synthetic decode step of bf16 GEMVs: fp16 GEMV + separate "
                          "narrowing launch (staged route) against the direct bf16 store")
@@ -501,6 +504,7 @@ def main():
                                for _ in range(R - 1)]
     split_k = args.split_k
     tc = bool(args.tensor_cores)
+    pm = bool(args.prefill_mma_sync)
     stream = torch.cuda.Stream(dev)
 
     def step(j):
@@ -508,7 +512,7 @@ def main():
         for i, o in enumerate(outs):
             q, s, z = copies[(j * L + i) % R]
             mnb.gemv(x, q, s, z, out_dtype=o, split_k=split_k, y=ys[o], stream=stream,
-                     weights_ready=True, tensor_cores=tc, block=w_block(w))
+                     weights_ready=True, tensor_cores=tc, block=w_block(w), prefill_mma_sync=pm)
 
     # Warm-up: W eager steps.
     with torch.cuda.stream(stream):
@@ -591,7 +595,7 @@ def main():
                 dz.copy_(hz, non_blocking=True)
             for o in outs:
                 mnb.gemv(dx, dq, ds, dz, out_dtype=o, split_k=split_k, y=ys[o], stream=stream,
-                         tensor_cores=tc, block=w_block(w))
+                         tensor_cores=tc, block=w_block(w), prefill_mma_sync=pm)
                 hy[o].copy_(ys[o], non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -624,6 +628,7 @@ def main():
         "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "out_dtypes": outs,
                    "block": w_block(w), "zero_points": w_zp(w, inp) is not None,
                    "split_k": split_k if split_k else "auto", "tensor_cores": tc,
+                   **({"prefill_form": "mma.sync" if pm else "tcgen05"} if w.M > 8 else {}),
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"inputs larger than L2: {R} rotating weight copies, "
                          f"{R * wbytes / 2**20:.0f} MiB vs L2 {l2 / 2**20:.0f} MiB",

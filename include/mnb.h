@@ -145,16 +145,28 @@ int mnb_gemv(const void *x, const uint8_t *qweight, const void *scales, const ui
  * accumulates them in fp32 with mma.sync m16n8k16 instead of fp32 FMAs;
  * results meet the same error bound and bf16 invariant, but their bits may
  * differ from the default kernels'. Without the flag no decode launch (M <=
- * MNB_MAX_M) uses a tensor-core instruction. On the prefill path (M >
- * MNB_MAX_M, which by default runs mma.sync on the same exact products) the
- * flag selects the tcgen05 form when x is 16-byte aligned: every dequantized
- * weight (q - zp) s is split exactly into two fp16 parts, so the products
- * stay exact and the sums fp32 (in tensor memory); it differs from the
- * default only where an infinite activation meets a weight whose low part is
- * zero (NaN instead of +-inf) and for weights below 2^-11 in magnitude (the
- * low part is rounded).
+ * MNB_MAX_M) uses a tensor-core instruction. The prefill path (M >
+ * MNB_MAX_M) always runs on tensor cores and ignores this flag.
  */
 #define MNB_FLAG_TENSOR_CORES 2u
+
+/*
+ * The prefill path (M > MNB_MAX_M) has two forms of one GEMM, both with exact
+ * products, fp32 sums and the decode epilogue, meeting the same bound and
+ * bf16 invariant (their fp16 bits may differ: different summation order):
+ *   tcgen05   the default where x is 16-byte aligned.  Every dequantized
+ *             weight (q - zp) s is split exactly into two fp16 parts
+ *             (hi = fp16(w), lo = (w - hi) 2^11, both exact); two fp16
+ *             tcgen05 GEMMs accumulate x hi and x lo in fp32 in tensor
+ *             memory and the epilogue forms hi + 2^-11 lo (hi alone where it
+ *             is not finite, so infinities and NaNs follow the exact form).
+ *   mma.sync  per-block fp32 sums of the exact fp16 products (q - zp) x,
+ *             scaled into fp32 accumulators.  Used where x is not 16-byte
+ *             aligned, and on request:
+ * MNB_FLAG_PREFILL_MMA_SYNC: run the mma.sync form of the prefill GEMM.  No
+ * effect for M <= MNB_MAX_M.
+ */
+#define MNB_FLAG_PREFILL_MMA_SYNC 4u
 
 /* mnb_gemv with flags (0 or an OR of the MNB_FLAG_* bits); mnb_gemv(...) is
  * mnb_gemv_flags(..., 0, stream).  Same arguments, checks and statuses, plus
@@ -212,14 +224,14 @@ int mnb_device_error(void *stream, unsigned int *code, int clear);
 /* Launch counters, for tests that must prove the GPU kernel ran:
  *   [0] launches, [1] fp16-output launches, [2] bf16-output launches,
  *   [3] launches with split_k > 1 (cluster reduction), [4 + M - 1] launches
- *   with M rows (M = 1..8), [12] launches with tensor-core math (only with
- *   MNB_FLAG_TENSOR_CORES), [13] launches of the step kernel (either math:
+ *   with M rows (M = 1..8), [12] decode launches with tensor-core math (only
+ *   with MNB_FLAG_TENSOR_CORES), [13] launches of the step kernel (either math:
  *   tiles streamed in K steps by TMA tensor copies, no K split), [14]
  *   launches of mnb_cast_f16_to_bf16, [15] launches of the general-format
  *   kernel (block size other than 32, or no zero-points), [16] launches of the
- *   prefill GEMM (M > MNB_MAX_M).
+ *   prefill GEMM (M > MNB_MAX_M), [17] prefill launches of its tcgen05 form.
  * Copies min(n, MNB_NUM_COUNTERS) counters to out; returns how many. */
-#define MNB_NUM_COUNTERS 17
+#define MNB_NUM_COUNTERS 18
 int mnb_debug_counters(uint64_t *out, int n);
 void mnb_debug_counters_reset(void);
 

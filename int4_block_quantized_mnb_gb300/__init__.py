@@ -10,13 +10,13 @@ from __future__ import annotations
 
 import ctypes
 
-from ._native import (BLOCK, FLAG_TENSOR_CORES, FLAG_WEIGHTS_READY, MAX_M, MAX_SPLIT_K,
-                      NUM_COUNTERS, OUT_BF16, OUT_F16,
-                      MnbError, check, load)
+from ._native import (BLOCK, FLAG_PREFILL_MMA_SYNC, FLAG_TENSOR_CORES, FLAG_WEIGHTS_READY, MAX_M,
+                      MAX_SPLIT_K, NUM_COUNTERS, OUT_BF16, OUT_F16, MnbError, check, load)
 
 __all__ = ["gemv", "gemv_ptr", "cast_f16_to_bf16", "split_k_auto", "min_split_k", "max_split_k", "counters",
            "reset_counters", "device_error", "MnbError", "OUT_F16", "OUT_BF16", "BLOCK",
-           "MAX_M", "MAX_SPLIT_K", "FLAG_WEIGHTS_READY", "FLAG_TENSOR_CORES"]
+           "MAX_M", "MAX_SPLIT_K", "FLAG_WEIGHTS_READY", "FLAG_TENSOR_CORES",
+           "FLAG_PREFILL_MMA_SYNC"]
 
 _DTYPES = {"f16": OUT_F16, "float16": OUT_F16, "bf16": OUT_BF16, "bfloat16": OUT_BF16}
 
@@ -47,7 +47,8 @@ def gemv_ptr(x: int, qweight: int, scales: int, zp: int, y: int, M: int, N: int,
 
 
 def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stream=None,
-         weights_ready: bool = False, tensor_cores: bool = False, block: int = BLOCK):
+         weights_ready: bool = False, tensor_cores: bool = False, block: int = BLOCK,
+         prefill_mma_sync: bool = False):
     """y = MatMulNBits(x, qweight, scales, zp) on the current CUDA device.
 
     x [M][K] float16, qweight [N][K/2] uint8, scales [N][K/block] float16,
@@ -57,7 +58,10 @@ def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stre
     promises that the kernel launched just before on the stream does not
     write qweight, scales or zp (static weights), so the call may start
     streaming them before that kernel completes.  ``tensor_cores=True``
-    permits the tensor-core kernel where it applies (MNB_FLAG_TENSOR_CORES).
+    permits the decode step kernel's tensor-core math where it applies
+    (MNB_FLAG_TENSOR_CORES).  ``prefill_mma_sync=True`` runs the mma.sync form
+    of the prefill GEMM (M > 8) instead of its tcgen05 form
+    (MNB_FLAG_PREFILL_MMA_SYNC).
     """
     import torch
     code = _out_code(out_dtype)
@@ -90,7 +94,8 @@ def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stre
                  0 if zp is None else zp.data_ptr(), y.data_ptr(), M, N, K, int(block), code,
                  int(split_k), stream.cuda_stream,
                  (FLAG_WEIGHTS_READY if weights_ready else 0) |
-                 (FLAG_TENSOR_CORES if tensor_cores else 0))
+                 (FLAG_TENSOR_CORES if tensor_cores else 0) |
+                 (FLAG_PREFILL_MMA_SYNC if prefill_mma_sync else 0))
     return y
 
 

@@ -18,11 +18,12 @@ STATUS = {0: "MNB_OK", 1: "MNB_ERR_NULL", 2: "MNB_ERR_SHAPE", 3: "MNB_ERR_BLOCK"
           8: "MNB_ERR_CUDA", 9: "MNB_ERR_DEVICE", 10: "MNB_ERR_FLAGS"}
 FLAG_WEIGHTS_READY = 1
 FLAG_TENSOR_CORES = 2
+FLAG_PREFILL_MMA_SYNC = 4
 MAX_M = 8
 MAX_PREFILL_M = 4194240
 BLOCK = 32
 MAX_SPLIT_K = 8
-NUM_COUNTERS = 17
+NUM_COUNTERS = 18
 
 # Every symbol the header declares, with (restype, argtypes).
 _vp, _u8p, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)

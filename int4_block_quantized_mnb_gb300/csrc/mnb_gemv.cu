@@ -1366,7 +1366,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 std::atomic<unsigned long long> g_counters[MNB_NUM_COUNTERS];
 
-// mnb_prefill_tc.cu: the prefill GEMM on tcgen05 (MNB_FLAG_TENSOR_CORES).
+// mnb_prefill_tc.cu: the prefill GEMM on tcgen05 (the default form).
 int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                       void* y, int M, int N, int K, int block, int out_bf16, unsigned int* err,
                       int sms, cudaStream_t stream);
@@ -1799,8 +1799,9 @@ int gemm_prefill(const void* x, const uint8_t* qweight, const void* scales, cons
   DeviceInfo dev;
   int st = device_info(&dev);
   if (st != MNB_OK) return st;
-  // tcgen05 form on request, where the activations are 16-byte aligned
-  const bool tc = (flags & MNB_FLAG_TENSOR_CORES) && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  // the tcgen05 form where the activations are 16-byte aligned (its tensor
+  // copies need it) unless the mma.sync form is requested
+  const bool tc = !(flags & MNB_FLAG_PREFILL_MMA_SYNC) && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   if (tc)
     st = launch_prefill_tc(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
                            dev.err, dev.sms, static_cast<cudaStream_t>(stream));
@@ -1808,10 +1809,8 @@ int gemm_prefill(const void* x, const uint8_t* qweight, const void* scales, cons
     st = launch_prefill(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
                         dev.sms, static_cast<cudaStream_t>(stream));
   if (st != MNB_OK) return st;
-  if (tc) {
-    g_counters[12].fetch_add(1, std::memory_order_relaxed);
-    g_counters[16].fetch_add(1, std::memory_order_relaxed);
-  }
+  g_counters[16].fetch_add(1, std::memory_order_relaxed);
+  if (tc) g_counters[17].fetch_add(1, std::memory_order_relaxed);
   g_counters[0].fetch_add(1, std::memory_order_relaxed);
   g_counters[out_dtype == MNB_OUT_BF16 ? 2 : 1].fetch_add(1, std::memory_order_relaxed);
   return MNB_OK;
@@ -1877,7 +1876,8 @@ int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const ui
 int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                    void* y, int M, int N, int K, int block, int out_dtype, int split_k,
                    unsigned int flags, void* stream) {
-  if (flags & ~static_cast<unsigned int>(MNB_FLAG_WEIGHTS_READY | MNB_FLAG_TENSOR_CORES))
+  if (flags & ~static_cast<unsigned int>(MNB_FLAG_WEIGHTS_READY | MNB_FLAG_TENSOR_CORES |
+                                          MNB_FLAG_PREFILL_MMA_SYNC))
     return fail(MNB_ERR_FLAGS, "unknown flag bits");
   if (!x || !qweight || !scales || !y) return fail(MNB_ERR_NULL, "x, qweight, scales and y are required");
   if (block != 16 && block != 32 && block != 64 && block != 128)

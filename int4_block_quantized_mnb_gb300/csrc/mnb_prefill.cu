@@ -446,7 +446,6 @@ int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, co
   }
   const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC(prefill)");
-  g_counters[16].fetch_add(1, std::memory_order_relaxed);
   return MNB_OK;
 }
 

@@ -509,7 +509,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
       tc_ld32(tmem + (static_cast<uint32_t>(lane_base) << 16) + kTcTok + col, vl);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float v = fmaf(vl[j], 1.f / 2048.f, vh[j]);
+        // D_hi is non-finite whenever a term is (hi is nonzero wherever w
+        // is); it then holds the exact form's value (inf, or NaN for inf x 0)
+        // and D_lo, whose lo' may be 0 there, must not be added
+        const float v = fabsf(vh[j]) <= 3.402823466e38f ? fmaf(vl[j], 1.f / 2048.f, vh[j]) : vh[j];
         if (p.ksplit > 1) {
           part[(col + j) * kTcRows + lane_base + lane] = v;
         } else {

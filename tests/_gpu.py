@@ -48,13 +48,13 @@ def sentinel(M, N, out, device="cuda") -> torch.Tensor:
     return torch.full((M, N), float("nan"), dtype=dt, device=device)
 
 
-def run(dev, out="f16", split_k=0, y=None, tensor_cores=False, block=32):
+def run(dev, out="f16", split_k=0, y=None, tensor_cores=False, block=32, prefill_mma_sync=False):
     x, q, s, z = dev
     M, N = x.shape[0], q.shape[0]
     if y is None:
         y = sentinel(M, N, out, x.device)
     mnb.gemv(x, q, s, z, out_dtype=out, split_k=split_k, y=y, tensor_cores=tensor_cores,
-             block=block)
+             block=block, prefill_mma_sync=prefill_mma_sync)
     torch.cuda.synchronize()
     return y
 

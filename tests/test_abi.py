@@ -73,11 +73,11 @@ def test_host_validation(lib, kw, status):
 
 
 def test_unknown_flags_rejected(lib):
-    st = lib.mnb_gemv_flags(X, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, 4, None)
-    assert st == 10
+    for bad in (8, 16, 0x80000000, 9):
+        assert lib.mnb_gemv_flags(X, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, bad, None) == 10
     # valid flags fall through to the ordinary checks (here: a NULL pointer)
-    assert lib.mnb_gemv_flags(0, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, 1, None) == 1
-    assert lib.mnb_gemv_flags(0, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, 3, None) == 1
+    for ok in (1, 2, 3, 4, 7):
+        assert lib.mnb_gemv_flags(0, Q, S, Z, Y, 1, 64, 256, 32, 0, 1, ok, None) == 1
 
 
 def test_split_limits(lib):

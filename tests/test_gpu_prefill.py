@@ -21,14 +21,17 @@ def built():
     mnb.load()
 
 
-def _run_both(inp, symmetric, cols=None, tensor_cores=False):
+def _run_both(inp, symmetric, cols=None, tc=True):
+    """Both output dtypes on the tcgen05 form (the default) or, with tc=False,
+    the mma.sync form; checks which form ran and the oracle bound."""
     dev = _gpu.to_device(inp, symmetric=symmetric)
     c0 = mnb.counters()
-    y16 = _gpu.bits(_gpu.run(dev, "f16", 0, block=inp.block, tensor_cores=tensor_cores))
-    ybf = _gpu.bits(_gpu.run(dev, "bf16", 0, block=inp.block, tensor_cores=tensor_cores))
+    y16 = _gpu.bits(_gpu.run(dev, "f16", 0, block=inp.block, prefill_mma_sync=not tc))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16", 0, block=inp.block, prefill_mma_sync=not tc))
     c1 = mnb.counters()
     assert c1[16] - c0[16] == 2
-    assert c1[12] - c0[12] == (2 if tensor_cores else 0)      # tcgen05 form only on request
+    assert c1[17] - c0[17] == (2 if tc else 0)
+    assert c1[12] == c0[12]                                     # decode tensor-core math only
     return _gpu.compare(inp, y16, ybf, cols=cols, symmetric=symmetric)
 
 
@@ -39,7 +42,7 @@ def test_small_shapes(block, symmetric, M, N, K):
     if K % block:
         pytest.skip("K not a multiple of the block size")
     inp = make_inputs(M, N, K, seed=M * 11 + N + K + block, block=block)
-    _run_both(inp, symmetric)
+    _run_both(inp, symmetric, tc=False)
 
 
 @pytest.mark.parametrize("M,N,K,block,symmetric", [
@@ -47,23 +50,24 @@ def test_small_shapes(block, symmetric, M, N, K):
     (1000, 1024, 8192, 128, False),
 ])
 def test_full_size(M, N, K, block, symmetric):
-    """Prefill-sized layers, compared on sampled output columns."""
+    """Prefill-sized layers on the mma.sync form, compared on sampled output
+    columns."""
     inp = make_inputs(M, N, K, seed=M + N + block, block=block)
     cols = np.random.default_rng(M).choice(N, size=min(N, 96), replace=False)
     cols.sort()
-    _run_both(inp, symmetric, cols=cols)
+    _run_both(inp, symmetric, cols=cols, tc=False)
 
 
 @pytest.mark.parametrize("block,symmetric", FORMATS, ids=FORMAT_IDS)
 @pytest.mark.parametrize("M", [9, 64, 130, 257])
 @pytest.mark.parametrize("N,K", [(1, 128), (33, 96), (130, 1024), (257, 384)])
 def test_tensor_core_small_shapes(block, symmetric, M, N, K):
-    """The tcgen05 form (MNB_FLAG_TENSOR_CORES): each weight split exactly into
-    two fp16 parts, fp32 accumulators in tensor memory; same bound."""
+    """The tcgen05 form (the default): each weight split exactly into two fp16
+    parts, fp32 accumulators in tensor memory; same bound."""
     if K % block:
         pytest.skip("K not a multiple of the block size")
     inp = make_inputs(M, N, K, seed=M * 13 + N + K + block, block=block)
-    _run_both(inp, symmetric, tensor_cores=True)
+    _run_both(inp, symmetric, tc=True)
 
 
 @pytest.mark.parametrize("M,N,K,block,symmetric", [
@@ -76,7 +80,7 @@ def test_tensor_core_full_size(M, N, K, block, symmetric):
     inp = make_inputs(M, N, K, seed=M + N + block + 1, block=block)
     cols = np.random.default_rng(M + 1).choice(N, size=min(N, 96), replace=False)
     cols.sort()
-    _run_both(inp, symmetric, cols=cols, tensor_cores=True)
+    _run_both(inp, symmetric, cols=cols, tc=True)
 
 
 @pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
@@ -96,7 +100,7 @@ def test_scale_ranges(M, N, K, block, symmetric, tc):
     sc[(r % 13 == 0)[:, None] & (np.arange(sc.shape[1]) % 3 == 0)[None, :]] *= -1.0
     inp.scales[...] = sc.astype(np.float16).view(np.uint16)
     cols = None if N <= 520 else np.arange(0, N, 3)
-    _run_both(inp, symmetric, cols=cols, tensor_cores=tc)
+    _run_both(inp, symmetric, cols=cols, tc=tc)
 
 
 @pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
@@ -110,10 +114,10 @@ def test_k_split_over_a_cluster(M, N, K, block, symmetric, tc):
     forms: within the bound, and the same bits on every run."""
     inp = make_inputs(M, N, K, seed=M + K + block, block=block)
     cols = None if N <= 512 else np.arange(0, N, 9)
-    _run_both(inp, symmetric, cols=cols, tensor_cores=tc)
+    _run_both(inp, symmetric, cols=cols, tc=tc)
     dev = _gpu.to_device(inp, symmetric=symmetric)
-    a = _gpu.bits(_gpu.run(dev, "f16", 0, block=block, tensor_cores=tc))
-    b = _gpu.bits(_gpu.run(dev, "f16", 0, block=block, tensor_cores=tc))
+    a = _gpu.bits(_gpu.run(dev, "f16", 0, block=block, prefill_mma_sync=not tc))
+    b = _gpu.bits(_gpu.run(dev, "f16", 0, block=block, prefill_mma_sync=not tc))
     assert np.array_equal(a, b)
 
 
@@ -132,6 +136,60 @@ def test_exact_zero_rows():
     assert np.all(y2 == 0)
 
 
+@pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
+def test_non_finite_inputs_follow_ieee(tc):
+    """+inf meeting nonzero weights gives the exact form's +-inf (the tcgen05
+    form must not add its low part, whose lo' is often 0 there); +inf meeting
+    a code equal to its zero-point gives NaN; -inf and NaN propagate."""
+    M, N, K = 20, 70, 512
+    inp = make_inputs(M, N, K, seed=12)
+    xs = inp.x.copy()
+    xs[0, 3] = 0x7C00                    # +inf
+    xs[5, 100] = 0xFC00                  # -inf
+    xs[7, 200] = 0x7E00                  # NaN
+    inp.x = xs
+    qw = inp.qweight.copy()
+    z0 = int(inp.zp[0, 0]) & 0xF
+    qw[0, 1] = (qw[0, 1] & 0x0F) | (z0 << 4)          # row 0, k = 3: q = zp
+    inp.qweight = qw
+    dev = _gpu.to_device(inp)
+    y16 = _gpu.bits(_gpu.run(dev, "f16", 0, prefill_mma_sync=not tc))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16", 0, prefill_mma_sync=not tc))
+    o = _gpu.oracle()
+    ref = o.gemv(inp.x, inp.qweight, inp.scales, inp.zp, M, N, K)
+    g, r = o.f16_to_f64(y16), o.f16_to_f64(ref["y_f16"])
+    assert np.isnan(r[0, 0]) and np.isinf(r[0]).sum() > 0 and np.isinf(r[5]).sum() > 0
+    assert np.array_equal(np.isnan(g), np.isnan(r))
+    assert np.array_equal(g[np.isinf(r)], r[np.isinf(r)])
+    fin = np.isfinite(r)
+    bound = _gpu.REL * np.abs(r[fin]) + _gpu.ABS * ref["abs_sum"][fin]
+    assert np.all(np.abs(g[fin] - r[fin]) <= bound)
+    assert np.array_equal(ybf, o.f16_to_bf16(y16))
+
+
+@pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
+def test_exact_sums_with_rounded_weights(tc):
+    """Small integer activations and one scale per weight row: on even rows a
+    small normal one with a full 11-bit significand (1e-4 .. 4e-4), so fp16(w)
+    rounds for many weights and the tcgen05 form's low parts are nonzero; on
+    odd rows a subnormal one (k 2^-24), so its high parts are subnormal fp16
+    operands.  Every sum is exact in fp32 (s times an integer below 2^13), so
+    both forms must give the oracle's fp16 bits exactly."""
+    M, N, K = 16, 64, 128
+    inp = make_inputs(M, N, K, seed=21)
+    rng = np.random.default_rng(21)
+    inp.x = rng.integers(-3, 4, size=(M, K)).astype(np.float16).view(np.uint16)
+    sc = rng.uniform(1e-4, 4e-4, size=N).astype(np.float16)
+    sc[1::2] = (rng.integers(1, 1024, size=N // 2) * 2.0 ** -24).astype(np.float16)
+    assert np.all(sc[0::2].astype(np.float64) >= 2.0 ** -14)          # normal
+    assert np.all(sc[1::2].astype(np.float64) < 2.0 ** -14)           # subnormal
+    inp.scales[...] = np.repeat(sc[:, None], inp.scales.shape[1], axis=1).view(np.uint16)
+    dev = _gpu.to_device(inp)
+    y16 = _gpu.bits(_gpu.run(dev, "f16", 0, prefill_mma_sync=not tc))
+    ref = _gpu.oracle().gemv(inp.x, inp.qweight, inp.scales, inp.zp, M, N, K)
+    assert np.array_equal(y16, ref["y_f16"]), int((y16 != ref["y_f16"]).sum())
+
+
 def test_misaligned_activations():
     M, N, K = 20, 70, 512
     inp = make_inputs(M, N, K, seed=8)
@@ -140,8 +198,12 @@ def test_misaligned_activations():
     xm = buf[1:1 + M * K].view(M, K)
     xm.copy_(x)
     assert xm.data_ptr() % 16 != 0
-    a = _gpu.bits(mnb.gemv(x, q, s, z, "f16"))
+    # unaligned activations take the synchronous mma.sync form: the bits of
+    # the pipelined mma.sync form on aligned activations, never the tcgen05 form
+    a = _gpu.bits(mnb.gemv(x, q, s, z, "f16", prefill_mma_sync=True))
+    c0 = mnb.counters()
     b = _gpu.bits(mnb.gemv(xm, q, s, z, "f16"))
+    assert mnb.counters()[17] == c0[17]
     assert np.array_equal(a, b)
     _gpu.compare(inp, b, None)
 

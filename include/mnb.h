@@ -98,10 +98,12 @@ typedef enum mnb_status {
  *            split_k 0 or 1).   N >= 1.   K >= 32, a multiple of 32 and of
  *            block.
  *   block    16, 32 (MNB_BLOCK), 64 or 128.  Block 32 with zero-points runs
- *            the kernels tuned for it; the other formats run one CUDA-core
- *            kernel of the same exact arithmetic, where split_k (0 = chosen
- *            by the library) is the number of warps that split each row's K
- *            range inside one CTA, at most 8.
+ *            the kernels tuned for it, and so does block 32 without them
+ *            where the TMA step kernel applies (constant zero-points of 8 in
+ *            its stages); the other formats run one CUDA-core kernel of the
+ *            same exact arithmetic, where split_k (0 = chosen by the
+ *            library) is the number of warps that split each row's K range
+ *            inside one CTA, at most 8.
  *   out_dtype  an mnb_out_dtype.  It changes only the final store: for the
  *            same inputs and split_k the bf16 result equals the
  *            round-to-nearest-even bf16 narrowing of the fp16 result, bit

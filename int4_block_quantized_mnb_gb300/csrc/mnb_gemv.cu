@@ -855,7 +855,7 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.tx_bytes));
     tma_load_3d(st, tm_q, 0, row0, seg0, bar);
     tma_load_3d(st + p.sc_offset, tm_sc, 0, seg0, row0, bar);
-    tma_load_3d(st + p.zp_offset, tm_zp, 0, seg0 >> 2, row0, bar);
+    if (p.zp) tma_load_3d(st + p.zp_offset, tm_zp, 0, seg0 >> 2, row0, bar);
     issued = i + 1;
     if (++step == p.steps) {
       step = 0;
@@ -928,6 +928,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (p.zp == nullptr) {
+    // symmetric format: no zero-point copies; every stage's zero-point bytes
+    // hold 0x88 (zero-point 8 in both nibbles) for the whole launch
+    for (int s = 0; s < p.stages; ++s)
+      for (int i = threadIdx.x; i < p.zp_bytes / 16; i += blockDim.x)
+        *reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes + p.zp_offset +
+                                  16 * i) = make_uint4(0x88888888u, 0x88888888u, 0x88888888u,
+                                                       0x88888888u);
   }
   __syncthreads();
   allow_dependents();
@@ -1909,7 +1918,19 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
                                     std::to_string(hi) + "] for this M and K");
   DeviceInfo dev;
   if ((st = device_info(&dev)) != MNB_OK) return st;
-  if (block != kBlock || zp == nullptr) {
+  const bool tc = (flags & MNB_FLAG_TENSOR_CORES) != 0;
+  const int math = step_math(M, tc);
+  bool step = block == kBlock && use_step(M, K, split_k, scales, zp, tc);
+  Plan plan{};
+  if (step && make_mma_plan(dev, M, N, K, &plan) != MNB_OK) {
+    step = false;                                 // no stage layout fits: row-tile kernel
+    plan = Plan{};
+  }
+  // block 32 without zero-points runs the step kernel where it applies (its
+  // stages then hold constant zero-points of 8); the other formats, and the
+  // symmetric format where the step kernel does not apply, run one CUDA-core
+  // kernel for all of them
+  if (block != kBlock || (zp == nullptr && !step)) {
     // the other formats of the family: one CUDA-core kernel for all of them
     if ((st = launch_general(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
                              split_k, dev.sms, static_cast<cudaStream_t>(stream))) != MNB_OK)
@@ -1918,14 +1939,6 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
     g_counters[out_dtype == MNB_OUT_BF16 ? 2 : 1].fetch_add(1, std::memory_order_relaxed);
     g_counters[4 + M - 1].fetch_add(1, std::memory_order_relaxed);
     return MNB_OK;
-  }
-  const bool tc = (flags & MNB_FLAG_TENSOR_CORES) != 0;
-  const int math = step_math(M, tc);
-  bool step = use_step(M, K, split_k, scales, zp, tc);
-  Plan plan{};
-  if (step && make_mma_plan(dev, M, N, K, &plan) != MNB_OK) {
-    step = false;                                 // no stage layout fits: row-tile kernel
-    plan = Plan{};
   }
   const bool mma = step && math == kMathMma;
   const int split = step ? 1 : (split_k == 0 ? auto_split(M, N, K, dev.sms) : split_k);
@@ -1943,9 +1956,14 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   CUtensorMap maps[3];
   if (step) {
     if ((st = tensor_map(kMapCodes, qweight, p, &maps[0])) != MNB_OK ||
-        (st = tensor_map(kMapScales, scales, p, &maps[1])) != MNB_OK ||
-        (st = tensor_map(kMapZeros, zp, p, &maps[2])) != MNB_OK)
+        (st = tensor_map(kMapScales, scales, p, &maps[1])) != MNB_OK)
       return st;
+    if (zp) {
+      if ((st = tensor_map(kMapZeros, zp, p, &maps[2])) != MNB_OK) return st;
+    } else {
+      maps[2] = maps[1];                          // never copied from (no zero-points)
+      p.tx_bytes -= kMmaRows * p.tr * p.zp_zb * 16;
+    }
   }
   const void* fn = step ? reinterpret_cast<const void*>(pick_step_kernel(M, math))
                         : reinterpret_cast<const void*>(pick_kernel(M, ks));

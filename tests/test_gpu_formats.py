@@ -38,7 +38,14 @@ def test_small_shapes(block, symmetric, M, N, K):
     inp = make_inputs(M, N, K, seed=M * 7 + N + K + block, block=block)
     c0 = mnb.counters()
     _run_both(inp, symmetric)
-    assert mnb.counters()[15] - c0[15] == 2
+    c1 = mnb.counters()
+    if block == 32:
+        # symmetric block 32: the step kernel where it applies (K a multiple
+        # of 1024, no K split), else the general kernel
+        step = K % 1024 == 0
+        assert c1[13] - c0[13] == (2 if step else 0) and c1[15] - c0[15] == (0 if step else 2)
+    else:
+        assert c1[15] - c0[15] == 2
 
 
 @pytest.mark.parametrize("block,symmetric", FORMATS, ids=FORMAT_IDS)
@@ -114,6 +121,42 @@ def test_weights_ready_chain_matches_plain_calls():
     for a, c in zip(ref[1:], got[1:]):
         assert torch.equal(a.view(torch.int16), c.view(torch.int16))
         assert torch.isfinite(a.float()).all()
+
+
+@pytest.mark.parametrize("tc", [False, True], ids=["default", "tensor_cores"])
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (1, 27648, 5120), (2, 300, 8192), (4, 1000, 2048),
+                                   (8, 8192, 8192), (1, 1, 1024), (3, 129, 3072)])
+def test_symmetric_block32_on_the_step_kernel(M, N, K, tc):
+    """Block 32 without zero-points runs the TMA step kernel (constant
+    zero-points of 8 in its stages instead of copied ones): parity, the bf16
+    invariant, and the kernel that ran."""
+    if tc and (K % 1024 or M * K > 33792):
+        pytest.skip("outside the tensor-core math's shapes")
+    inp = make_inputs(M, N, K, seed=M + N + K, block=32)
+    dev = _gpu.to_device(inp, symmetric=True)
+    c0 = mnb.counters()
+    y16 = _gpu.bits(_gpu.run(dev, "f16", 0, tensor_cores=tc))
+    ybf = _gpu.bits(_gpu.run(dev, "bf16", 0, tensor_cores=tc))
+    c1 = mnb.counters()
+    assert c1[13] - c0[13] == 2 and c1[15] == c0[15]
+    assert c1[12] - c0[12] == (2 if tc else 0)
+    cols = None if N <= 1000 else np.random.default_rng(N).choice(N, size=384, replace=False)
+    _gpu.compare(inp, y16, ybf, cols=cols, symmetric=True)
+
+
+def test_symmetric_and_asymmetric_step_launches_interleave():
+    """Symmetric and asymmetric block-32 step launches back to back (with early
+    weight streaming) give the bits of plain calls: a launch's constant
+    zero-points never leak into the next launch's stages."""
+    M, N, K = 1, 4096, 4096
+    devs = [_gpu.to_device(make_inputs(M, N, K, seed=90 + i), symmetric=bool(i % 2)) for i in range(4)]
+    x = devs[0][0]
+    ref = [_gpu.bits(mnb.gemv(x, q, s, z, "f16")) for (_, q, s, z) in devs]
+    torch.cuda.synchronize()
+    got = [mnb.gemv(x, q, s, z, "f16", weights_ready=True) for (_, q, s, z) in devs * 3]
+    torch.cuda.synchronize()
+    for i, g in enumerate(got):
+        assert np.array_equal(_gpu.bits(g), ref[i % 4])
 
 
 def test_block32_with_zero_points_keeps_its_kernels():

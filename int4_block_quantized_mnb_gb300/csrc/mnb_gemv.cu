@@ -929,15 +929,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (p.zp == nullptr) {
-    // symmetric format: no zero-point copies; every stage's zero-point bytes
-    // hold 0x88 (zero-point 8 in both nibbles) for the whole launch
-    for (int s = 0; s < p.stages; ++s)
-      for (int i = threadIdx.x; i < p.zp_bytes / 16; i += blockDim.x)
-        *reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes + p.zp_offset +
-                                  16 * i) = make_uint4(0x88888888u, 0x88888888u, 0x88888888u,
-                                                       0x88888888u);
-  }
   __syncthreads();
   allow_dependents();
 
@@ -991,6 +982,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           v.w = __ldg(src + 6) | (static_cast<uint32_t>(__ldg(src + 7)) << 16);
           *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + x_off(rem)) = pair_k4(v);
         }
+    }
+    if (p.zp == nullptr) {
+      // symmetric format: the producer copies no zero-points; every stage's
+      // zero-point bytes hold 0x88 (zero-point 8 in both nibbles) for the
+      // whole launch, written here before any consumer reads a stage
+      for (int s = 0; s < p.stages; ++s)
+        for (int i = threadIdx.x; i < p.zp_bytes / 16; i += W * 32)
+          *reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes + p.zp_offset +
+                                    16 * i) = make_uint4(0x88888888u, 0x88888888u, 0x88888888u,
+                                                         0x88888888u);
     }
     // all consumer warps (named barrier 1; producer and epilogue do not take part)
     asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");

@@ -94,15 +94,6 @@ __device__ __forceinline__ uint32_t sw128(int r, int j) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
 }
 
-// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled tile:
-// start address >> 4 (bits 0-13), leading offset 1 (unused for this layout,
-// bits 16-29), stride between 8-row groups 1024 >> 4 (bits 32-45), descriptor
-// version 1 (bits 46-47), swizzle mode 2 = 128 bytes (bits 61-63).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) |
-         (1ull << 46) | (2ull << 61);
-}
-
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), fp16 A
 // and B (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits
 // 17-22, M >> 4 at bits 24-28.
@@ -110,12 +101,26 @@ constexpr uint32_t tc_idesc(int kTok) {
   return (1u << 4) | (static_cast<uint32_t>(kTok >> 3) << 17) | ((kTcRows >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled tile:
+// start address >> 4 (bits 0-13), leading offset 1 (unused for this layout,
+// bits 16-29), stride between 8-row groups 1024 >> 4 (bits 32-45), descriptor
+// version 1 (bits 46-47), swizzle mode 2 = 128 bytes (bits 61-63).  Its high
+// word is a constant; its low word advances by 2 for a tile 32 bytes further
+// along K (addresses stay below 256 KB: no carry out of the 14-bit field).
+constexpr uint32_t kDescHi = 64u | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr) {
+  return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
+}
+
+// One MMA from the descriptors' low words (the single issuing thread builds
+// no 64-bit values).
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint32_t adesc_lo, uint32_t bdesc_lo,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %4, 0;\n"
+      " mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(adesc_lo), "r"(bdesc_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
       : "memory");
 }
 
@@ -458,14 +463,14 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t a_hi = smem_addr(smem + rs * kWBuf), a_lo = a_hi + kTcTile;
-      const uint32_t bx = smem_addr(xstages + xs * kXBytes);
+      const uint32_t d_hi = sw128_desc_lo(smem_addr(smem + rs * kWBuf));
+      const uint32_t d_lo = d_hi + (kTcTile >> 4);
+      const uint32_t d_x = sw128_desc_lo(smem_addr(xstages + xs * kXBytes));
 #pragma unroll
-      for (int ks = 0; ks < kTcK / 16; ++ks) {       // K = 16 slices: 32 bytes apart
+      for (int ks = 0; ks < kTcK / 16; ++ks) {       // K = 16 slices: 32 bytes (2 units) apart
         const uint32_t acc = (st > 0 || ks > 0) ? 1u : 0u;
-        tc_mma(tmem, sw128_desc(a_hi + 32 * ks), sw128_desc(bx + 32 * ks), tc_idesc(kTok), acc);
-        tc_mma(tmem + kTcTok, sw128_desc(a_lo + 32 * ks), sw128_desc(bx + 32 * ks),
-               tc_idesc(kTok), acc);
+        tc_mma(tmem, d_hi + 2 * ks, d_x + 2 * ks, tc_idesc(kTok), acc);
+        tc_mma(tmem + kTcTok, d_lo + 2 * ks, d_x + 2 * ks, tc_idesc(kTok), acc);
       }
       tc_commit(empty0 + 8 * rs);
       tc_commit(xempty0 + 8 * xs);

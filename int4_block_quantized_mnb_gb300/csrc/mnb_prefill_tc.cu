@@ -17,10 +17,10 @@
 //                loaded two steps ahead), regrouping the dequant's exact
 //                (k, k + 4) pairs into natural k order; each warp then
 //                arrives on the stage's "full" mbarrier;
-//   activations  one more warp copies each step's tile with a tiled tensor
+//   activations  a copy warp issues each step's tile as a tiled tensor
 //                copy (zero fill past K and M) onto the stage's "xfull"
 //                barrier, a few steps ahead.
-// That warp waits on both, issues the step's eight MMAs (hi and lo, four
+// An MMA warp waits on both, issues the step's eight MMAs (hi and lo, four
 // K = 16 slices each) and commits them to the stages' "empty" and "xempty"
 // barriers, which gate their refills.  The epilogue reads TMEM (warp w:
 // lanes 32 (w mod 4) .. + 31, a quarter of the columns by w / 4), forms
@@ -63,7 +63,7 @@ constexpr int tc_xbuf(int kTok) { return kTok * kTcK * 2; }             // one a
 constexpr int tc_wring(int kTok) { return kTok == 256 ? 2 : 3; }
 constexpr int tc_xring(int kTok) { return kTok == 256 ? 4 : 6; }
 constexpr int kAhead = 2;                    // steps of codes in flight per dequant thread
-constexpr int kDequantThreads = 512;         // dequant and epilogue threads; one more warp issues MMAs
+constexpr int kDequantThreads = 512;         // dequant and epilogue threads; two more warps issue MMAs and copies
 constexpr int tc_ring_bytes(int kTok) { return tc_wring(kTok) * kWBuf + tc_xring(kTok) * tc_xbuf(kTok); }
 constexpr int tc_smem(int kTok) { return tc_ring_bytes(kTok) + 1024 + 256; }   // + alignment, barriers
 constexpr int tc_cols(int kTok) { return 2 * kTok; }
@@ -253,7 +253,7 @@ __device__ __forceinline__ void pf_out(void* y, size_t idx, float v, int out_bf1
 // kThreads dequant threads (plus one MMA warp): a thread handles one weight
 // row x kKPer k per step.
 template <int kThreads, int kTok>
-__global__ void __launch_bounds__(kThreads + 32, 1)
+__global__ void __launch_bounds__(kThreads + 64, 1)
     gemm_prefill_tc(const TcParams p, const __grid_constant__ CUtensorMap tm_x) {
   constexpr int kTcTok = kTok;
   constexpr int kWR = tc_wring(kTok), kXR = tc_xring(kTok);
@@ -277,7 +277,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   const int m0 = blockIdx.y * kTcTok;
   const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8 * kWR, xfull0 = empty0 + 8 * kWR,
                  xempty0 = xfull0 + 8 * kXR, done = xempty0 + 8 * kXR;
-  const bool is_mma = warp == kThreads / 32;                // the extra warp issues the MMAs
+  const bool is_mma = warp == kThreads / 32;                // this extra warp issues the MMAs
+  const bool is_copy = warp == kThreads / 32 + 1;           // this one the activation copies
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (is_mma && lane == 0)
+  if (is_copy && lane == 0)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   // step's MMAs and commits them to empty and xempty, and after the last step
   // to done.  Every wait is bounded; a wait that gives up raises the abort
   // flag and the others then give up too.
-  if (!is_mma) {
+  if (warp < kThreads / 32) {
     StepIn fifo[kAhead];                             // steps st .. st + kAhead - 1
 #pragma unroll
     for (int i = 0; i < kAhead; ++i)
@@ -439,26 +440,34 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     }
     // the MMAs of the last stage have completed when done arrives
     if (!*abort_flag && !tc_wait(done, 0, p.err)) *abort_flag = 1;
-  } else if (lane == 0) {
+  } else if (is_copy && lane == 0) {
     // activation tile of step st (k0 = 64 (st_begin + st), rows m0 ..) into
     // stage st % XR: 128-byte rows, 128-byte swizzle (the MMA's layout);
-    // rows past M and k past K arrive as zeros
-    auto copy_x = [&](int st) {
-      const int xs = st % kXR;
-      tc_expect_tx(xfull0 + 8 * xs, kXBytes);
-      tc_tma_2d(smem_addr(xstages + xs * kXBytes), &tm_x, (st_begin + st) * kTcK, m0,
-                xfull0 + 8 * xs);
-    };
-    int issued = 0, consumed = 0;
-    for (; issued < kXR && issued < nsteps; ++issued) copy_x(issued);
+    // rows past M and k past K arrive as zeros.  A stage is refilled once
+    // the MMAs of its previous use have committed (xempty).
+    int issued = 0;
     for (int st = 0; st < nsteps; ++st) {
-      const int rs = st % kWR, xs = st % kXR;
-      if (!tc_wait(xfull0 + 8 * xs, (st / kXR) & 1, p.err)) {
+      const int xs = st % kXR;
+      if (st >= kXR && !tc_wait(xempty0 + 8 * xs, ((st / kXR) - 1) & 1, p.err)) {
         *abort_flag = 1;
         break;
       }
-      consumed = st + 1;
-      if (!tc_wait(full0 + 8 * rs, (st / kWR) & 1, p.err) || *abort_flag) {
+      if (*abort_flag) break;
+      tc_expect_tx(xfull0 + 8 * xs, kXBytes);
+      tc_tma_2d(smem_addr(xstages + xs * kXBytes), &tm_x, (st_begin + st) * kTcK, m0,
+                xfull0 + 8 * xs);
+      issued = st + 1;
+    }
+    // copies still in flight land before the CTA's shared memory is released
+    // (a phase the MMA thread already consumed completes the wait at once)
+    if (*abort_flag)
+      for (int st = max(0, issued - kXR); st < issued; ++st)
+        if (!tc_wait(xfull0 + 8 * (st % kXR), (st / kXR) & 1, p.err)) break;
+  } else if (is_mma && lane == 0) {
+    for (int st = 0; st < nsteps; ++st) {
+      const int rs = st % kWR, xs = st % kXR;
+      if (!tc_wait(xfull0 + 8 * xs, (st / kXR) & 1, p.err) ||
+          !tc_wait(full0 + 8 * rs, (st / kWR) & 1, p.err) || *abort_flag) {
         *abort_flag = 1;
         break;
       }
@@ -474,24 +483,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
       }
       tc_commit(empty0 + 8 * rs);
       tc_commit(xempty0 + 8 * xs);
-      // refill the activation stage of step st - 1 once its MMAs (queued
-      // ahead of these) have completed
-      if (st >= 1 && issued < nsteps) {
-        const int ps = (st - 1) % kXR;
-        if (!tc_wait(xempty0 + 8 * ps, ((st - 1) / kXR) & 1, p.err)) {
-          *abort_flag = 1;
-          break;
-        }
-        copy_x(issued++);
-      }
     }
-    if (!*abort_flag) {
-      tc_commit(done);
-    } else {
-      // copies still in flight land before the CTA's shared memory is released
-      for (int st = consumed; st < issued; ++st)
-        if (!tc_wait(xfull0 + 8 * (st % kXR), (st / kXR) & 1, p.err)) break;
-    }
+    if (!*abort_flag) tc_commit(done);
   }
   __syncthreads();
   ok = *abort_flag == 0;
@@ -505,7 +498,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   // CTA's shared memory (the stage buffers are free) instead of to y: a
   // warp's lanes store consecutive words
   float* part = reinterpret_cast<float*>(smem);
-  if (ok && !is_mma) {
+  if (ok && warp < kThreads / 32) {
 #pragma unroll 1
     for (int cc = 0; cc < kColsPerWarp / 32; ++cc) {
       const int col = col0 + 32 * cc;
@@ -537,7 +530,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     const int share = kTcRows * kTcTok / p.ksplit;
     const uint32_t part_addr = smem_addr(part);
     if (ok) {
-      for (int e = tid; e < share; e += kThreads + 32) {
+      for (int e = tid; e < share; e += kThreads + 64) {
         const int gidx = static_cast<int>(rank) * share + e;
         const int tok = gidx / kTcRows, row = gidx - tok * kTcRows;   // y row, column
         const uint32_t local = part_addr + 4u * static_cast<uint32_t>(gidx);
@@ -629,7 +622,7 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
                      static_cast<unsigned>(p.ksplit));
-  cfg.blockDim = dim3(kDequantThreads + 32);
+  cfg.blockDim = dim3(kDequantThreads + 64);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

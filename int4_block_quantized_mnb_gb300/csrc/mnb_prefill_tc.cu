@@ -489,8 +489,10 @@ __global__ void __launch_bounds__(kThreads + 64, 1)
   __syncthreads();
   ok = *abort_flag == 0;
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  // warp w: TMEM lanes 32 (w mod 4) .., a 1/(warps/4) share of the columns
-  constexpr int kColsPerWarp = kTcTok / (kThreads / 128);
+  // warp w < kEpiWarps: TMEM lanes 32 (w mod 4) .., a 1/(kEpiWarps/4) share
+  // of the columns (at least 32 a warp)
+  constexpr int kEpiWarps = kTcTok >= 128 ? kThreads / 32 : 4 * (kTcTok / 32);
+  constexpr int kColsPerWarp = kTcTok / (kEpiWarps / 4);
   const int lane_base = 32 * (warp & 3);
   const int col0 = kColsPerWarp * (warp >> 2);
   const int n = n0 + lane_base + lane;
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(kThreads + 64, 1)
   // CTA's shared memory (the stage buffers are free) instead of to y: a
   // warp's lanes store consecutive words
   float* part = reinterpret_cast<float*>(smem);
-  if (ok && warp < kThreads / 32) {
+  if (ok && warp < kEpiWarps) {
 #pragma unroll 1
     for (int cc = 0; cc < kColsPerWarp / 32; ++cc) {
       const int col = col0 + 32 * cc;
@@ -603,9 +605,11 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
   // Activation tiles of 256 rows (all of TMEM) for M > 128: a CTA's dequant
   // work per step does not depend on the tile width, so the wider tile does
   // twice the products per dequantized weight (small grids split K below).
+  // Smaller M takes the narrowest tile of 32, 64 or 128 rows that holds it:
+  // the MMA thread's issue waits for the tensor pipe, whose work per step
+  // grows with the tile width.
   const long long gx = (static_cast<long long>(N) + kTcRows - 1) / kTcRows;
-  const bool t256 = M > 128;
-  const int tok = t256 ? 256 : 128;
+  const int tok = M > 128 ? 256 : M > 64 ? 128 : M > 32 ? 64 : 32;
   const long long gy = (static_cast<long long>(M) + tok - 1) / tok;
   if (gx > 0x7FFFFFFFLL || gy > 65535) return fail(MNB_ERR_SHAPE, "prefill shape too large");
   // one CTA per SM (the ring fills most of its shared memory): a grid of at
@@ -614,8 +618,11 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
   const int nsteps = (K + kTcK - 1) / kTcK;
   p.ksplit = 1;
   while (p.ksplit < 8 && gx * gy * p.ksplit * 2 <= sms && nsteps >= 4 * p.ksplit) p.ksplit *= 2;
-  const void* fn = t256 ? reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 256>)
-                        : reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 128>);
+  const void* fn =
+      tok == 256 ? reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 256>)
+      : tok == 128 ? reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 128>)
+      : tok == 64 ? reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 64>)
+                  : reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 32>);
   const int smem = tc_smem(tok);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill tc)");

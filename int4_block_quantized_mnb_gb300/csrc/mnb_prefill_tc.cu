@@ -612,12 +612,29 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
   const int tok = M > 128 ? 256 : M > 64 ? 128 : M > 32 ? 64 : 32;
   const long long gy = (static_cast<long long>(M) + tok - 1) / tok;
   if (gx > 0x7FFFFFFFLL || gy > 65535) return fail(MNB_ERR_SHAPE, "prefill shape too large");
-  // one CTA per SM (the ring fills most of its shared memory): a grid of at
-  // most half the SM count splits K over a cluster of up to 8 CTAs, doubling
-  // while the grid still fits the SMs (each CTA keeps at least two steps)
+  // One CTA per SM (the ring fills most of its shared memory), so a launch
+  // takes ceil(CTAs / SMs) waves of one CTA's steps; K may be split over a
+  // cluster of up to 8 CTAs (each keeping at least two steps).  256-row
+  // tiles (128 KB fp32 partials) split only a grid of at most half the SM
+  // count, doubling while it still fits the SMs.  Narrower tiles take the
+  // split with the least waves x (steps per CTA + about three steps of
+  // start and epilogue + two for the reduction of their, at most 64 KB,
+  // partials).
   const int nsteps = (K + kTcK - 1) / kTcK;
   p.ksplit = 1;
-  while (p.ksplit < 8 && gx * gy * p.ksplit * 2 <= sms && nsteps >= 4 * p.ksplit) p.ksplit *= 2;
+  if (tok == 256) {
+    while (p.ksplit < 8 && gx * gy * p.ksplit * 2 <= sms && nsteps >= 4 * p.ksplit) p.ksplit *= 2;
+  } else {
+    long long best = ((gx * gy + sms - 1) / sms) * (nsteps + 3);
+    for (int ks = 2; ks <= 8 && nsteps >= 4 * ks; ks *= 2) {
+      const long long cost =
+          ((gx * gy * ks + sms - 1) / sms) * ((nsteps + ks - 1) / ks + 3 + 2);
+      if (cost < best) {
+        best = cost;
+        p.ksplit = ks;
+      }
+    }
+  }
   const void* fn =
       tok == 256 ? reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 256>)
       : tok == 128 ? reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 128>)

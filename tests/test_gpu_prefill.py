@@ -73,6 +73,7 @@ def test_tensor_core_small_shapes(block, symmetric, M, N, K):
 @pytest.mark.parametrize("M,N,K,block,symmetric", [
     (512, 4096, 4096, 32, False), (300, 27648, 5120, 64, True), (1000, 1024, 8192, 128, False),
     (300, 19456, 256, 32, False), (2100, 19456, 512, 64, True),
+    (16, 27648, 5120, 32, False), (100, 27648, 5120, 64, True),
 ])
 def test_tensor_core_full_size(M, N, K, block, symmetric):
     """Prefill-sized layers on the tcgen05 form (128- and 256-row activation

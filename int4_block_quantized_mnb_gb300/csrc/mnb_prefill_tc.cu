@@ -9,8 +9,8 @@
 // fp32 sums: y = D_hi + 2^-11 D_lo.  No per-block scaling is needed, so both
 // accumulators stay in TMEM across the whole K loop.
 //
-// Tile.  A CTA computes 128 weight rows x 128 or 256 activation rows (UMMA
-// M = 128, N = 128 or 256) in K steps of 64, through two rings of stage
+// Tile.  A CTA computes 128 weight rows x 32, 64, 128 or 256 activation rows
+// (UMMA M = 128, N = the same) in K steps of 64, through two rings of stage
 // buffers in the 128-byte swizzled K-major layout the tensor core reads:
 //   weights      512 dequant threads write each step's hi and lo tiles
 //                (thread = one row x 16 k: its codes, scale and zero-point,
@@ -23,10 +23,11 @@
 // An MMA warp waits on both, issues the step's eight MMAs (hi and lo, four
 // K = 16 slices each) and commits them to the stages' "empty" and "xempty"
 // barriers, which gate their refills.  The epilogue reads TMEM (warp w:
-// lanes 32 (w mod 4) .. + 31, a quarter of the columns by w / 4), forms
-// D_hi + 2^-11 D_lo, rounds once to fp16 and, on the bf16 arm, narrows.  A
-// grid of at most half the SM count splits K over a cluster of up to 8 CTAs;
-// their fp32 tiles are summed in rank order through distributed shared memory.
+// lanes 32 (w mod 4) .. + 31, 32 or 64 columns by w / 4), forms
+// D_hi + 2^-11 D_lo (D_hi alone where it is not finite), rounds once to fp16
+// and, on the bf16 arm, narrows.  K may be split over a cluster of up to 8
+// CTAs (the launcher weighs waves of CTAs against the reduction); their fp32
+// tiles are summed in rank order through distributed shared memory.
 #include "mnb.h"
 #include "mnb_dequant.cuh"
 #include "mnb_narrow.cuh"
@@ -250,8 +251,8 @@ __device__ __forceinline__ void pf_out(void* y, size_t idx, float v, int out_bf1
     static_cast<__half*>(y)[idx] = h;
 }
 
-// kThreads dequant threads (plus one MMA warp): a thread handles one weight
-// row x kKPer k per step.
+// kThreads dequant (and epilogue) threads plus an MMA warp and a copy warp; a
+// dequant thread handles one weight row x kKPer k per step.
 template <int kThreads, int kTok>
 __global__ void __launch_bounds__(kThreads + 64, 1)
     gemm_prefill_tc(const TcParams p, const __grid_constant__ CUtensorMap tm_x) {

@@ -48,3 +48,29 @@ def test_oracle_sample_accounts_whole_passes():
     inp = make_inputs(w.M, w.N, w.K, seed=0)
     gbs, desc, dt = bench.oracle_sample(w, inp, 0.2, 2)
     assert gbs > 0 and dt > 0 and "passes over all 256 output columns" in desc
+
+
+def test_prefill_workload_names_and_rows():
+    base = WORKLOADS["attn-proj-m1-k4096-n4096"]
+    w = bench.FormatWorkload(base, 32, False, 512)
+    assert (w.M, w.N, w.K) == (512, 4096, 4096) and w.name == "prefill-m512-k4096-n4096"
+    w = bench.FormatWorkload(base, 64, True, 0)
+    assert w.M == 1 and w.name == "attn-proj-m1-k4096-n4096-b64-sym"
+
+
+def test_tensor_roofline_counts_two_m_n_k(tmp_path, monkeypatch):
+    w = bench.FormatWorkload(WORKLOADS["attn-proj-m1-k4096-n4096"], 32, False, 2048)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))                 # no peaks file here
+    r = bench.tensor_roofline(w, 100e-6, 150.0, 6000.0)
+    flops = 2.0 * 2048 * 4096 * 4096
+    assert r["bound"] == "tensor" and r["flops_per_launch"] == flops
+    assert abs(r["achieved"] - flops / 100e-6 / 1e12) < 1e-9
+    assert r["peak"] == bench.FALLBACK_BF16_TFLOPS and r["peak_kind"].startswith("fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"bf16_tflops": 2000.0}')
+    assert bench.measured_tensor_peak() == (2000.0, "measured")
+
+
+def test_prefill_options_parse(monkeypatch):
+    monkeypatch.setattr("sys.argv", ["bench.py", "--m", "512", "--prefill-mma-sync", "--block", "64"])
+    a = bench.parse()
+    assert a.m == 512 and a.prefill_mma_sync and a.block == 64 and not a.tensor_cores

@@ -18,11 +18,11 @@
 //                (k, k + 4) pairs into natural k order; each warp then
 //                arrives on the stage's "full" mbarrier;
 //   activations  a copy warp issues each step's tile as a tiled tensor
-//                copy (zero fill past K and M) onto the stage's "xfull"
-//                barrier, a few steps ahead.
-// An MMA warp waits on both, issues the step's eight MMAs (hi and lo, four
-// K = 16 slices each) and commits them to the stages' "empty" and "xempty"
-// barriers, which gate their refills.  The epilogue reads TMEM (warp w:
+//                copy (zero fill past K and M) onto its own "xfull" barrier
+//                and, once it has landed, adds the last arrival on "full".
+// An MMA warp waits on "full", issues the step's eight MMAs (hi and lo, four
+// K = 16 slices each) and commits them to the step's "empty" barrier, which
+// gates both refills.  The epilogue reads TMEM (warp w:
 // lanes 32 (w mod 4) .. + 31, 32 or 64 columns by w / 4), forms
 // D_hi + 2^-11 D_lo (D_hi alone where it is not finite), rounds once to fp16
 // and, on the bf16 arm, narrows.  K may be split over a cluster of up to 8
@@ -53,16 +53,16 @@ namespace {
 constexpr int kTcRows = 128;                 // weight rows per CTA (UMMA M)
 constexpr int kTcK = 64;                     // k per step: one 128-byte swizzle row of fp16
 constexpr int kTcTile = 128 * 128;           // bytes of one 128 x 64 fp16 tile
-// Per activation-tile width kTok (UMMA N, 128 or 256): a weight stage holds
-// the hi and lo tiles of a step, an activation stage its kTok x 64 tile, in
-// two rings: the activation ring, filled by tensor copies, runs further
-// ahead (memory latency) than the weight ring, filled by the dequant threads
-// from codes they load kAhead steps ahead.  TMEM holds D_hi (columns
-// 0 .. kTok - 1) and D_lo (kTok .. 2 kTok - 1).
+// Per activation-tile width kTok (UMMA N: 32, 64, 128 or 256): a weight
+// stage holds the hi and lo tiles of a step, an activation stage its kTok x 64
+// tile; step st uses stage st % R of both (R = 3 or 4).  The dequant threads
+// fill the weight stages from codes they load kAhead steps ahead, a copy warp
+// the activation stages.  TMEM holds D_hi (columns 0 .. kTok - 1) and D_lo
+// (kTok .. 2 kTok - 1).
 constexpr int kWBuf = 2 * kTcTile;                                      // one weight stage
 constexpr int tc_xbuf(int kTok) { return kTok * kTcK * 2; }             // one activation stage
-constexpr int tc_wring(int kTok) { return kTok == 256 ? 2 : 3; }
-constexpr int tc_xring(int kTok) { return kTok == 256 ? 4 : 6; }
+constexpr int tc_wring(int kTok) { return kTok == 256 ? 3 : 4; }
+constexpr int tc_xring(int kTok) { return tc_wring(kTok); }   // one index for both rings
 constexpr int kAhead = 2;                    // steps of codes in flight per dequant thread
 constexpr int kDequantThreads = 512;         // dequant and epilogue threads; two more warps issue MMAs and copies
 constexpr int tc_ring_bytes(int kTok) { return tc_wring(kTok) * kWBuf + tc_xring(kTok) * tc_xbuf(kTok); }
@@ -265,8 +265,8 @@ __global__ void __launch_bounds__(kThreads + 64, 1)
   constexpr uint32_t kXBytes = tc_xbuf(kTok);               // one activation tile
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  // weight stages, activation stages, then full[WR] empty[WR] xfull[XR]
-  // xempty[XR] done, the TMEM address and the abort flag
+  // weight stages, activation stages, then full[R] empty[R] xfull[R] done,
+  // the TMEM address and the abort flag
   unsigned char* xstages = smem + kWR * kWBuf;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + tc_ring_bytes(kTok));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + tc_ring_bytes(kTok) + 224);
@@ -276,20 +276,19 @@ __global__ void __launch_bounds__(kThreads + 64, 1)
   const int lane = tid & 31;
   const int n0 = blockIdx.x * kTcRows;
   const int m0 = blockIdx.y * kTcTok;
+  static_assert(kWR == kXR, "the weight and activation stages of a step share an index");
   const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8 * kWR, xfull0 = empty0 + 8 * kWR,
-                 xempty0 = xfull0 + 8 * kXR, done = xempty0 + 8 * kXR;
+                 done = xfull0 + 8 * kXR;
   const bool is_mma = warp == kThreads / 32;                // this extra warp issues the MMAs
   const bool is_copy = warp == kThreads / 32 + 1;           // this one the activation copies
 
   if (tid == 0) {
     *abort_flag = 0;
     for (int r = 0; r < kWR; ++r) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * r), "r"(kThreads / 32) : "memory");
+      // full: every dequant warp, plus the copy thread once the activations landed
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full0 + 8 * r), "r"(kThreads / 32 + 1) : "memory");
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * r) : "memory");
-    }
-    for (int r = 0; r < kXR; ++r) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(xfull0 + 8 * r) : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(xempty0 + 8 * r) : "memory");
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(done) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -354,14 +353,13 @@ __global__ void __launch_bounds__(kThreads + 64, 1)
     }
   };
 
-  // Step st uses weight stage st % WR and activation stage st % XR.  Dequant
-  // warps write the weight stage's hi and lo tiles once the MMAs of its
-  // previous use have committed (empty), then arrive on full; the MMA thread
-  // copies the activation tile by TMA (xfull) once the MMAs of that stage's
-  // previous use have committed (xempty), waits on full and xfull, issues the
-  // step's MMAs and commits them to empty and xempty, and after the last step
-  // to done.  Every wait is bounded; a wait that gives up raises the abort
-  // flag and the others then give up too.
+  // Step st uses weight stage and activation stage st % R.  Once the MMAs of
+  // their previous use have committed (empty), dequant warps write the hi and
+  // lo tiles and arrive on full, and the copy thread issues the activation
+  // copy (xfull) and, when it has landed, adds the last arrival on full; the
+  // MMA thread waits on full, issues the step's MMAs and commits them to
+  // empty, and after the last step to done.  Every wait is bounded; a wait
+  // that gives up raises the abort flag and the others then give up too.
   if (warp < kThreads / 32) {
     StepIn fifo[kAhead];                             // steps st .. st + kAhead - 1
 #pragma unroll
@@ -443,13 +441,21 @@ __global__ void __launch_bounds__(kThreads + 64, 1)
     if (!*abort_flag && !tc_wait(done, 0, p.err)) *abort_flag = 1;
   } else if (is_copy && lane == 0) {
     // activation tile of step st (k0 = 64 (st_begin + st), rows m0 ..) into
-    // stage st % XR: 128-byte rows, 128-byte swizzle (the MMA's layout);
-    // rows past M and k past K arrive as zeros.  A stage is refilled once
-    // the MMAs of its previous use have committed (xempty).
-    int issued = 0;
+    // stage st % R: 128-byte rows, 128-byte swizzle (the MMA's layout); rows
+    // past M and k past K arrive as zeros.  A stage is refilled once the
+    // MMAs of its previous use have committed (empty); the copy completes on
+    // its own barrier (xfull), and once it has landed this thread adds the
+    // last arrival to the stage's full barrier, one step behind the issue.
+    auto landed = [&](int st) {                      // false: gave up (device error set)
+      return tc_wait(xfull0 + 8 * (st % kXR), (st / kXR) & 1, p.err);
+    };
+    auto release = [&](int st) {
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(full0 + 8 * (st % kWR)) : "memory");
+    };
+    int issued = 0, released = 0;
     for (int st = 0; st < nsteps; ++st) {
       const int xs = st % kXR;
-      if (st >= kXR && !tc_wait(xempty0 + 8 * xs, ((st / kXR) - 1) & 1, p.err)) {
+      if (st >= kXR && !tc_wait(empty0 + 8 * xs, ((st / kXR) - 1) & 1, p.err)) {
         *abort_flag = 1;
         break;
       }
@@ -458,17 +464,31 @@ __global__ void __launch_bounds__(kThreads + 64, 1)
       tc_tma_2d(smem_addr(xstages + xs * kXBytes), &tm_x, (st_begin + st) * kTcK, m0,
                 xfull0 + 8 * xs);
       issued = st + 1;
+      if (st >= 1) {
+        if (!landed(st - 1)) {
+          *abort_flag = 1;
+          break;
+        }
+        release(st - 1);
+        released = st;
+      }
     }
-    // copies still in flight land before the CTA's shared memory is released
-    // (a phase the MMA thread already consumed completes the wait at once)
+    if (!*abort_flag && issued == nsteps && released < nsteps) {
+      if (landed(nsteps - 1))
+        release(nsteps - 1);
+      else
+        *abort_flag = 1;
+      released = nsteps;
+    }
+    // on an abort, copies still in flight land before the CTA's shared memory
+    // is released
     if (*abort_flag)
-      for (int st = max(0, issued - kXR); st < issued; ++st)
-        if (!tc_wait(xfull0 + 8 * (st % kXR), (st / kXR) & 1, p.err)) break;
+      for (int st = released; st < issued; ++st)
+        if (!landed(st)) break;
   } else if (is_mma && lane == 0) {
     for (int st = 0; st < nsteps; ++st) {
       const int rs = st % kWR, xs = st % kXR;
-      if (!tc_wait(xfull0 + 8 * xs, (st / kXR) & 1, p.err) ||
-          !tc_wait(full0 + 8 * rs, (st / kWR) & 1, p.err) || *abort_flag) {
+      if (!tc_wait(full0 + 8 * rs, (st / kWR) & 1, p.err) || *abort_flag) {
         *abort_flag = 1;
         break;
       }
@@ -482,8 +502,7 @@ __global__ void __launch_bounds__(kThreads + 64, 1)
         tc_mma(tmem, d_hi + 2 * ks, d_x + 2 * ks, tc_idesc(kTok), acc);
         tc_mma(tmem + kTcTok, d_lo + 2 * ks, d_x + 2 * ks, tc_idesc(kTok), acc);
       }
-      tc_commit(empty0 + 8 * rs);
-      tc_commit(xempty0 + 8 * xs);
+      tc_commit(empty0 + 8 * rs);                    // frees both stages of the step
     }
     if (!*abort_flag) tc_commit(done);
   }

@@ -61,12 +61,15 @@ constexpr int kTcTile = 128 * 128;           // bytes of one 128 x 64 fp16 tile
 // (kTok .. 2 kTok - 1).
 constexpr int kWBuf = 2 * kTcTile;                                      // one weight stage
 constexpr int tc_xbuf(int kTok) { return kTok * kTcK * 2; }             // one activation stage
-constexpr int tc_wring(int kTok) { return kTok == 256 ? 3 : 4; }
-constexpr int tc_xring(int kTok) { return tc_wring(kTok); }   // one index for both rings
+// 512 dequant threads run one CTA per SM; 256 (32-row tiles) run two CTAs
+// per SM with two-stage rings
+constexpr int tc_wring(int kTok, int kThreads) { return kThreads == 256 ? 2 : kTok == 256 ? 3 : 4; }
+constexpr int tc_xring(int kTok, int kThreads) { return tc_wring(kTok, kThreads); }   // one index for both
 constexpr int kAhead = 2;                    // steps of codes in flight per dequant thread
-constexpr int kDequantThreads = 512;         // dequant and epilogue threads; two more warps issue MMAs and copies
-constexpr int tc_ring_bytes(int kTok) { return tc_wring(kTok) * kWBuf + tc_xring(kTok) * tc_xbuf(kTok); }
-constexpr int tc_smem(int kTok) { return tc_ring_bytes(kTok) + 1024 + 256; }   // + alignment, barriers
+constexpr int tc_ring_bytes(int kTok, int kThreads) {
+  return tc_wring(kTok, kThreads) * kWBuf + tc_xring(kTok, kThreads) * tc_xbuf(kTok);
+}
+constexpr int tc_smem(int kTok, int kThreads) { return tc_ring_bytes(kTok, kThreads) + 1024 + 256; }
 constexpr int tc_cols(int kTok) { return 2 * kTok; }
 constexpr unsigned kTcErrMma = 5;            // device error: a pipeline wait gave up
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
@@ -254,10 +257,10 @@ __device__ __forceinline__ void pf_out(void* y, size_t idx, float v, int out_bf1
 // kThreads dequant (and epilogue) threads plus an MMA warp and a copy warp; a
 // dequant thread handles one weight row x kKPer k per step.
 template <int kThreads, int kTok>
-__global__ void __launch_bounds__(kThreads + 64, 1)
+__global__ void __launch_bounds__(kThreads + 64, kThreads == 256 ? 2 : 1)
     gemm_prefill_tc(const TcParams p, const __grid_constant__ CUtensorMap tm_x) {
   constexpr int kTcTok = kTok;
-  constexpr int kWR = tc_wring(kTok), kXR = tc_xring(kTok);
+  constexpr int kWR = tc_wring(kTok, kThreads), kXR = tc_xring(kTok, kThreads);
   constexpr int kTcCols = tc_cols(kTok);
   constexpr int kKPer = kTcRows * kTcK / kThreads;           // k per thread and step
   constexpr int kWords = kKPer / 8;
@@ -268,9 +271,10 @@ __global__ void __launch_bounds__(kThreads + 64, 1)
   // weight stages, activation stages, then full[R] empty[R] xfull[R] done,
   // the TMEM address and the abort flag
   unsigned char* xstages = smem + kWR * kWBuf;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + tc_ring_bytes(kTok));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + tc_ring_bytes(kTok) + 224);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + tc_ring_bytes(kTok) + 240);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + tc_ring_bytes(kTok, kThreads));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + tc_ring_bytes(kTok, kThreads) + 224);
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(smem + tc_ring_bytes(kTok, kThreads) + 240);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -632,8 +636,12 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
   const int tok = M > 128 ? 256 : M > 64 ? 128 : M > 32 ? 64 : 32;
   const long long gy = (static_cast<long long>(M) + tok - 1) / tok;
   if (gx > 0x7FFFFFFFLL || gy > 65535) return fail(MNB_ERR_SHAPE, "prefill shape too large");
-  // One CTA per SM (the ring fills most of its shared memory), so a launch
-  // takes ceil(CTAs / SMs) waves of one CTA's steps; K may be split over a
+  // 32-row tiles: 256 dequant threads and two CTAs per SM (two independent
+  // pipelines; measured faster there, slower at 64 and 128 rows); wider
+  // tiles: 512 dequant threads and one CTA per SM
+  const int dq = tok == 32 ? 256 : 512;
+  const long long slots = static_cast<long long>(sms) * (dq == 256 ? 2 : 1);
+  // A launch takes ceil(CTAs / resident CTAs) waves of one CTA's steps; K may be split over a
   // cluster of up to 8 CTAs (each keeping at least two steps).  256-row
   // tiles (128 KB fp32 partials) split only a grid of at most half the SM
   // count, doubling while it still fits the SMs.  Narrower tiles take the
@@ -645,10 +653,10 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
   if (tok == 256) {
     while (p.ksplit < 8 && gx * gy * p.ksplit * 2 <= sms && nsteps >= 4 * p.ksplit) p.ksplit *= 2;
   } else {
-    long long best = ((gx * gy + sms - 1) / sms) * (nsteps + 3);
+    long long best = ((gx * gy + slots - 1) / slots) * (nsteps + 3);
     for (int ks = 2; ks <= 8 && nsteps >= 4 * ks; ks *= 2) {
       const long long cost =
-          ((gx * gy * ks + sms - 1) / sms) * ((nsteps + ks - 1) / ks + 3 + 2);
+          ((gx * gy * ks + slots - 1) / slots) * ((nsteps + ks - 1) / ks + 3 + 2);
       if (cost < best) {
         best = cost;
         p.ksplit = ks;
@@ -656,17 +664,17 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
     }
   }
   const void* fn =
-      tok == 256 ? reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 256>)
-      : tok == 128 ? reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 128>)
-      : tok == 64 ? reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 64>)
-                  : reinterpret_cast<const void*>(&gemm_prefill_tc<kDequantThreads, 32>);
-  const int smem = tc_smem(tok);
+      tok == 256 ? reinterpret_cast<const void*>(&gemm_prefill_tc<512, 256>)
+      : tok == 128 ? reinterpret_cast<const void*>(&gemm_prefill_tc<512, 128>)
+      : tok == 64 ? reinterpret_cast<const void*>(&gemm_prefill_tc<512, 64>)
+                  : reinterpret_cast<const void*>(&gemm_prefill_tc<256, 32>);
+  const int smem = tc_smem(tok, dq);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill tc)");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
                      static_cast<unsigned>(p.ksplit));
-  cfg.blockDim = dim3(kDequantThreads + 64);
+  cfg.blockDim = dim3(dq + 64);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

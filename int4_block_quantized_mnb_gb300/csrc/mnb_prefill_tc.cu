@@ -12,9 +12,10 @@
 // Tile.  A CTA computes 128 weight rows x 32, 64, 128 or 256 activation rows
 // (UMMA M = 128, N = the same) in K steps of 64, through two rings of stage
 // buffers in the 128-byte swizzled K-major layout the tensor core reads:
-//   weights      512 dequant threads write each step's hi and lo tiles
-//                (thread = one row x 16 k: its codes, scale and zero-point,
-//                loaded two steps ahead), regrouping the dequant's exact
+//   weights      512 dequant threads (256 at 32-row tiles, two CTAs an SM)
+//                write each step's hi and lo tiles (thread = one row x 16 or
+//                32 k: its codes, scale and zero-point, loaded two steps
+//                ahead), regrouping the dequant's exact
 //                (k, k + 4) pairs into natural k order; each warp then
 //                arrives on the stage's "full" mbarrier;
 //   activations  a copy warp issues each step's tile as a tiled tensor

@@ -2,8 +2,10 @@
 """Benchmark of the int4 block-quantized MatMulNBits decode GEMV on GB300.
 
 One step = one pass of the hot path over one input batch: the GEMV of the
-chosen workload once per output dtype the workload names (the 4096x4096
-attention projection runs an fp16-output and a bf16-output launch per step).
+chosen workload once per output dtype the workload names.  The default
+workload is the M=1 lm_head-sized projection (K=4096, N=151936, fp16 output),
+the largest single-GPU decode configuration; the 4096x4096 attention
+projection runs an fp16-output and a bf16-output launch per step.
 
   value      algorithmic HBM bytes of the step's GEMV calls / device time per
              step, with inputs resident in HBM.  Weight copies rotate over more
@@ -15,6 +17,11 @@ attention projection runs an fp16-output and a bf16-output launch per step).
              runs the GEMV(s) and copies y back.
   roofline   the GEMV kernel's achieved bandwidth against the measured HBM peak.
   cpu_baseline  the CPU oracle timed on a bounded sample on this host's cores.
+  configs    one sub-record per decode configuration (tiny 256x256, attention
+             projection in fp16 and bf16, fused gate_up, lm_head, small batch
+             M = 2, 4, 8): per-call time spread, GB/s, roofline fractions, the
+             kernel's registers and theoretical occupancy, committed DRAM
+             traffic.
 
 ``--impl reference`` times the CPU oracle alone (the reference arm).  With
 torchrun and N > 1 every rank runs an independent replica (the path has no
@@ -42,15 +49,15 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode GEMV µs/call and achieved HBM GB/s (% of GB300 peak) at M=1"
 UNIT = "GB/s"
-DEFAULT_WORKLOAD = "attn-proj-m1-k4096-n4096"
+DEFAULT_WORKLOAD = "lm-head-m1-k4096-n151936"
 FALLBACK_HBM_GBS = 6800.0
 
 
 def parse():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
-    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["mnb", "reference"], default="mnb")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--split-k", type=int, default=0,
@@ -71,6 +78,8 @@ def parse():
                     help="activation rows instead of the workload's (M > 8: the prefill GEMM)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration sub-records (configs 0-4)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU seconds for the oracle baseline sample")
     return ap.parse_args()
@@ -451,6 +460,154 @@ def run_ab_staged(args):
     return 0
 
 
+# The pages' own figures, quoted beside the GB300 numbers (other hardware:
+# context, not the target).
+PAGES_CONTEXT = {
+    "hardware": "A100-class GPU (the pages' \"GPU 6\")",
+    "gate_up_gemv": {"us_per_call": 26.69, "dram_tb_per_s": 2.267, "registers_per_thread": 64,
+                     "achieved_occupancy_pct": 41.17,
+                     "source": "PORT-1 (offline bias+interleave) -- measured NO-GO on the "
+                               "multicol asymmetric-zp GEMV (onnx-genai PR 1002), ncu table"},
+    "decode_64_tokens_bf16": {"cast_half_launches": [3024, 2398], "kernel_ms": [22.5, 21.3],
+                              "source": "perf(cuda): let the split-K decode GEMV store bf16 "
+                                        "directly (onnx-genai PR 1550), results"},
+}
+
+# The five decode configurations the GEMV is measured on; the attention
+# projection is timed once per output dtype.
+CONFIG_RECORDS = [
+    (0, "tiny-m1-k256-n256", "f16"),
+    (1, "attn-proj-m1-k4096-n4096", "f16"),
+    (1, "attn-proj-m1-k4096-n4096", "bf16"),
+    (2, "gate-up-m1-k5120-n27648", "bf16"),
+    (3, "lm-head-m1-k4096-n151936", "f16"),
+    (4, "small-batch-m2-k8192-n8192", "bf16"),
+    (4, "small-batch-m4-k8192-n8192", "bf16"),
+    (4, "small-batch-m8-k8192-n8192", "bf16"),
+]
+
+
+def to_device(a, dtype, dev):
+    import torch
+    return torch.from_numpy(a.view(np.int16).copy() if a.dtype == np.uint16 else a).view(
+        dtype).to(dev)
+
+
+class DeviceWorkload:
+    """One workload's inputs on the device: the activations, R copies of the
+    weights (R such that the copies together exceed 4x the L2 size, so a
+    launch that follows the rotation finds none of its weights in L2) and one
+    output buffer per output dtype."""
+
+    def __init__(self, w, inp, dev, l2_bytes, zero_points=True, multiple=1):
+        import torch
+        self.w, self.dev = w, dev
+        self.x = to_device(inp.x, torch.float16, dev)
+        q0 = to_device(inp.qweight, torch.uint8, dev)
+        s0 = to_device(inp.scales, torch.float16, dev)
+        z0 = to_device(inp.zp, torch.uint8, dev) if zero_points else None
+        self.wbytes = q0.numel() + 2 * s0.numel() + (0 if z0 is None else z0.numel())
+        self.R = math.ceil(max(1, math.ceil(4 * l2_bytes / self.wbytes)) / multiple) * multiple
+        self.copies = [(q0, s0, z0)] + [(q0.clone(), s0.clone(), None if z0 is None else z0.clone())
+                                        for _ in range(self.R - 1)]
+        self.ys = {o: torch.empty((w.M, w.N), dtype=torch.float16 if o == "f16" else torch.bfloat16,
+                                  device=dev) for o in w.out_dtypes}
+
+    def l2_note(self, l2_bytes):
+        return (f"inputs larger than L2: {self.R} rotating weight copies, "
+                f"{self.R * self.wbytes / 2**20:.0f} MiB vs L2 {l2_bytes / 2**20:.0f} MiB")
+
+
+def graph_steps(steps, rotation):
+    """Steps per captured graph for the K timed steps: a whole number of weight
+    rotations (`rotation` steps each) near K / 10, so about ten replays give
+    the per-call spread; never more than K."""
+    return min(steps, rotation * max(1, round(steps / 10 / rotation)))
+
+
+def graph_replays(launch, n_launches, replays, warm, stream, dev):
+    """Captures `n_launches` calls launch(i) in one CUDA graph, replays it
+    `warm` times untimed, then `replays` times with a CUDA event recorded
+    between consecutive replays on the launching stream.  Returns the
+    per-replay times in ms."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_launches):
+                launch(i)
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(replays):
+            g.replay()
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(replays)]
+
+
+def traffic_entry(name, bytes_call, tc):
+    """The committed ncu DRAM bytes of one launch of `name`'s kernel, or why
+    there is none."""
+    key = name + ("+tensor-cores" if tc else "")
+    t = recorded_traffic(key)
+    if t is None:
+        return {"bytes": None, "why": "no committed ncu capture for the current kernel sources"}
+    return {"bytes": t, "ratio_to_algorithmic": t / bytes_call}
+
+
+def launch_record(mnb, w, out, tc, block=32, symmetric=False, pm=False):
+    info = mnb.launch_info(w.M, w.N, w.K, block=block, out_dtype=out, symmetric=symmetric,
+                           tensor_cores=tc, prefill_mma_sync=pm)
+    return info
+
+
+def config_record(mnb, cfg, name, out, dev, stream, l2, peak, props, clk_hint, tc):
+    """One configuration's sub-record: per-call time spread over 20 graph
+    replays of at least 40 launches each (weights rotating over > 4x L2),
+    bandwidth, roofline fractions, the kernel's registers and theoretical
+    occupancy, and its committed DRAM traffic."""
+    import torch
+    from int4_block_quantized_mnb_gb300.synth import WORKLOADS, make_inputs
+    w = WORKLOADS[name]
+    inp = make_inputs(w.M, w.N, w.K, seed=0)
+    d = DeviceWorkload(w, inp, dev, l2)
+    n = d.R * max(1, math.ceil(40 / d.R))
+
+    def launch(i):
+        q, s, z = d.copies[i % d.R]
+        mnb.gemv(d.x, q, s, z, out_dtype=out, y=d.ys[out], stream=stream, weights_ready=True,
+                 tensor_cores=tc)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            launch(i)
+    ms = graph_replays(launch, n, 20, 3, stream, dev)
+    per = sorted(m * 1e3 / n for m in ms)
+    p10, p50, p90 = (pct(per, q) for q in (10, 50, 90))
+    b = w.algorithmic_bytes()
+    gbs = b / (p50 * 1e-6) / 1e9
+    info = launch_record(mnb, w, out, tc)
+    rec = {"config": cfg, "workload": name, "M": w.M, "K": w.K, "N": w.N, "out": out,
+           "bytes_per_call": b, "us_per_call": p50, "us_p10_p50_p90": [p10, p50, p90],
+           "gbs": gbs, "frac_hbm": gbs / peak, "frac_datasheet": gbs / DATASHEET_HBM_GBS,
+           "fma_bound": None, "kernel": info["kernel"],
+           "registers_per_thread": info["registers_per_thread"],
+           "theoretical_occupancy": info["theoretical_occupancy"],
+           "grid": info["grid"], "threads": info["threads"], "dynamic_smem": info["dynamic_smem"],
+           "traffic": traffic_entry(name, b, tc),
+           "timing": f"median of 20 replays of a {n}-launch graph (3 untimed before); "
+                     + d.l2_note(l2)}
+    if w.M > 1:
+        fb = fma_bound(w, props, clk_hint)
+        rec["fma_bound"] = {"us": fb["us"], "frac": fb["us"] / p50, "rate_source": fb["rate_source"]}
+    del d
+    return rec
+
+
 def main():
     args = parse()
     if args.ab_staged:
@@ -459,7 +616,8 @@ def main():
     if args.workload not in WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {list(WORKLOADS)}")
     w = WORKLOADS[args.workload]
-    if args.block != 32 or args.symmetric or args.m:
+    formats = args.block != 32 or args.symmetric or args.m
+    if formats:
         w = FormatWorkload(w, args.block, args.symmetric, args.m)
     if args.impl == "reference":
         return run_reference(args, w)
@@ -484,24 +642,15 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     mnb.load()
 
-    def to_dev(a, dtype):
-        return torch.from_numpy(a.view(np.int16).copy() if a.dtype == np.uint16 else a).view(dtype).to(dev)
-
-    x = to_dev(inp.x, torch.float16)
-    q0 = to_dev(inp.qweight, torch.uint8)
-    s0 = to_dev(inp.scales, torch.float16)
-    z0 = None if w_zp(w, inp) is None else to_dev(inp.zp, torch.uint8)
-    outs = list(w.out_dtypes)
-    L = len(outs)
-    ys = {o: torch.empty((w.M, w.N), dtype=torch.float16 if o == "f16" else torch.bfloat16,
-                         device=dev) for o in outs}
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    wbytes = q0.numel() + 2 * s0.numel() + (0 if z0 is None else z0.numel())
-    R = max(L, math.ceil(4 * l2 / wbytes))
-    R = int(math.ceil(R / L) * L)
-    copies = [(q0, s0, z0)] + [(q0.clone(), s0.clone(), None if z0 is None else z0.clone())
-                               for _ in range(R - 1)]
+    outs = list(w.out_dtypes)
+    L = len(outs)
+    d = DeviceWorkload(w, inp, dev, l2, zero_points=w_zp(w, inp) is not None, multiple=L)
+    R = d.R
+    l2_note = d.l2_note(l2)
+    x, copies, ys = d.x, d.copies, d.ys
+    z0 = copies[0][2]
     split_k = args.split_k
     tc = bool(args.tensor_cores)
     pm = bool(args.prefill_mma_sync)
@@ -520,10 +669,11 @@ def main():
             step(j)
     torch.cuda.synchronize(dev)
 
-    # Graph of G steps, G * L a multiple of R so copies rotate without reuse.
-    base = R // L
-    G = min(base * max(1, 4000 // (base * L)), args.steps)
-    graphs = []
+    # The K timed steps: replays of a graph of G steps, G a whole number of
+    # weight rotations (R / L steps) and about K / 10, so the per-call spread
+    # comes from about ten replays; a shorter graph takes the remainder.
+    # Three untimed replays of each graph come first.
+    G = graph_steps(args.steps, R // L)
     full, rem = divmod(args.steps, G)
 
     def capture(nsteps):
@@ -538,7 +688,8 @@ def main():
     g_rem = capture(rem) if rem else None
     for g in (g_main, g_rem):
         if g is not None:
-            g.replay()       # uploads the graph; not timed
+            for _ in range(3):
+                g.replay()
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local_rank)
@@ -572,6 +723,7 @@ def main():
     value = bytes_call * launches * world / (t_ms / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
     achieved = bytes_call / per_launch_s / 1e9
+    info = launch_record(mnb, w, outs[0], tc, w_block(w), w_zp(w, inp) is None, pm)
 
     # End to end through the public API with pinned host buffers.
     e2e = None
@@ -581,6 +733,7 @@ def main():
         hs = torch.from_numpy(inp.scales.view(np.int16).copy()).view(torch.float16).pin_memory()
         hz = None if z0 is None else torch.from_numpy(inp.zp).pin_memory()
         hy = {o: torch.empty(ys[o].shape, dtype=ys[o].dtype).pin_memory() for o in outs}
+        q0, s0 = copies[0][0], copies[0][1]
         dq, ds, dx = torch.empty_like(q0), torch.empty_like(s0), torch.empty_like(x)
         dz = None if z0 is None else torch.empty_like(z0)
         h2d = hx.numel() * 2 + hq.numel() + hs.numel() * 2 + (0 if hz is None else hz.numel())
@@ -612,6 +765,18 @@ def main():
         te = e0.elapsed_time(e1) / 1e3
         e2e = {"value": bytes_call * L * E / te / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": E}
+        del dq, ds, dx, dz
+
+    # One sub-record per decode configuration (default format only).
+    records = None
+    if rank == 0 and not args.no_configs and not formats:
+        del d, copies, ys, g_main, g_rem
+        torch.cuda.empty_cache()
+        records = []
+        for cfg, name, out in CONFIG_RECORDS:
+            records.append(config_record(mnb, cfg, name, out, dev, stream, l2, peak, props, clk,
+                                         tc))
+            torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
@@ -630,23 +795,25 @@ def main():
                    "split_k": split_k if split_k else "auto", "tensor_cores": tc,
                    **({"prefill_form": "mma.sync" if pm else "tcgen05"} if w.M > 8 else {}),
                    "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "l2": f"inputs larger than L2: {R} rotating weight copies, "
-                         f"{R * wbytes / 2**20:.0f} MiB vs L2 {l2 / 2**20:.0f} MiB",
+                   "l2": l2_note,
                    "timing": f"CUDA events around {full} replays of a {G}-step graph"
                              + (f" + 1 replay of a {rem}-step graph" if rem else "")
-                             + "; warm-up: W eager steps, then one untimed replay per graph"},
+                             + "; warm-up: W eager steps, then three untimed replays per graph"},
         "roofline": ({"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                       "frac": achieved / peak, "peak_kind": peak_kind,
-                      "traffic": None if tc else recorded_traffic(w.name),
+                      "traffic": recorded_traffic(w.name + ("+tensor-cores" if tc else "")),
                       "algorithmic_bytes_per_launch": bytes_call,
                       "peak_datasheet": DATASHEET_HBM_GBS,
                       "frac_datasheet": achieved / DATASHEET_HBM_GBS,
                       "fma_bound": fma_bound(w, props, clk) if w.M > 1 else None}
                      if w.M <= 8 else tensor_roofline(w, per_launch_s, achieved, peak)),
+        "launch": info,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,
+        "context_pages_a100": PAGES_CONTEXT,
+        "configs": records,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

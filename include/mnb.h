@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define MNB_ABI_VERSION 1
+#define MNB_ABI_VERSION 2
 
 /* Output element type of mnb_gemv. */
 typedef enum mnb_out_dtype {
@@ -63,8 +63,8 @@ typedef enum mnb_status {
     MNB_ERR_DTYPE = 4,   /* out_dtype not an mnb_out_dtype */
     MNB_ERR_SPLITK = 5,  /* split_k outside [0, mnb_max_split_k] or too small for K */
     MNB_ERR_ALIGN = 6,   /* a pointer is misaligned for its element type (see mnb_gemv) */
-    MNB_ERR_ALIAS = 7,   /* y overlaps an input array */
-    MNB_ERR_CUDA = 8,    /* a CUDA runtime call failed; see mnb_last_error_detail */
+    MNB_ERR_CUDA = 7,    /* a CUDA runtime call failed; see mnb_last_cuda_error */
+    MNB_ERR_ALIAS = 8,   /* y overlaps an input array */
     MNB_ERR_DEVICE = 9,  /* the current device is not an sm_103 GPU */
     MNB_ERR_FLAGS = 10   /* unknown bits in the flags of mnb_gemv_flags */
 } mnb_status;
@@ -214,6 +214,10 @@ const char *mnb_status_string(int status);
  * none).  Valid until the thread's next call into the library. */
 const char *mnb_last_error_detail(void);
 
+/* The same thread-local text, under the name that says what it holds after
+ * MNB_ERR_CUDA: the failing CUDA call with its error name and message. */
+const char *mnb_last_cuda_error(void);
+
 /* Device-side error word of the current device: 0, or the first code a
  * kernel recorded when one of its bounded waits gave up (1 = stage data never
  * arrived, 2 = a stage was never released, 3 = copies still in flight at exit,
@@ -222,6 +226,35 @@ const char *mnb_last_error_detail(void);
  * `stream`, synchronises that stream and writes the word to *code; clears it
  * when `clear` is non-zero.  Returns MNB_ERR_CUDA if the read fails. */
 int mnb_device_error(void *stream, unsigned int *code, int clear);
+
+/*
+ * mnb_launch_info -- what one mnb_gemv_flags call with these arguments would
+ * launch on the current device, for measurement harnesses (registers,
+ * occupancy) and tests.  Filled by mnb_gemv_launch_info; nothing is launched.
+ */
+typedef struct mnb_launch_info {
+    char kernel[64];          /* name of the kernel family, e.g. "step kernel (CUDA-core, 4 rows/lane)" */
+    int counter;              /* mnb_debug_counters index that the launch bumps for its kernel
+                                 family (13 step, 15 general, 16 prefill), or -1 for the
+                                 row-tile kernel, which has none of its own */
+    int grid;                 /* CTAs in the grid */
+    int threads;              /* threads per CTA */
+    int cluster;              /* CTAs per thread-block cluster (1 = no cluster) */
+    int dynamic_smem;         /* dynamic shared memory per CTA, bytes */
+    int static_smem;          /* static shared memory per CTA, bytes */
+    int registers_per_thread; /* registers the compiled kernel uses per thread */
+    int ctas_per_sm;          /* resident CTAs per SM (occupancy calculator) */
+    int max_threads_per_sm;   /* the device's limit */
+    double theoretical_occupancy; /* ctas_per_sm * threads / max_threads_per_sm */
+} mnb_launch_info;
+
+/* The arguments, checks and statuses of mnb_gemv_flags (the pointers are only
+ * inspected for their alignment and overlap, never dereferenced); on MNB_OK
+ * *info describes the launch that call would make.  Needs an sm_103 device
+ * current (MNB_ERR_DEVICE otherwise). */
+int mnb_gemv_launch_info(const void *x, const uint8_t *qweight, const void *scales,
+                         const uint8_t *zp, const void *y, int M, int N, int K, int block,
+                         int out_dtype, int split_k, unsigned int flags, mnb_launch_info *info);
 
 /* Launch counters, for tests that must prove the GPU kernel ran:
  *   [0] launches, [1] fp16-output launches, [2] bf16-output launches,

@@ -11,10 +11,11 @@ from __future__ import annotations
 import ctypes
 
 from ._native import (BLOCK, FLAG_PREFILL_MMA_SYNC, FLAG_TENSOR_CORES, FLAG_WEIGHTS_READY, MAX_M,
-                      MAX_SPLIT_K, NUM_COUNTERS, OUT_BF16, OUT_F16, MnbError, check, load)
+                      MAX_SPLIT_K, NUM_COUNTERS, OUT_BF16, OUT_F16, LaunchInfo, MnbError, check,
+                      load)
 
-__all__ = ["gemv", "gemv_ptr", "cast_f16_to_bf16", "split_k_auto", "min_split_k", "max_split_k", "counters",
-           "reset_counters", "device_error", "MnbError", "OUT_F16", "OUT_BF16", "BLOCK",
+__all__ = ["gemv", "gemv_ptr", "launch_info", "cast_f16_to_bf16", "split_k_auto", "min_split_k",
+           "max_split_k", "counters", "reset_counters", "device_error", "MnbError", "OUT_F16", "OUT_BF16", "BLOCK",
            "MAX_M", "MAX_SPLIT_K", "FLAG_WEIGHTS_READY", "FLAG_TENSOR_CORES",
            "FLAG_PREFILL_MMA_SYNC"]
 
@@ -97,6 +98,32 @@ def gemv(x, qweight, scales, zp, out_dtype="f16", split_k: int = 0, y=None, stre
                  (FLAG_TENSOR_CORES if tensor_cores else 0) |
                  (FLAG_PREFILL_MMA_SYNC if prefill_mma_sync else 0))
     return y
+
+
+def launch_info(M: int, N: int, K: int, block: int = BLOCK, out_dtype="f16", split_k: int = 0,
+                symmetric: bool = False, tensor_cores: bool = False,
+                prefill_mma_sync: bool = False, x_aligned: bool = True) -> dict:
+    """What ``gemv`` would launch for this shape on the current device
+    (mnb_gemv_launch_info): kernel family, grid, threads, cluster, shared
+    memory, registers per thread, resident CTAs per SM and theoretical
+    occupancy.  The call only inspects pointers for alignment, so stand-in
+    addresses with torch's allocation alignment are passed; nothing runs."""
+    base = 1 << 40                     # 256-byte aligned stand-ins, far apart
+    span = 1 << 36
+    x = base + (0 if x_aligned else 2)
+    info = LaunchInfo()
+    flags = ((FLAG_TENSOR_CORES if tensor_cores else 0) |
+             (FLAG_PREFILL_MMA_SYNC if prefill_mma_sync else 0))
+    check(load().mnb_gemv_launch_info(x, base + span, base + 2 * span,
+                                      0 if symmetric else base + 3 * span, base + 4 * span,
+                                      M, N, K, int(block), _out_code(out_dtype), int(split_k),
+                                      flags, ctypes.byref(info)))
+    return {"kernel": info.kernel.decode(), "counter": info.counter, "grid": info.grid,
+            "threads": info.threads, "cluster": info.cluster,
+            "dynamic_smem": info.dynamic_smem, "static_smem": info.static_smem,
+            "registers_per_thread": info.registers_per_thread,
+            "ctas_per_sm": info.ctas_per_sm, "max_threads_per_sm": info.max_threads_per_sm,
+            "theoretical_occupancy": info.theoretical_occupancy}
 
 
 def cast_f16_to_bf16(src, dst=None, stream=None):

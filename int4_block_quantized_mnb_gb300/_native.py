@@ -14,8 +14,9 @@ LIBRARY = os.path.join(PKG, "libmnb.so")
 OUT_F16 = 0
 OUT_BF16 = 1
 STATUS = {0: "MNB_OK", 1: "MNB_ERR_NULL", 2: "MNB_ERR_SHAPE", 3: "MNB_ERR_BLOCK",
-          4: "MNB_ERR_DTYPE", 5: "MNB_ERR_SPLITK", 6: "MNB_ERR_ALIGN", 7: "MNB_ERR_ALIAS",
-          8: "MNB_ERR_CUDA", 9: "MNB_ERR_DEVICE", 10: "MNB_ERR_FLAGS"}
+          4: "MNB_ERR_DTYPE", 5: "MNB_ERR_SPLITK", 6: "MNB_ERR_ALIGN", 7: "MNB_ERR_CUDA",
+          8: "MNB_ERR_ALIAS", 9: "MNB_ERR_DEVICE", 10: "MNB_ERR_FLAGS"}
+ABI_VERSION = 2
 FLAG_WEIGHTS_READY = 1
 FLAG_TENSOR_CORES = 2
 FLAG_PREFILL_MMA_SYNC = 4
@@ -24,6 +25,16 @@ MAX_PREFILL_M = 4194240
 BLOCK = 32
 MAX_SPLIT_K = 8
 NUM_COUNTERS = 18
+
+
+class LaunchInfo(ctypes.Structure):
+    """struct mnb_launch_info."""
+    _fields_ = [("kernel", ctypes.c_char * 64), ("counter", ctypes.c_int), ("grid", ctypes.c_int),
+                ("threads", ctypes.c_int), ("cluster", ctypes.c_int),
+                ("dynamic_smem", ctypes.c_int), ("static_smem", ctypes.c_int),
+                ("registers_per_thread", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("max_threads_per_sm", ctypes.c_int), ("theoretical_occupancy", ctypes.c_double)]
+
 
 # Every symbol the header declares, with (restype, argtypes).
 _vp, _u8p, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)
@@ -39,6 +50,11 @@ SIGNATURES = {
     "mnb_max_split_k": (ctypes.c_int, [ctypes.c_int, _ip]),
     "mnb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "mnb_last_error_detail": (ctypes.c_char_p, []),
+    "mnb_last_cuda_error": (ctypes.c_char_p, []),
+    "mnb_gemv_launch_info": (ctypes.c_int, [_vp, _u8p, _vp, _u8p, _vp, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_uint,
+                                            ctypes.POINTER(LaunchInfo)]),
     "mnb_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint), ctypes.c_int]),
     "mnb_debug_counters": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int]),
     "mnb_debug_counters_reset": (None, []),
@@ -71,7 +87,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    if lib.mnb_abi_version() != 1:
+    if lib.mnb_abi_version() != ABI_VERSION:
         raise RuntimeError("libmnb.so ABI version mismatch")
     if path is None:
         _lib = lib

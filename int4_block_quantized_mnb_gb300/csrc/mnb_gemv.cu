@@ -41,6 +41,7 @@
 
 #include "mnb.h"
 #include "mnb_dequant.cuh"
+#include "mnb_launch.cuh"
 #include "mnb_narrow.cuh"
 
 #include <cuda_bf16.h>
@@ -484,8 +485,10 @@ __device__ __forceinline__ void run_epilogue(const Params& p, const float* red, 
 
 // ------------------------------------------------------------------ kernel --
 
+namespace {
+
 template <int M, int KPL, int RC>
-__global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p) {
+__global__ void __launch_bounds__(max_threads(M), 1) mnb_gemv_rowtile_kernel(const Params p) {
   constexpr int kWords = KPL / 8;                   // 32-bit code words per lane segment
   constexpr int kLaneBlocks = KPL >= 32 ? KPL / 32 : 1;   // 32-blocks a lane's segment touches
   constexpr int kBlockWords = KPL >= 32 ? 4 : kWords;     // words of the segment in one block
@@ -768,11 +771,13 @@ __global__ void __launch_bounds__(max_threads(M), 1) gemv_kernel(const Params p)
   }
 }
 
+}  // namespace
+
 
 // ------------------------------------------------------------- step kernel --
 //
 // Weight tiles stream in through TMA tensor copies; the multiply-accumulate
-// runs on CUDA cores by default (see gemv_step_kernel) or, on request, on the
+// runs on CUDA cores by default (see mnb_gemv_step_kernel) or, on request, on the
 // tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulation):
 //   A = 16 weight rows x 16 k: lane (g, t) holds code word t (k = 8t..8t+7 of
 //       the block) of rows g and g+8, dequantized exactly to q - zp by the same
@@ -885,9 +890,11 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
 // tensor-core (on request).
 enum StepMath : int { kMathFma = 0, kMathWide = 1, kMathMma = 2 };
 
+namespace {
+
 template <int M, int kMath>
 __global__ void __launch_bounds__(kMmaThreads, 1)
-    gemv_step_kernel(const Params p, const __grid_constant__ CUtensorMap tm_q,
+    mnb_gemv_step_kernel(const Params p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_sc,
                     const __grid_constant__ CUtensorMap tm_zp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1320,6 +1327,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   }
 }
 
+}  // namespace
+
 // ------------------------------------------------------------- host side --
 
 struct KernelShape {
@@ -1339,7 +1348,7 @@ using KernelFn = void (*)(const Params);
 
 template <int M>
 constexpr KernelFn kernel_for() {
-  return &gemv_kernel<M, shape_for(M).kpl, shape_for(M).rc>;
+  return &mnb_gemv_rowtile_kernel<M, shape_for(M).kpl, shape_for(M).rc>;
 }
 
 // Lane segment and rows per tile: the per-M default.  (The kernel template
@@ -1379,17 +1388,17 @@ std::atomic<unsigned long long> g_counters[MNB_NUM_COUNTERS];
 // mnb_prefill_tc.cu: the prefill GEMM on tcgen05 (the default form).
 int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                       void* y, int M, int N, int K, int block, int out_bf16, unsigned int* err,
-                      int sms, cudaStream_t stream);
+                      int sms, cudaStream_t stream, LaunchDesc* query);
 
 // mnb_prefill.cu: more than MNB_MAX_M activation rows.
 int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                    void* y, int M, int N, int K, int block, int out_bf16, int sms,
-                   cudaStream_t stream);
+                   cudaStream_t stream, LaunchDesc* query);
 
 // mnb_general.cu: block sizes other than 32 and the symmetric format.
 int launch_general(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                    void* y, int M, int N, int K, int block, int out_bf16, int split_k, int sms,
-                   cudaStream_t stream);
+                   cudaStream_t stream, LaunchDesc* query);
 
 struct DeviceInfo {
   bool ready = false;
@@ -1569,14 +1578,14 @@ using MmaFn = void (*)(const Params, const CUtensorMap, const CUtensorMap, const
 template <int kMath>
 MmaFn step_kernel_for(int M) {
   switch (M) {
-    case 1: return &gemv_step_kernel<1, kMath>;
-    case 2: return &gemv_step_kernel<2, kMath>;
-    case 3: return &gemv_step_kernel<3, kMath>;
-    case 4: return &gemv_step_kernel<4, kMath>;
-    case 5: return &gemv_step_kernel<5, kMath>;
-    case 6: return &gemv_step_kernel<6, kMath>;
-    case 7: return &gemv_step_kernel<7, kMath>;
-    default: return &gemv_step_kernel<8, kMath>;
+    case 1: return &mnb_gemv_step_kernel<1, kMath>;
+    case 2: return &mnb_gemv_step_kernel<2, kMath>;
+    case 3: return &mnb_gemv_step_kernel<3, kMath>;
+    case 4: return &mnb_gemv_step_kernel<4, kMath>;
+    case 5: return &mnb_gemv_step_kernel<5, kMath>;
+    case 6: return &mnb_gemv_step_kernel<6, kMath>;
+    case 7: return &mnb_gemv_step_kernel<7, kMath>;
+    default: return &mnb_gemv_step_kernel<8, kMath>;
   }
 }
 
@@ -1584,9 +1593,9 @@ MmaFn pick_step_kernel(int M, int math) {
   if (math == kMathMma) return step_kernel_for<kMathMma>(M);
   if (math == kMathWide) return step_kernel_for<kMathWide>(M);
   switch (M) {            // four rows per lane: M <= kStepFmaMaxM
-    case 1: return &gemv_step_kernel<1, kMathFma>;
-    case 2: return &gemv_step_kernel<2, kMathFma>;
-    default: return &gemv_step_kernel<3, kMathFma>;
+    case 1: return &mnb_gemv_step_kernel<1, kMathFma>;
+    case 2: return &mnb_gemv_step_kernel<2, kMathFma>;
+    default: return &mnb_gemv_step_kernel<3, kMathFma>;
   }
 }
 
@@ -1785,7 +1794,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // The prefill path (M > MNB_MAX_M): its own checks, then one launch.
 int gemm_prefill(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                  void* y, int M, int N, int K, int block, int out_dtype, int split_k,
-                 unsigned int flags, void* stream) {
+                 unsigned int flags, void* stream, LaunchDesc* query) {
   if (block == 16) return fail(MNB_ERR_BLOCK, "the prefill path takes block 32, 64 or 128");
   if (N < 1) return fail(MNB_ERR_SHAPE, "N must be >= 1");
   if (K < kBlock || K % kBlock != 0 || K % block != 0)
@@ -1814,11 +1823,11 @@ int gemm_prefill(const void* x, const uint8_t* qweight, const void* scales, cons
   const bool tc = !(flags & MNB_FLAG_PREFILL_MMA_SYNC) && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   if (tc)
     st = launch_prefill_tc(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
-                           dev.err, dev.sms, static_cast<cudaStream_t>(stream));
+                           dev.err, dev.sms, static_cast<cudaStream_t>(stream), query);
   else
     st = launch_prefill(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
-                        dev.sms, static_cast<cudaStream_t>(stream));
-  if (st != MNB_OK) return st;
+                        dev.sms, static_cast<cudaStream_t>(stream), query);
+  if (st != MNB_OK || query) return st;
   g_counters[16].fetch_add(1, std::memory_order_relaxed);
   if (tc) g_counters[17].fetch_add(1, std::memory_order_relaxed);
   g_counters[0].fetch_add(1, std::memory_order_relaxed);
@@ -1826,66 +1835,11 @@ int gemm_prefill(const void* x, const uint8_t* qweight, const void* scales, cons
   return MNB_OK;
 }
 
-}  // namespace mnb
-
-using namespace mnb;
-
-extern "C" {
-
-int mnb_abi_version(void) { return MNB_ABI_VERSION; }
-
-const char* mnb_status_string(int status) {
-  switch (status) {
-    case MNB_OK: return "ok";
-    case MNB_ERR_NULL: return "a required pointer is NULL";
-    case MNB_ERR_SHAPE: return "shape out of range";
-    case MNB_ERR_BLOCK: return "block size must be 32";
-    case MNB_ERR_DTYPE: return "unknown output dtype";
-    case MNB_ERR_SPLITK: return "split_k out of range";
-    case MNB_ERR_ALIGN: return "pointer misaligned";
-    case MNB_ERR_ALIAS: return "output overlaps an input";
-    case MNB_ERR_CUDA: return "CUDA runtime error";
-    case MNB_ERR_DEVICE: return "unsupported device";
-    case MNB_ERR_FLAGS: return "unknown flag bits";
-    default: return "unknown status";
-  }
-}
-
-const char* mnb_last_error_detail(void) { return t_detail.c_str(); }
-
-int mnb_max_split_k(int K, int* max_split) {
-  if (!max_split) return fail(MNB_ERR_NULL, "max_split is NULL");
-  if (K < kBlock || K % kBlock != 0) return fail(MNB_ERR_SHAPE, "K must be a positive multiple of 32");
-  *max_split = std::min(kMaxSplit, K / kBlock);
-  return MNB_OK;
-}
-
-int mnb_min_split_k(int M, int K, int* out) {
-  if (!out) return fail(MNB_ERR_NULL, "min_split is NULL");
-  int st = check_shape(M, 1, K);
-  if (st != MNB_OK) return st;
-  *out = min_split(M, K);
-  return MNB_OK;
-}
-
-int mnb_split_k_auto(int M, int N, int K, int* split_k) {
-  if (!split_k) return fail(MNB_ERR_NULL, "split_k is NULL");
-  int st = check_shape(M, N, K);
-  if (st != MNB_OK) return st;
-  DeviceInfo dev;
-  if ((st = device_info(&dev)) != MNB_OK) return st;
-  *split_k = step_shape(M, K, false) ? 1 : auto_split(M, N, K, dev.sms);
-  return MNB_OK;
-}
-
-int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp, void* y,
-             int M, int N, int K, int block, int out_dtype, int split_k, void* stream) {
-  return mnb_gemv_flags(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, 0u, stream);
-}
-
-int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
-                   void* y, int M, int N, int K, int block, int out_dtype, int split_k,
-                   unsigned int flags, void* stream) {
+// Validates a call, picks its kernel and launch shape, and launches it; with
+// `query` non-null it fills *query instead and launches nothing.
+int dispatch(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
+             void* y, int M, int N, int K, int block, int out_dtype, int split_k,
+             unsigned int flags, void* stream, LaunchDesc* query) {
   if (flags & ~static_cast<unsigned int>(MNB_FLAG_WEIGHTS_READY | MNB_FLAG_TENSOR_CORES |
                                           MNB_FLAG_PREFILL_MMA_SYNC))
     return fail(MNB_ERR_FLAGS, "unknown flag bits");
@@ -1894,7 +1848,7 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
     return fail(MNB_ERR_BLOCK, "block size must be 16, 32, 64 or 128");
   if (M > kMaxM && M <= MNB_MAX_PREFILL_M)
     return gemm_prefill(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, flags,
-                        stream);
+                        stream, query);
   int st = check_shape(M, N, K);
   if (st != MNB_OK) return st;
   if (K % block != 0) return fail(MNB_ERR_SHAPE, "K must be a multiple of the block size");
@@ -1934,7 +1888,8 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   if (block != kBlock || (zp == nullptr && !step)) {
     // the other formats of the family: one CUDA-core kernel for all of them
     if ((st = launch_general(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
-                             split_k, dev.sms, static_cast<cudaStream_t>(stream))) != MNB_OK)
+                             split_k, dev.sms, static_cast<cudaStream_t>(stream), query)) != MNB_OK ||
+        query)
       return st;
     g_counters[0].fetch_add(1, std::memory_order_relaxed);
     g_counters[out_dtype == MNB_OUT_BF16 ? 2 : 1].fetch_add(1, std::memory_order_relaxed);
@@ -1954,6 +1909,21 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   p.out_bf16 = out_dtype == MNB_OUT_BF16;
   p.weights_ready = (flags & MNB_FLAG_WEIGHTS_READY) ? 1 : 0;
 
+  const void* fn = step ? reinterpret_cast<const void*>(pick_step_kernel(M, math))
+                        : reinterpret_cast<const void*>(pick_kernel(M, ks));
+  if (query) {
+    query->fn = fn;
+    query->name = !step ? (split > 1 ? "row-tile kernel (K split over a cluster)" : "row-tile kernel")
+                  : math == kMathMma  ? "step kernel (tensor-core math)"
+                  : math == kMathWide ? "step kernel (CUDA-core, two rows per lane)"
+                                      : "step kernel (CUDA-core, four rows per lane)";
+    query->counter = step ? 13 : -1;
+    query->grid = plan.grid.x;
+    query->threads = plan.block.x;
+    query->cluster = static_cast<unsigned>(split);
+    query->smem = plan.smem;
+    return MNB_OK;
+  }
   CUtensorMap maps[3];
   if (step) {
     if ((st = tensor_map(kMapCodes, qweight, p, &maps[0])) != MNB_OK ||
@@ -1966,8 +1936,6 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
       p.tx_bytes -= kMmaRows * p.tr * p.zp_zb * 16;
     }
   }
-  const void* fn = step ? reinterpret_cast<const void*>(pick_step_kernel(M, math))
-                        : reinterpret_cast<const void*>(pick_kernel(M, ks));
   cudaError_t e = cudaFuncSetAttribute(fn,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(plan.smem));
@@ -1999,6 +1967,111 @@ int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, co
   g_counters[4 + M - 1].fetch_add(1, std::memory_order_relaxed);
   if (mma) g_counters[12].fetch_add(1, std::memory_order_relaxed);
   if (step) g_counters[13].fetch_add(1, std::memory_order_relaxed);
+  return MNB_OK;
+}
+
+}  // namespace mnb
+
+using namespace mnb;
+
+extern "C" {
+
+int mnb_abi_version(void) { return MNB_ABI_VERSION; }
+
+const char* mnb_status_string(int status) {
+  switch (status) {
+    case MNB_OK: return "ok";
+    case MNB_ERR_NULL: return "a required pointer is NULL";
+    case MNB_ERR_SHAPE: return "shape out of range";
+    case MNB_ERR_BLOCK: return "block size must be 16, 32, 64 or 128";
+    case MNB_ERR_DTYPE: return "unknown output dtype";
+    case MNB_ERR_SPLITK: return "split_k out of range";
+    case MNB_ERR_ALIGN: return "pointer misaligned";
+    case MNB_ERR_ALIAS: return "output overlaps an input";
+    case MNB_ERR_CUDA: return "CUDA runtime error";
+    case MNB_ERR_DEVICE: return "unsupported device";
+    case MNB_ERR_FLAGS: return "unknown flag bits";
+    default: return "unknown status";
+  }
+}
+
+const char* mnb_last_error_detail(void) { return t_detail.c_str(); }
+
+const char* mnb_last_cuda_error(void) { return t_detail.c_str(); }
+
+int mnb_max_split_k(int K, int* max_split) {
+  if (!max_split) return fail(MNB_ERR_NULL, "max_split is NULL");
+  if (K < kBlock || K % kBlock != 0) return fail(MNB_ERR_SHAPE, "K must be a positive multiple of 32");
+  *max_split = std::min(kMaxSplit, K / kBlock);
+  return MNB_OK;
+}
+
+int mnb_min_split_k(int M, int K, int* out) {
+  if (!out) return fail(MNB_ERR_NULL, "min_split is NULL");
+  int st = check_shape(M, 1, K);
+  if (st != MNB_OK) return st;
+  *out = min_split(M, K);
+  return MNB_OK;
+}
+
+int mnb_split_k_auto(int M, int N, int K, int* split_k) {
+  if (!split_k) return fail(MNB_ERR_NULL, "split_k is NULL");
+  int st = check_shape(M, N, K);
+  if (st != MNB_OK) return st;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != MNB_OK) return st;
+  *split_k = step_shape(M, K, false) ? 1 : auto_split(M, N, K, dev.sms);
+  return MNB_OK;
+}
+
+int mnb_gemv(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp, void* y,
+             int M, int N, int K, int block, int out_dtype, int split_k, void* stream) {
+  return mnb_gemv_flags(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, 0u, stream);
+}
+
+int mnb_gemv_flags(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
+                   void* y, int M, int N, int K, int block, int out_dtype, int split_k,
+                   unsigned int flags, void* stream) {
+  return dispatch(x, qweight, scales, zp, y, M, N, K, block, out_dtype, split_k, flags, stream,
+                  nullptr);
+}
+
+int mnb_gemv_launch_info(const void* x, const uint8_t* qweight, const void* scales,
+                         const uint8_t* zp, const void* y, int M, int N, int K, int block,
+                         int out_dtype, int split_k, unsigned int flags, mnb_launch_info* info) {
+  if (!info) return fail(MNB_ERR_NULL, "info is NULL");
+  LaunchDesc d;
+  int st = dispatch(x, qweight, scales, zp, const_cast<void*>(y), M, N, K, block, out_dtype,
+                    split_k, flags, nullptr, &d);
+  if (st != MNB_OK) return st;
+  cudaError_t e = cudaFuncSetAttribute(d.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(d.smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  cudaFuncAttributes fa{};
+  if ((e = cudaFuncGetAttributes(&fa, d.fn)) != cudaSuccess)
+    return cuda_fail(e, "cudaFuncGetAttributes");
+  int ctas = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, d.fn, static_cast<int>(d.threads),
+                                                         d.smem)) != cudaSuccess)
+    return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  int dev = 0, max_threads = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if ((e = cudaDeviceGetAttribute(&max_threads, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) !=
+      cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(max threads per SM)");
+  std::memset(info, 0, sizeof(*info));
+  std::snprintf(info->kernel, sizeof(info->kernel), "%s", d.name);
+  info->counter = d.counter;
+  info->grid = static_cast<int>(d.grid);
+  info->threads = static_cast<int>(d.threads);
+  info->cluster = static_cast<int>(d.cluster);
+  info->dynamic_smem = static_cast<int>(d.smem);
+  info->static_smem = static_cast<int>(fa.sharedSizeBytes);
+  info->registers_per_thread = fa.numRegs;
+  info->ctas_per_sm = ctas;
+  info->max_threads_per_sm = max_threads;
+  info->theoretical_occupancy =
+      max_threads > 0 ? static_cast<double>(ctas) * d.threads / max_threads : 0.0;
   return MNB_OK;
 }
 

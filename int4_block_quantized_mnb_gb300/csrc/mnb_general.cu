@@ -24,6 +24,7 @@
 // fp32 sums per (row, m), reduced across lanes by a fixed shuffle tree and
 // across the S warps through shared memory in warp order.
 #include "mnb.h"
+#include "mnb_launch.cuh"
 #include "mnb_dequant.cuh"
 #include "mnb_narrow.cuh"
 
@@ -513,7 +514,7 @@ int general_split(int M, int N, int K, int split_k, int sms) {
 // (block in {16, 32, 64, 128}, K a multiple of 32 and of the block size).
 int launch_general(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                    void* y, int M, int N, int K, int block, int out_bf16, int split_k, int sms,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, LaunchDesc* query) {
   GenParams p{};
   p.x = static_cast<const uint16_t*>(x);
   p.q = qweight;
@@ -552,6 +553,16 @@ int launch_general(const void* x, const uint8_t* qweight, const void* scales, co
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kGenXSmemMax);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(general format)");
+  if (query) {
+    query->fn = reinterpret_cast<const void*>(fn);
+    query->name = M <= 2 ? "general-format kernel (rows of a warp over chunks)"
+                         : "general-format kernel (two rows per lane)";
+    query->counter = 15;
+    query->grid = cfg.gridDim.x;
+    query->threads = cfg.blockDim.x;
+    query->smem = cfg.dynamicSmemBytes;
+    return MNB_OK;
+  }
   void* args[1] = {&p};
   e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(fn), args);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC(general format)");

@@ -17,6 +17,7 @@
 // fp32; each quantization block's sum D starts from zero and is scaled into
 // fp32 accumulators when the block ends.
 #include "mnb.h"
+#include "mnb_launch.cuh"
 #include "mnb_dequant.cuh"
 #include "mnb_narrow.cuh"
 
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(kPfWarps * 32, kCtas) gemm_prefill_pipelined(c
 // block 32, 64 or 128, K a multiple of 32 and of the block size).
 int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                    void* y, int M, int N, int K, int block, int out_bf16, int sms,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, LaunchDesc* query) {
   PfParams p{};
   p.x = static_cast<const uint16_t*>(x);
   p.q = qweight;
@@ -443,6 +444,17 @@ int launch_prefill(const void* x, const uint8_t* qweight, const void* scales, co
     const cudaError_t ea =
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (ea != cudaSuccess) return cuda_fail(ea, "cudaFuncSetAttribute(prefill)");
+  }
+  if (query) {
+    query->fn = fn;
+    query->name = p.x_aligned ? "prefill GEMM, mma.sync form (pipelined)"
+                              : "prefill GEMM, mma.sync form (synchronous, unaligned x)";
+    query->counter = 16;
+    query->grid = cfg.gridDim.x * cfg.gridDim.y * cfg.gridDim.z;
+    query->threads = cfg.blockDim.x;
+    query->cluster = static_cast<unsigned>(p.ksplit);
+    query->smem = cfg.dynamicSmemBytes;
+    return MNB_OK;
   }
   const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC(prefill)");

@@ -30,6 +30,7 @@
 // CTAs (the launcher weighs waves of CTAs against the reduction); their fp32
 // tiles are summed in rank order through distributed shared memory.
 #include "mnb.h"
+#include "mnb_launch.cuh"
 #include "mnb_dequant.cuh"
 #include "mnb_narrow.cuh"
 
@@ -611,7 +612,7 @@ TcEncodeFn tc_encode_fn() {
 // arguments and checked that x is 16-byte aligned.
 int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales, const uint8_t* zp,
                       void* y, int M, int N, int K, int block, int out_bf16, unsigned int* err,
-                      int sms, cudaStream_t stream) {
+                      int sms, cudaStream_t stream, LaunchDesc* query) {
   TcParams p{};
   p.x = static_cast<const uint16_t*>(x);
   p.q = qweight;
@@ -689,6 +690,16 @@ int launch_prefill_tc(const void* x, const uint8_t* qweight, const void* scales,
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = static_cast<unsigned>(p.ksplit);
     cfg.numAttrs = 2;
+  }
+  if (query) {
+    query->fn = fn;
+    query->name = "prefill GEMM, tcgen05 form";
+    query->counter = 17;
+    query->grid = cfg.gridDim.x * cfg.gridDim.y * cfg.gridDim.z;
+    query->threads = cfg.blockDim.x;
+    query->cluster = static_cast<unsigned>(p.ksplit);
+    query->smem = cfg.dynamicSmemBytes;
+    return MNB_OK;
   }
   // the activations as (k, row) fp16 pairs of bits: boxes of 64 k (one
   // 128-byte swizzle row) x tok rows, zero-filled past K and M

@@ -10,6 +10,8 @@ the two bf16 values may be one bf16 ulp apart.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -59,10 +61,12 @@ def run(dev, out="f16", split_k=0, y=None, tensor_cores=False, block=32, prefill
     return y
 
 
-def compare(inp, y16_bits, ybf_bits=None, cols=None, threads=8, symmetric=False):
-    """Assert the bound and the bf16 invariant on columns ``cols`` (all if None);
-    the oracle runs at the inputs' block size, without zero-points when
-    ``symmetric``."""
+def compare(inp, y16_bits, ybf_bits=None, cols=None, threads=None, symmetric=False):
+    """Assert the bound and the bf16 invariant on columns ``cols`` (all if None,
+    the default everywhere: every one of the M*N outputs is compared); the
+    oracle runs at the inputs' block size, without zero-points when
+    ``symmetric``, on all host threads unless ``threads`` says otherwise."""
+    threads = threads or os.cpu_count() or 1
     o = oracle()
     M, N, K = inp.M, inp.N, inp.K
     ref = o.gemv(inp.x, inp.qweight, inp.scales, None if symmetric else inp.zp, M, N, K,

@@ -74,3 +74,38 @@ def test_prefill_options_parse(monkeypatch):
     monkeypatch.setattr("sys.argv", ["bench.py", "--m", "512", "--prefill-mma-sync", "--block", "64"])
     a = bench.parse()
     assert a.m == 512 and a.prefill_mma_sync and a.block == 64 and not a.tensor_cores
+
+
+def test_default_workload_is_the_lm_head_projection():
+    assert bench.DEFAULT_WORKLOAD == "lm-head-m1-k4096-n151936"
+    assert bench.DEFAULT_WORKLOAD in WORKLOADS
+
+
+def test_graph_steps_give_about_ten_replays_of_whole_rotations():
+    # the full test run: 20 steps of lm-head (2 weight copies, one launch a step)
+    G = bench.graph_steps(20, 2)
+    assert G == 2 and divmod(20, G) == (10, 0)
+    assert bench.graph_steps(2000, 2) == 200
+    assert bench.graph_steps(20, 28) == 20            # one rotation is longer than K
+    assert bench.graph_steps(3, 1) == 1
+    for steps in (1, 7, 20, 99, 2000):
+        for rot in (1, 2, 3, 28):
+            g = bench.graph_steps(steps, rot)
+            assert 1 <= g <= steps and (g % rot == 0 or g == steps)
+
+
+def test_config_records_cover_the_five_configurations():
+    cfgs = {c for c, _, _ in bench.CONFIG_RECORDS}
+    assert cfgs == {0, 1, 2, 3, 4}
+    names = [(n, o) for _, n, o in bench.CONFIG_RECORDS]
+    assert ("attn-proj-m1-k4096-n4096", "f16") in names and ("attn-proj-m1-k4096-n4096", "bf16") in names
+    assert {n for n, _ in names if n.startswith("small-batch")} == {
+        "small-batch-m2-k8192-n8192", "small-batch-m4-k8192-n8192", "small-batch-m8-k8192-n8192"}
+    for _, n, o in bench.CONFIG_RECORDS:
+        assert o in WORKLOADS[n].out_dtypes
+
+
+def test_pages_context_quotes_the_a100_figures():
+    c = bench.PAGES_CONTEXT
+    assert c["gate_up_gemv"]["us_per_call"] == 26.69 and c["gate_up_gemv"]["dram_tb_per_s"] == 2.267
+    assert c["decode_64_tokens_bf16"]["cast_half_launches"] == [3024, 2398]

@@ -22,11 +22,11 @@ def built():
     mnb.load()
 
 
-def _run_both(inp, symmetric, split=0, cols=None):
+def _run_both(inp, symmetric, split=0):
     dev = _gpu.to_device(inp, symmetric=symmetric)
     y16 = _gpu.bits(_gpu.run(dev, "f16", split, block=inp.block))
     ybf = _gpu.bits(_gpu.run(dev, "bf16", split, block=inp.block))
-    return _gpu.compare(inp, y16, ybf, cols=cols, symmetric=symmetric)
+    return _gpu.compare(inp, y16, ybf, symmetric=symmetric)
 
 
 @pytest.mark.parametrize("block,symmetric", FORMATS, ids=FORMAT_IDS)
@@ -62,11 +62,9 @@ def test_every_split(block, symmetric, split):
     (4, 8192, 8192, 128, True),
 ])
 def test_full_size(M, N, K, block, symmetric):
-    """Decode-layer sizes, compared on sampled output columns."""
+    """Decode-layer sizes, every output element compared with the oracle."""
     inp = make_inputs(M, N, K, seed=N + block, block=block)
-    cols = np.random.default_rng(block).choice(N, size=min(N, 384), replace=False)
-    cols.sort()
-    _run_both(inp, symmetric, cols=cols)
+    _run_both(inp, symmetric)
 
 
 @pytest.mark.parametrize("block", [16, 64, 128])
@@ -140,8 +138,7 @@ def test_symmetric_block32_on_the_step_kernel(M, N, K, tc):
     c1 = mnb.counters()
     assert c1[13] - c0[13] == 2 and c1[15] == c0[15]
     assert c1[12] - c0[12] == (2 if tc else 0)
-    cols = None if N <= 1000 else np.random.default_rng(N).choice(N, size=384, replace=False)
-    _gpu.compare(inp, y16, ybf, cols=cols, symmetric=True)
+    _gpu.compare(inp, y16, ybf, symmetric=True)
 
 
 def test_symmetric_and_asymmetric_step_launches_interleave():

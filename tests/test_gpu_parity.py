@@ -46,11 +46,6 @@ def test_every_split_k(M):
         _gpu.compare(inp, y16, ybf)
 
 
-def sample_cols(N, rng, n=384):
-    edge = np.r_[np.arange(min(N, 64)), np.arange(max(0, N - 64), N)]
-    return np.unique(np.r_[edge, rng.choice(N, size=min(N, n), replace=False)]).astype(np.int64)
-
-
 @pytest.mark.parametrize("tc", [False, True], ids=["default", "tensor_cores"])
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_workload_full_size(name, tc):
@@ -65,8 +60,8 @@ def test_workload_full_size(name, tc):
     assert not np.isnan(o.bf16_to_f64(ybf)).any()
     # the bf16 arm is the narrowed fp16 arm everywhere, not only where sampled
     assert np.array_equal(ybf, o.f16_to_bf16(y16))
-    cols = None if w.N * w.K <= 1 << 20 else sample_cols(w.N, np.random.default_rng(1))
-    _gpu.compare(inp, y16, ybf, cols=cols)
+    # every output element against the oracle
+    _gpu.compare(inp, y16, ybf)
 
 
 @pytest.mark.parametrize("M", [2, 4, 8])
@@ -82,9 +77,8 @@ def test_small_batch_every_row_written(M):
     # rows are distinct computations: no row is a copy of row 0
     for m in rows[1:]:
         assert not np.array_equal(ybits[m], ybits[0])
-    cols = sample_cols(N, np.random.default_rng(M), n=128)
     y16 = _gpu.bits(_gpu.run(dev, "f16"))
-    _gpu.compare(inp, y16, ybits, cols=cols)
+    _gpu.compare(inp, y16, ybits)
 
 
 def test_counters_prove_the_kernel_ran():
@@ -112,8 +106,7 @@ def test_tensor_core_kernel_only_on_request():
         y16 = _gpu.bits(_gpu.run(dev, "f16", split, tensor_cores=tc))
         ybf = _gpu.bits(_gpu.run(dev, "bf16", split, tensor_cores=tc))
         assert mnb.counters()[12] - before == 2 * want, (M, N, K, split, tc)
-        cols = None if N <= 256 else np.arange(0, N, 7)
-        _gpu.compare(inp, y16, ybf, cols=cols)
+        _gpu.compare(inp, y16, ybf)
 
 
 def test_mixed_shape_chain_matches_plain_calls():
@@ -154,8 +147,7 @@ def test_step_kernel_takes_default_launches():
         assert c1[12] == c0[12]
         if want:
             assert mnb.split_k_auto(M, N, K) == 1
-        cols = None if N <= 256 else np.arange(0, N, 5)
-        _gpu.compare(inp, y16, ybf, cols=cols)
+        _gpu.compare(inp, y16, ybf)
 
 
 TC_SHAPES = [(1, 1024), (17, 1024), (130, 2048), (33, 3072), (300, 5120), (19, 8192)]

@@ -519,9 +519,14 @@ class DeviceWorkload:
 
 
 def graph_steps(steps, rotation):
-    """Steps per captured graph for the K timed steps: a whole number of weight
-    rotations (`rotation` steps each) near K / 10, so about ten replays give
-    the per-call spread; never more than K."""
+    """Steps per captured graph for the K timed steps.  Up to 200 steps: all K
+    in one graph (a graph boundary costs the overlap of two launches, about
+    3.5 us, which at a few steps per graph would be measured as several
+    percent of the call).  Beyond that: a whole number of weight rotations
+    (`rotation` steps each) near K / 10, so about ten replays give the
+    per-call spread.  Never more than K."""
+    if steps <= 200:
+        return steps
     return min(steps, rotation * max(1, round(steps / 10 / rotation)))
 
 
@@ -669,10 +674,9 @@ def main():
             step(j)
     torch.cuda.synchronize(dev)
 
-    # The K timed steps: replays of a graph of G steps, G a whole number of
-    # weight rotations (R / L steps) and about K / 10, so the per-call spread
-    # comes from about ten replays; a shorter graph takes the remainder.
-    # Three untimed replays of each graph come first.
+    # The K timed steps: replays of a graph of G steps (graph_steps); a shorter
+    # graph takes the remainder.  Three untimed replays of each graph come
+    # first.
     G = graph_steps(args.steps, R // L)
     full, rem = divmod(args.steps, G)
 
@@ -782,13 +786,23 @@ def main():
         if world > 1:
             torch.distributed.destroy_process_group()
         return 0
+    # per-call spread: from the timed replays when there are several, else from
+    # the configuration sub-record of the same workload (20 replays)
+    spread, spread_source = None, None
+    if len(per_call_us) > 1:
+        spread = [pct(per_call_us, q) for q in (10, 50, 90)]
+        spread_source = f"{full} timed replays"
+    else:
+        for r in records or []:
+            if r["workload"] == w.name and r["out"] == outs[0]:
+                spread, spread_source = r["us_p10_p50_p90"], "configs sub-record of this workload"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "us_per_call": per_launch_s * 1e6,
-        "us_per_call_p10_p50_p90": ([pct(per_call_us, q) for q in (10, 50, 90)]
-                                    if per_call_us else None),
+        "us_per_call_p10_p50_p90": spread,
+        "us_per_call_spread_source": spread_source,
         "pct_of_hbm_peak": 100.0 * achieved / peak,
         "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "out_dtypes": outs,
                    "block": w_block(w), "zero_points": w_zp(w, inp) is not None,

@@ -157,11 +157,13 @@ int mnb_gemv(const void *x, const uint8_t *qweight, const void *scales, const ui
  * products, fp32 sums and the decode epilogue, meeting the same bound and
  * bf16 invariant (their fp16 bits may differ: different summation order):
  *   tcgen05   the default where x is 16-byte aligned.  Every dequantized
- *             weight (q - zp) s is split exactly into two fp16 parts
- *             (hi = fp16(w), lo = (w - hi) 2^11, both exact); two fp16
- *             tcgen05 GEMMs accumulate x hi and x lo in fp32 in tensor
- *             memory and the epilogue forms hi + 2^-11 lo (hi alone where it
- *             is not finite, so infinities and NaNs follow the exact form).
+ *             weight, as v = ((q - zp) / 16) s, is split exactly into two
+ *             fp16 parts (hi = fp16(v), which cannot overflow, and
+ *             lo = (v - hi) 2^11; exact for every finite fp16 scale); two
+ *             fp16 tcgen05 GEMMs accumulate x hi and x lo in fp32 in tensor
+ *             memory and the epilogue forms 16 (hi + 2^-11 lo) (16 hi alone
+ *             where it is not finite, so infinities and NaNs follow the exact
+ *             form).
  *   mma.sync  per-block fp32 sums of the exact fp16 products (q - zp) x,
  *             scaled into fp32 accumulators.  Used where x is not 16-byte
  *             aligned, and on request:

@@ -56,6 +56,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <type_traits>
 
 namespace mnb {
 
@@ -176,6 +177,57 @@ __device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity,
   return ok != 0;
 }
 
+// Calls f(std::integral_constant<int, 0>) .. f(std::integral_constant<int, N - 1>):
+// an unrolled loop whose index is a compile-time constant (immediate offsets).
+template <int I, int N, typename F>
+__device__ __forceinline__ void static_for_from(F&& f) {
+  if constexpr (I < N) {
+    f(std::integral_constant<int, I>{});
+    static_for_from<I + 1, N>(f);
+  }
+}
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  static_for_from<0, N>(f);
+}
+
+// Shared-memory loads at 32-bit shared addresses.  They are ordered after the
+// preceding mbarrier wait (both are volatile with a memory clobber), which is
+// what makes the stage's bytes visible.
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+// The same at a + OFF, OFF folded into the instruction's immediate.
+template <int OFF>
+__device__ __forceinline__ uint4 lds_v4_at(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4+%5];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a), "n"(OFF)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -184,6 +236,10 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Slow path of mbar_wait: polls until the phase completes, the CTA abort flag
 // is raised, or kWaitLimitNs pass (then records `code` and raises the flag).
+// (A try_wait with a suspend-time hint sleeps instead of polling, but was
+// measured 1-4 % slower end to end on GB300, for the consumers' waits and for
+// the producer's and epilogue's alike: the wake-up after the phase completes
+// comes late.)
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                             unsigned code) {
   const uint64_t t0 = global_ns();
@@ -960,12 +1016,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   // Activations, staged once per CTA by the consumer warps: row m, block b,
   // k group tq -> 16 bytes holding x[m][32b + 8tq + {0..7}] paired (0,4)
   // (1,5) (2,6) (3,7), at xp + m * xp_pitch + b * 64 + tq * 16 (the B
-  // fragments of the tensor-core math) or + tq * C * 16 + b * 16 (CUDA-core
-  // math: eight lanes read eight consecutive blocks).
+  // fragments of the tensor-core math) or xp + b * (64 M + 16) + (tq * M + m)
+  // * 16 (CUDA-core math: a lane's block holds all M rows at offsets fixed at
+  // compile time, and the 16-byte pad puts the 8 blocks a quarter warp reads
+  // at once (four rows per lane) or the 4 blocks a warp reads (two rows per
+  // lane) in different bank groups).
   wait_prerequisites();
   unsigned char* xp = smem + p.xp_offset;
-  auto x_off = [&](int rem) {
-    return kMath == kMathMma ? rem * 16 : ((rem & 3) * p.C + (rem >> 2)) * 16;
+  auto x_at = [&](int m, int rem) {
+    return kMath == kMathMma ? m * p.xp_pitch + rem * 16
+                             : (rem >> 2) * (64 * M + 16) + ((rem & 3) * M + m) * 16;
   };
   {
     // 8 activations (one k group of a block) per element; K is a multiple of
@@ -976,7 +1036,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         for (int rem = threadIdx.x; rem < per_row; rem += W * 32) {
           const uint4 v =
               __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K) + rem);
-          *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + x_off(rem)) = pair_k4(v);
+          *reinterpret_cast<uint4*>(xp + x_at(m, rem)) = pair_k4(v);
         }
     } else {
       for (int m = 0; m < M; ++m)
@@ -987,7 +1047,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           v.y = __ldg(src + 2) | (static_cast<uint32_t>(__ldg(src + 3)) << 16);
           v.z = __ldg(src + 4) | (static_cast<uint32_t>(__ldg(src + 5)) << 16);
           v.w = __ldg(src + 6) | (static_cast<uint32_t>(__ldg(src + 7)) << 16);
-          *reinterpret_cast<uint4*>(xp + m * p.xp_pitch + x_off(rem)) = pair_k4(v);
+          *reinterpret_cast<uint4*>(xp + x_at(m, rem)) = pair_k4(v);
         }
     }
     if (p.zp == nullptr) {
@@ -1094,19 +1154,31 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // of the fp16 products (fma.rn.f32.f16); each block sum is scaled into the
     // row's accumulator.  A tile ends with a butterfly over the eight lanes of
     // a row and one partial per (row, m) for the epilogue.
+    //
+    // Every shared-memory address is a 32-bit offset fixed per lane except
+    // for the stage base (advanced by a whole stage) and the activation base
+    // (advanced by W_k segments per step); the four rows' products form four
+    // independent fp32 chains, interleaved k group by k group.
     const int j = lane & 7;
     const int rg = lane >> 3;
+    const int r0 = rho * kMmaRows + rg;                   // rows r0 + 4 i
     const uint32_t zsh = (j & 1) * 4;                     // this block's nibble in its zp byte
-    int qo[4], so[4], zo[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = rho * kMmaRows + rg + 4 * i;
-      qo[i] = (R * ks + r) * 128 + 16 * (j ^ (r & 7));
-      so[i] = p.sc_offset + (r * p.sc_sb + ks) * 16 + 2 * j;
-      zo[i] = p.zp_offset + r * p.zp_zb * 16 + (j >> 1);
-    }
-    const unsigned char* xl = xp + j * 16;
-    const int kg_pitch = p.C * 16;                        // bytes per k group of a row
+    // rows i and i + 2 share their swizzle: row i + 2 is 1024 bytes on
+    const uint32_t q_lane0 = (R * ks + r0) * 128 + 16 * (j ^ (r0 & 7));
+    const uint32_t q_lane1 = (R * ks + r0 + 4) * 128 + 16 * (j ^ ((r0 + 4) & 7));
+    const uint32_t sc_lane = p.sc_offset + (r0 * p.sc_sb + ks) * 16 + 2 * j;
+    const uint32_t sc_row4 = 4 * p.sc_sb * 16;            // scale offset of row + 4
+    const uint32_t zp_lane = p.zp_offset + r0 * p.zp_zb * 16 + (j >> 1);
+    const uint32_t zp_row4 = 4 * p.zp_zb * 16;            // zero-point offset of row + 4
+    const uint32_t ring0 = smem_u32(smem);
+    const uint32_t stage_bytes = p.stage_bytes;
+    const int stages = p.stages;
+    const int steps = p.steps;
+    const int wk = p.wk;
+    constexpr uint32_t kXBlock = 64 * M + 16;            // bytes per activation block
+    const uint32_t x_lane = smem_u32(xp) + (8 * ks + j) * kXBlock;   // block 8 ks + j of step 0
+    const uint32_t x_step = wk * 8 * kXBlock;
+    uint32_t sb = ring0, fb = full0, eb = empty0;         // stage s: data, full and empty barriers
     int s = 0;
     uint32_t ph = 0;
     bool run = true;
@@ -1116,60 +1188,80 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
-      for (int step = 0; step < p.steps; ++step) {
-        if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) {
+      uint32_t xa = x_lane;
+      uint32_t zr = 0;                                    // first segment of the stage, mod 4
+      for (int step = 0; step < steps; ++step) {
+        if (!mbar_wait(fb, ph, abort_flag, kErrStageData)) {
           run = false;
           break;
         }
-        const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-        const int seg0 = step * p.wk;
-        const int G = seg0 + ks;                            // this warp's segment
-        const int zb = ((G >> 2) - (seg0 >> 2)) * 16 + (G & 3) * 4;
-        const unsigned char* xb = xl + G * 128;             // block 8 G + j
+        // zero-point bytes of segment G = seg0 + ks sit 4 (seg0 % 4 + ks) bytes into
+        // the row's box, which starts at the 16-byte chunk holding seg0
+        const uint32_t zrow = sb + zp_lane + 4 * (zr + ks);
         uint4 xr[M][4];
-#pragma unroll
-        for (int m = 0; m < M; ++m)
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            xr[m][g] = *reinterpret_cast<const uint4*>(xb + m * p.xp_pitch + g * kg_pitch);
+        static_for<M * 4>([&](auto c) {
+          constexpr int m = decltype(c)::value % M, g = decltype(c)::value / M;
+          xr[m][g] = lds_v4_at<(g * M + m) * 16>(xa);
+        });
+        uint4 w[4];
+        uint32_t zl[4], zh[4];
+        float sc[4];
+        const uint32_t qa0 = sb + q_lane0, qa1 = sb + q_lane1;
+        w[0] = lds_v4_at<0>(qa0);
+        w[1] = lds_v4_at<0>(qa1);
+        w[2] = lds_v4_at<1024>(qa0);
+        w[3] = lds_v4_at<1024>(qa1);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          // rows i and i + 2 share their swizzle: row i + 2 is 1024 bytes on
-          const uint4 w = *reinterpret_cast<const uint4*>(st + qo[i & 1] + 1024 * (i >> 1));
-          const uint32_t z = (static_cast<uint32_t>(st[zo[i] + zb]) >> zsh) & 0xFu;
+          const uint32_t z = (lds_u8(zrow + i * zp_row4) >> zsh) & 0xFu;
           // the bias words need no masking: z < 16 fills bits the magic leaves clear
-          const uint32_t zl = z * 0x00010001u + 0x64006400u;                       // 1024 + zp
-          const uint32_t zh = z * 0x00100010u + 0x54005400u;                       //   64 + zp
-          const float sc = half_word_to_float(*reinterpret_cast<const uint16_t*>(st + so[i]), 0);
-          const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-          float bs[M];
+          zl[i] = z * 0x00010001u + 0x64006400u;                                   // 1024 + zp
+          zh[i] = z * 0x00100010u + 0x54005400u;                                   //   64 + zp
+          sc[i] = half_word_to_float(lds_u16(sb + sc_lane + i * sc_row4), 0);
+        }
+        float bs[4][M];
 #pragma unroll
-          for (int m = 0; m < M; ++m) bs[m] = 0.f;
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint32_t word = words[g];
+          for (int m = 0; m < M; ++m) bs[i][m] = 0.f;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t word = g == 0 ? w[i].x : g == 1 ? w[i].y : g == 2 ? w[i].z : w[i].w;
             const uint32_t w8 = word >> 8;
-            const uint32_t d0 = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl);   // k0, k4
-            const uint32_t d1 = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh);   // k1, k5
-            const uint32_t d2 = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl);     // k2, k6
-            const uint32_t d3 = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh);     // k3, k7
+            const uint32_t d0 = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl[i]);   // k0, k4
+            const uint32_t d1 = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh[i]);   // k1, k5
+            const uint32_t d2 = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl[i]);     // k2, k6
+            const uint32_t d3 = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh[i]);     // k3, k7
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-              bs[m] = fma2_f16_f32(xr[m][g].x, d0, bs[m]);
-              bs[m] = fma2_f16_f32(xr[m][g].y, d1, bs[m]);
-              bs[m] = fma2_f16_f32(xr[m][g].z, d2, bs[m]);
-              bs[m] = fma2_f16_f32(xr[m][g].w, d3, bs[m]);
+              bs[i][m] = fma2_f16_f32(xr[m][g].x, d0, bs[i][m]);
+              bs[i][m] = fma2_f16_f32(xr[m][g].y, d1, bs[i][m]);
+              bs[i][m] = fma2_f16_f32(xr[m][g].z, d2, bs[i][m]);
+              bs[i][m] = fma2_f16_f32(xr[m][g].w, d3, bs[i][m]);
             }
           }
+        }
 #pragma unroll
-          for (int m = 0; m < M; ++m) acc[i][m] = fmaf(bs[m], sc, acc[i][m]);
-        }
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int m = 0; m < M; ++m) acc[i][m] = fmaf(bs[i][m], sc[i], acc[i][m]);
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8u * s);
-        if (++s == p.stages) {
+        if (lane == 0) mbar_arrive(eb);
+        if (++s == stages) {
           s = 0;
+          sb = ring0;
+          fb = full0;
+          eb = empty0;
           ph ^= 1u;
+        } else {
+          sb += stage_bytes;
+          fb += 8u;
+          eb += 8u;
         }
+        xa += x_step;
+        zr = (zr + wk) & 3u;
       }
       if (!run) break;
       // the eight blocks of each row's segment, in a fixed butterfly order
@@ -1192,7 +1284,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int m = 0; m < M; ++m) slot[(rho * kMmaRows + rg + 4 * i) * M + m] = acc[i][m];
+          for (int m = 0; m < M; ++m) slot[(r0 + 4 * i) * M + m] = acc[i][m];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(ready0 + 8u * js);
@@ -1204,20 +1296,27 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // 8-k group, shared by the eight lanes of a quarter warp) feeds both rows,
     // which balances shared-memory bandwidth against the FMA pipe; a lane holds
     // 2M accumulators, 2M block sums and one group's 4M activation registers.
+    // Activation offsets inside a block are compile-time constants; only the
+    // block base moves (by W_k segments a step).
     const int rr = lane & 7;
     const int q = lane >> 3;
     const int r0 = rho * kMmaRows + rr;                  // rows r0 and r0 + 8 (both rr mod 8)
-    uint32_t qo[2];                                      // block 2q + e of row r0; row r0 + 8 is +1024
-#pragma unroll
-    for (int e = 0; e < 2; ++e) qo[e] = (R * ks + r0) * 128 + 16 * ((2 * q + e) ^ rr);
-    int so[2], zo[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      so[i] = p.sc_offset + ((r0 + 8 * i) * p.sc_sb + ks) * 16 + 4 * q;   // scales of the pair
-      zo[i] = p.zp_offset + (r0 + 8 * i) * p.zp_zb * 16 + q;             // its zero-point byte
-    }
-    const unsigned char* xq = xp + (8 * ks + 2 * q) * 16;                // block 8 G + 2 q
-    const int kg_pitch = p.C * 16;                                         // bytes per k group
+    // block 2q + e of row r0; row r0 + 8 is 1024 bytes on
+    const uint32_t q_lane0 = (R * ks + r0) * 128 + 16 * ((2 * q) ^ rr);
+    const uint32_t q_lane1 = (R * ks + r0) * 128 + 16 * ((2 * q + 1) ^ rr);
+    const uint32_t sc_lane = p.sc_offset + (r0 * p.sc_sb + ks) * 16 + 4 * q;   // scales of the pair
+    const uint32_t sc_row8 = 8 * p.sc_sb * 16;
+    const uint32_t zp_lane = p.zp_offset + r0 * p.zp_zb * 16 + q;            // its zero-point byte
+    const uint32_t zp_row8 = 8 * p.zp_zb * 16;
+    constexpr uint32_t kXBlock = 64 * M + 16;                            // bytes per activation block
+    const uint32_t ring0 = smem_u32(smem);
+    const uint32_t stage_bytes = p.stage_bytes;
+    const int stages = p.stages;
+    const int steps = p.steps;
+    const int wk = p.wk;
+    const uint32_t x_lane = smem_u32(xp) + (8 * ks + 2 * q) * kXBlock;     // block 8 ks + 2 q
+    const uint32_t x_step = wk * 8 * kXBlock;
+    uint32_t sb = ring0, fb = full0, eb = empty0;
     int s = 0;
     uint32_t ph = 0;
     bool run = true;
@@ -1227,55 +1326,62 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
-      const unsigned char* xs = xq;
-      for (int step = 0; step < p.steps; ++step, xs += p.wk * 128) {
-        if (!mbar_wait(full0 + 8u * s, ph, abort_flag, kErrStageData)) {
+      uint32_t xa = x_lane;
+      uint32_t zr = 0;                                    // first segment of the stage, mod 4
+      for (int step = 0; step < steps; ++step) {
+        if (!mbar_wait(fb, ph, abort_flag, kErrStageData)) {
           run = false;
           break;
         }
-        const unsigned char* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-        const int seg0 = step * p.wk;
-        const int G = seg0 + ks;                            // this warp's segment
-        const int zb = ((G >> 2) - (seg0 >> 2)) * 16 + (G & 3) * 4;
-        uint32_t sw[2];
-        ZpPairs zz[2];
+        const uint32_t zrow = sb + zp_lane + 4 * (zr + ks);
+        uint32_t sw[2], zw[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          sw[i] = *reinterpret_cast<const uint32_t*>(st + so[i]);
-          const uint32_t zbyte = st[zo[i] + zb];
-          zz[i] = zp_pairs(zbyte * 0x00010001u);
+          sw[i] = lds_u32(sb + sc_lane + i * sc_row8);
+          zw[i] = lds_u8(zrow + i * zp_row8) * 0x00010001u;   // the pair's zp byte, both halves
         }
+        static_for<2>([&](auto ec) {                      // block 2q + e
+          constexpr int e = decltype(ec)::value;
+          // this block's codes and bias words for both rows (one block at a
+          // time keeps the wide M within the register budget)
+          const uint32_t qa = sb + (e ? q_lane1 : q_lane0);
+          uint4 w[2];
+          uint32_t zl[2], zh[2];
+          w[0] = lds_v4_at<0>(qa);
+          w[1] = lds_v4_at<1024>(qa);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {                       // block 2q + e
+          for (int i = 0; i < 2; ++i) {
+            if (e == 0) {
+              zl[i] = and_or(zw[i], 0x000F000Fu, 0x64006400u);        // 1024 + z_even
+              zh[i] = hsub2(zl[i], 0x63806380u);                       //   64 + z_even
+            } else {
+              zh[i] = and_or(zw[i], 0x00F000F0u, 0x54005400u);        //   64 + z_odd
+              zl[i] = hadd2(zh[i], 0x63806380u);                       // 1024 + z_odd
+            }
+          }
           float bs[2][M];
 #pragma unroll
           for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int m = 0; m < M; ++m) bs[i][m] = 0.f;
-          uint4 w[2];                                       // both rows' 32 codes
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-            w[i] = *reinterpret_cast<const uint4*>(st + qo[e] + 1024 * i);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          static_for<4>([&](auto gc) {
+            constexpr int g = decltype(gc)::value;
             // both rows' q - zp pairs of this 8-k group, then one activation
             // row at a time
             uint32_t d[2][4];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-              const uint32_t zl = e ? zz[i].lo_o : zz[i].lo_e;      // 1024 + zp
-              const uint32_t zh = e ? zz[i].hi_o : zz[i].hi_e;      //   64 + zp
-              const uint32_t word = g == 0 ? w[i].x : g == 1 ? w[i].y : g == 2 ? w[i].z : w[i].w;
+              const uint4 wv = w[i];
+              const uint32_t word = g == 0 ? wv.x : g == 1 ? wv.y : g == 2 ? wv.z : wv.w;
               const uint32_t w8 = word >> 8;
-              d[i][0] = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl);   // k0, k4
-              d[i][1] = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh);   // k1, k5
-              d[i][2] = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl);     // k2, k6
-              d[i][3] = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh);     // k3, k7
+              d[i][0] = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl[i]);   // k0, k4
+              d[i][1] = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh[i]);   // k1, k5
+              d[i][2] = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl[i]);     // k2, k6
+              d[i][3] = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh[i]);     // k3, k7
             }
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-              const uint4 xv =
-                  *reinterpret_cast<const uint4*>(xs + 16 * e + m * p.xp_pitch + g * kg_pitch);
+            static_for<M>([&](auto mc) {
+              constexpr int m = decltype(mc)::value;
+              const uint4 xv = lds_v4_at<e * kXBlock + (g * M + m) * 16>(xa);
 #pragma unroll
               for (int i = 0; i < 2; ++i) {
                 bs[i][m] = fma2_f16_f32(xv.x, d[i][0], bs[i][m]);
@@ -1283,21 +1389,30 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 bs[i][m] = fma2_f16_f32(xv.z, d[i][2], bs[i][m]);
                 bs[i][m] = fma2_f16_f32(xv.w, d[i][3], bs[i][m]);
               }
-            }
-          }
+            });
+          });
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             const float sc = half_word_to_float(sw[i], e);
 #pragma unroll
             for (int m = 0; m < M; ++m) acc[i][m] = fmaf(bs[i][m], sc, acc[i][m]);
           }
-        }
+        });
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8u * s);
-        if (++s == p.stages) {
+        if (lane == 0) mbar_arrive(eb);
+        if (++s == stages) {
           s = 0;
+          sb = ring0;
+          fb = full0;
+          eb = empty0;
           ph ^= 1u;
+        } else {
+          sb += stage_bytes;
+          fb += 8u;
+          eb += 8u;
         }
+        xa += x_step;
+        zr = (zr + wk) & 3u;
       }
       if (!run) break;
       // the four block pairs of each row's segment, in a fixed butterfly order
@@ -1544,6 +1659,8 @@ int make_plan(const DeviceInfo& dev, int M, int N, int K, int split, const Kerne
 // each) in one shared-memory wavefront of the tensor-core fragment loads.
 int mma_x_pitch(int C) { return C * 64 + ((C & 1) ? 0 : 64); }
 int mma_x_bytes(int M, int C) { return M * mma_x_pitch(C); }
+// CUDA-core maths: blocks of all M rows, 64 M + 16 bytes each
+int wide_x_bytes(int M, int C) { return C * (64 * M + 16); }
 
 // The step kernel takes a launch without a K split (split_k 0 or 1) when K
 // is a multiple of 1024 (whole 256-k segments and 16-byte zero-point rows for
@@ -1560,10 +1677,14 @@ int step_math(int M, bool tensor_cores) {
   return tensor_cores ? kMathMma : (M <= kStepFmaMaxM ? kMathFma : kMathWide);
 }
 
+int step_x_bytes(int M, int C, int math) {
+  return math == kMathMma ? mma_x_bytes(M, C) : wide_x_bytes(M, C);
+}
+
 bool step_shape(int M, int K, bool tensor_cores) {
   const int math = step_math(M, tensor_cores);
-  const int limit = math == kMathWide ? kWideXBytes : kMmaXBytes;
-  return K % 1024 == 0 && K <= 65536 && mma_x_bytes(M, K / kBlock) <= limit;
+  const int limit = math == kMathMma ? kMmaXBytes : kWideXBytes;
+  return K % 1024 == 0 && K <= 65536 && step_x_bytes(M, K / kBlock, math) <= limit;
 }
 
 bool use_step(int M, int K, int split_k, const void* scales, const void* zp,
@@ -1607,7 +1728,7 @@ int odd_at_least(int v) { return v | 1; }
 // the best and that keeps as many SMs busy; K slices: the largest divisor of
 // K / 256 up to 16 / tr (at least 4 where K allows, so a stage's zero-point
 // chunk is never re-read).  A stage always holds about 32 KB of codes.
-int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, Plan* plan) {
+int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, int math, Plan* plan) {
   Params& p = plan->p;
   p.M = M;
   p.N = N;
@@ -1618,7 +1739,7 @@ int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, Plan* plan) {
   p.groups = 1;
   const int S = K / kMmaSeg;
   p.xp_pitch = mma_x_pitch(p.C);
-  const int x_bytes = mma_x_bytes(M, p.C);
+  const int x_bytes = step_x_bytes(M, p.C, math);
   const int budget = static_cast<int>(dev.smem_optin) - 1024;   // 1 KB for the alignment
   const long long tiles16 = (static_cast<long long>(N) + kMmaRows - 1) / kMmaRows;
   const long long sms = std::max(1, dev.sms);
@@ -1877,7 +1998,7 @@ int dispatch(const void* x, const uint8_t* qweight, const void* scales, const ui
   const int math = step_math(M, tc);
   bool step = block == kBlock && use_step(M, K, split_k, scales, zp, tc);
   Plan plan{};
-  if (step && make_mma_plan(dev, M, N, K, &plan) != MNB_OK) {
+  if (step && make_mma_plan(dev, M, N, K, math, &plan) != MNB_OK) {
     step = false;                                 // no stage layout fits: row-tile kernel
     plan = Plan{};
   }

@@ -1,13 +1,17 @@
 // mnb_prefill_tc.cu -- the prefill GEMM (M > 8) on the fifth-generation tensor
 // cores: tcgen05.mma with fp32 accumulators in tensor memory (TMEM).
 //
-// Exactness.  Each dequantized weight w = (q - zp) s has at most 15
-// significant bits (4 of q - zp, 11 of the fp16 scale), so it splits exactly
-// into hi = fp16(w) and lo = w - hi, and lo' = lo 2^11 is an fp16 value as
-// well (at most 4 significant bits, at most |hi| in magnitude; normal for
-// |w| >= 2^-11).  Two fp16 GEMMs then give exact products x hi and x lo' with
-// fp32 sums: y = D_hi + 2^-11 D_lo.  No per-block scaling is needed, so both
-// accumulators stay in TMEM across the whole K loop.
+// Exactness.  Each dequantized weight, taken as v = w / 16 = ((q - zp) / 16) s,
+// has at most 15 significant bits (4 of q - zp, 11 of the fp16 scale) and
+// |v| <= (15 / 16) 65504 < 65504, so it splits into hi = fp16(v), which never
+// overflows, and lo = v - hi, where lo' = lo 2^11 is an fp16 value as well (at
+// most 4 significant bits, on a grid no finer than 2^-17).  The split is exact
+// for every finite fp16 scale and every code difference (checked exhaustively
+// on the host).  Two fp16 GEMMs then give exact products x hi and x lo' with
+// fp32 sums: y = 16 (D_hi + 2^-11 D_lo), the factor 16 exact.  No per-block
+// scaling is needed, so both accumulators stay in TMEM across the whole K
+// loop.  (Without the 1/16, hi = fp16((q - zp) s) would overflow for scales
+// above 4367, where the exact sum may still be finite.)
 //
 // Tile.  A CTA computes 128 weight rows x 32, 64, 128 or 256 activation rows
 // (UMMA M = 128, N = the same) in K steps of 64, through two rings of stage
@@ -219,8 +223,9 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
-// hi = fp16(d s) and lo' = (d s - hi) 2^11, both exact fp16, for one pair.
-// For |s| <= 2 (so |hi| <= 30 and both s 2^11 and hi 2^11 stay finite) one packed fp16 FMA
+// hi = fp16(d s) and lo' = (d s - hi) 2^11, both exact fp16, for one pair
+// (d = (q - zp) / 16, so |d s| < 65504).
+// For |s| <= 2 (so |hi| <= 2 and both s 2^11 and hi 2^11 stay finite) one packed fp16 FMA
 // forms lo' exactly: its exact value has at most 4 significant bits and is
 // no larger than |hi 2^11|, so the single rounding leaves it unchanged.
 // Larger scales take the fp32 form.
@@ -389,16 +394,19 @@ __global__ void __launch_bounds__(kThreads + 64, kThreads == 256 ? 2 : 1)
       const bool small = fabsf(cur.s) <= 2.f;
       const __half shk = __float2half_rn(small ? cur.s * 2048.f : 0.f);   // exact when small
       const uint32_t s2k = static_cast<uint32_t>(__half_as_ushort(shk)) * 0x00010001u;
-      const uint32_t zl = cur.z * 0x00010001u + 0x64006400u;
-      const uint32_t zh = cur.z * 0x00100010u + 0x54005400u;
-      // exact q - zp of pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7) of word g,
-      // regrouped into natural k order (k0,k1) (k2,k3) (k4,k5) (k6,k7)
+      // (q - zp) / 16, exact: low nibbles OR-ed under 64 (ulp 1/16) read as
+      // 64 + q / 16, high nibbles under 4 (ulp 1/256) as 4 + q / 16; subtracting
+      // 64 + zp / 16 or 4 + zp / 16 leaves the exact quotient
+      const uint32_t zl = cur.z * 0x00010001u + 0x54005400u;                //   64 + zp / 16
+      const uint32_t zh = cur.z * 0x00100010u + 0x44004400u;                //    4 + zp / 16
+      // exact (q - zp) / 16 of pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7) of word
+      // g, regrouped into natural k order (k0,k1) (k2,k3) (k4,k5) (k6,k7)
       auto pairs = [&](int g, uint32_t (&n)[4]) {
         const uint32_t word = cur.w[g], w8 = word >> 8;
-        const uint32_t d0 = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl);
-        const uint32_t d1 = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh);
-        const uint32_t d2 = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl);
-        const uint32_t d3 = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh);
+        const uint32_t d0 = hsub2(and_or(word, 0x000F000Fu, 0x54005400u), zl);
+        const uint32_t d1 = hsub2(and_or(word, 0x00F000F0u, 0x44004400u), zh);
+        const uint32_t d2 = hsub2(and_or(w8, 0x000F000Fu, 0x54005400u), zl);
+        const uint32_t d3 = hsub2(and_or(w8, 0x00F000F0u, 0x44004400u), zh);
         n[0] = prmt(d0, d1, 0x5410u);
         n[1] = prmt(d2, d3, 0x5410u);
         n[2] = prmt(d0, d1, 0x7632u);
@@ -537,8 +545,10 @@ __global__ void __launch_bounds__(kThreads + 64, kThreads == 256 ? 2 : 1)
       for (int j = 0; j < 32; ++j) {
         // D_hi is non-finite whenever a term is (hi is nonzero wherever w
         // is); it then holds the exact form's value (inf, or NaN for inf x 0)
-        // and D_lo, whose lo' may be 0 there, must not be added
-        const float v = fabsf(vh[j]) <= 3.402823466e38f ? fmaf(vl[j], 1.f / 2048.f, vh[j]) : vh[j];
+        // and D_lo, whose lo' may be 0 there, must not be added.  The factor
+        // 16 undoes the weights' exact 1/16.
+        const float v =
+            16.f * (fabsf(vh[j]) <= 3.402823466e38f ? fmaf(vl[j], 1.f / 2048.f, vh[j]) : vh[j]);
         if (p.ksplit > 1) {
           part[(col + j) * kTcRows + lane_base + lane] = v;
         } else {

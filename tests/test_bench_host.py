@@ -82,13 +82,15 @@ def test_default_workload_is_the_lm_head_projection():
 
 
 def test_graph_steps_give_about_ten_replays_of_whole_rotations():
-    # the full test run: 20 steps of lm-head (2 weight copies, one launch a step)
-    G = bench.graph_steps(20, 2)
-    assert G == 2 and divmod(20, G) == (10, 0)
-    assert bench.graph_steps(2000, 2) == 200
-    assert bench.graph_steps(20, 28) == 20            # one rotation is longer than K
-    assert bench.graph_steps(3, 1) == 1
-    for steps in (1, 7, 20, 99, 2000):
+    # the full test run: 20 steps of lm-head (2 weight copies, one launch a
+    # step) run as one graph; long runs as about ten replays of whole rotations
+    assert bench.graph_steps(20, 2) == 20
+    assert bench.graph_steps(200, 2) == 200
+    G = bench.graph_steps(2000, 2)
+    assert G == 200 and divmod(2000, G) == (10, 0)
+    assert bench.graph_steps(1000, 28) == 112          # four rotations of 28 steps
+    assert bench.graph_steps(3, 1) == 3
+    for steps in (1, 7, 20, 99, 201, 2000):
         for rot in (1, 2, 3, 28):
             g = bench.graph_steps(steps, rot)
             assert 1 <= g <= steps and (g % rot == 0 or g == steps)

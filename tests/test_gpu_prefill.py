@@ -133,6 +133,33 @@ def test_exact_zero_rows():
 
 
 @pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
+@pytest.mark.parametrize("M,N,K,block,symmetric", [
+    (20, 96, 256, 32, False), (130, 300, 512, 64, True), (40, 200, 1024, 128, False),
+])
+def test_large_scales_stay_finite(M, N, K, block, symmetric, tc):
+    """Scales of 8192 and 30000 (so (q - zp) s lies far outside the fp16
+    range) with small activations (|x| <= 2^-9): the exact sums are finite,
+    and both forms must give them within the bound, every element."""
+    inp = make_inputs(M, N, K, seed=31 + M, block=block)
+    rng = np.random.default_rng(31 + M)
+    inp.x = rng.uniform(-2.0 ** -9, 2.0 ** -9, size=(M, K)).astype(np.float16).view(np.uint16)
+    sc = np.empty((N, K // block), dtype=np.float32)
+    sc[0::2] = 8192.0
+    sc[1::2] = 30000.0
+    sc[(np.arange(N) % 5 == 0)] *= -1.0
+    inp.scales[...] = sc.astype(np.float16).view(np.uint16)
+    ref = _gpu.oracle().gemv(inp.x, inp.qweight, inp.scales, None if symmetric else inp.zp,
+                             M, N, K, block=block)
+    r = _gpu.oracle().f16_to_f64(ref["y_f16"])
+    assert np.isfinite(r).all() and (np.abs(r) > 65504 / 15).mean() > 0.01
+    _run_both(inp, symmetric, tc=tc)
+    dev = _gpu.to_device(inp, symmetric=symmetric)
+    y = _gpu.oracle().f16_to_f64(_gpu.bits(_gpu.run(dev, "f16", 0, block=block,
+                                                    prefill_mma_sync=not tc)))
+    assert np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
 def test_non_finite_inputs_follow_ieee(tc):
     """+inf meeting nonzero weights gives the exact form's +-inf (the tcgen05
     form must not add its low part, whose lo' is often 0 there); +inf meeting

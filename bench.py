@@ -147,7 +147,11 @@ def measured_peaks():
 
 KERNEL_SOURCES = ("int4_block_quantized_mnb_gb300/csrc/mnb_gemv.cu",
                   "int4_block_quantized_mnb_gb300/csrc/mnb_dequant.cuh",
-                  "int4_block_quantized_mnb_gb300/csrc/mnb_narrow.cuh")
+                  "int4_block_quantized_mnb_gb300/csrc/mnb_narrow.cuh",
+                  "int4_block_quantized_mnb_gb300/csrc/mnb_general.cu",
+                  "int4_block_quantized_mnb_gb300/csrc/mnb_prefill.cu",
+                  "int4_block_quantized_mnb_gb300/csrc/mnb_prefill_tc.cu",
+                  "int4_block_quantized_mnb_gb300/csrc/mnb_launch.cuh")
 
 
 def kernel_source_hash():
@@ -820,7 +824,8 @@ def main():
                       "peak_datasheet": DATASHEET_HBM_GBS,
                       "frac_datasheet": achieved / DATASHEET_HBM_GBS,
                       "fma_bound": fma_bound(w, props, clk) if w.M > 1 else None}
-                     if w.M <= 8 else tensor_roofline(w, per_launch_s, achieved, peak)),
+                     if w.M <= 8 else dict(tensor_roofline(w, per_launch_s, achieved, peak),
+                                           traffic=recorded_traffic(w.name))),
         "launch": info,
         "cpu_baseline": cpu,
         "e2e": e2e,

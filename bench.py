@@ -825,7 +825,8 @@ def main():
                       "frac_datasheet": achieved / DATASHEET_HBM_GBS,
                       "fma_bound": fma_bound(w, props, clk) if w.M > 1 else None}
                      if w.M <= 8 else dict(tensor_roofline(w, per_launch_s, achieved, peak),
-                                           traffic=recorded_traffic(w.name))),
+                                           traffic=recorded_traffic(
+                                               w.name + ("+mma-sync" if pm else "")))),
         "launch": info,
         "cpu_baseline": cpu,
         "e2e": e2e,

@@ -36,8 +36,9 @@ def link_command(objs: list, out: str) -> list:
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile libmnb.so unless it is newer than every source and header; the
     translation units compile in parallel, then link."""
-    deps = SOURCES + [os.path.join(INCLUDE, "mnb.h"), os.path.join(PKG, "csrc", "mnb_narrow.cuh"),
-                      os.path.join(PKG, "csrc", "mnb_dequant.cuh")]
+    csrc = os.path.join(PKG, "csrc")
+    deps = SOURCES + [os.path.join(INCLUDE, "mnb.h")] + \
+        [os.path.join(csrc, f) for f in sorted(os.listdir(csrc)) if f.endswith(".cuh")]
     if not force and os.path.exists(LIBRARY) and \
             all(os.path.getmtime(LIBRARY) >= os.path.getmtime(d) for d in deps):
         return LIBRARY

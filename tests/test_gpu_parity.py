@@ -132,8 +132,9 @@ def test_mixed_shape_chain_matches_plain_calls():
 def test_step_kernel_takes_default_launches():
     """Without a K split, with K a multiple of 1024 and activations that fit,
     launches run the step kernel (TMA tensor copies, CUDA-core math: four rows
-    per lane for M <= 3, two rows per lane for M >= 4); other launches run the
-    row-tile kernel.  No default launch uses tensor-core math."""
+    per lane for M = 2 and 3, two rows per lane for M = 1 and M >= 4); other
+    launches run the row-tile kernel.  No default launch uses tensor-core
+    math."""
     for M, N, K, split, want in ((1, 4096, 4096, 0, 1), (2, 300, 8192, 1, 1), (4, 130, 4096, 0, 1),
                                  (3, 77, 1024, 1, 1), (5, 130, 4096, 0, 1), (8, 300, 8192, 0, 1),
                                  (7, 40, 2048, 1, 1), (2, 130, 4096, 2, 0), (1, 75, 288, 0, 0)):
@@ -147,6 +148,27 @@ def test_step_kernel_takes_default_launches():
         assert c1[12] == c0[12]
         if want:
             assert mnb.split_k_auto(M, N, K) == 1
+            layout = "four rows per lane" if M in (2, 3) else "two rows per lane"
+            assert layout in mnb.launch_info(M, N, K, split_k=split)["kernel"], (M, N, K)
+        _gpu.compare(inp, y16, ybf)
+
+
+@pytest.mark.parametrize("M,K_fit", [(1, 55296), (2, 30720), (3, 20480), (5, 12288), (8, 8192)])
+def test_step_kernel_activation_limit(M, K_fit):
+    """Staged activations take K/32 * (64 M + 16) bytes of shared memory, at
+    most 136 KiB: the largest K (a multiple of 1024) that fits runs the step
+    kernel, with its fewest stages and reduction slots, and the next one runs
+    the row-tile kernel.  Every element of both against the oracle."""
+    assert K_fit // 32 * (64 * M + 16) <= 136 * 1024 < (K_fit + 1024) // 32 * (64 * M + 16)
+    for K, step in ((K_fit, True), (K_fit + 1024, False)):
+        N = 300
+        assert ("step kernel" in mnb.launch_info(M, N, K)["kernel"]) == step, (M, K)
+        inp = make_inputs(M, N, K, seed=M + K)
+        dev = _gpu.to_device(inp)
+        c0 = mnb.counters()[13]
+        y16 = _gpu.bits(_gpu.run(dev, "f16"))
+        ybf = _gpu.bits(_gpu.run(dev, "bf16"))
+        assert mnb.counters()[13] - c0 == (2 if step else 0), (M, K)
         _gpu.compare(inp, y16, ybf)
 
 

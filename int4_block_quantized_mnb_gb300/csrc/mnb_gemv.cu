@@ -265,6 +265,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return mbar_wait_slow(bar, parity, abort_flag, code);
 }
 
+// A wait with slack: polls with a pause of about `pause_ns` between polls, so
+// the waiting warp leaves its sub-partition's issue slots to the consumer
+// warps; bounded like mbar_wait.
+__device__ __noinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            unsigned code, unsigned pause_ns) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(&g_device_error, 0u, code);
+      return false;
+    }
+    __nanosleep(pause_ns);
+  }
+  return true;
+}
+
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar) {
   asm volatile(
@@ -507,6 +525,9 @@ __device__ __forceinline__ void run_producer(const Params& p, unsigned char* sme
 // stores them (or keeps them for the cluster reduction), then frees the slot.
 // Tile i belongs to group i % groups, its (i / groups)-th tile; each group has
 // `nslots` reduction slots.
+// Pause between the epilogue warp's polls before its last tile (0: none).
+constexpr unsigned kEpiloguePauseNs = 0;
+
 __device__ __forceinline__ void run_epilogue(const Params& p, const float* red, float* part,
                                              uint32_t ready0, uint32_t free0,
                                              volatile int* abort_flag, int row_begin,
@@ -517,7 +538,14 @@ __device__ __forceinline__ void run_epilogue(const Params& p, const float* red, 
   int g = 0, t = 0;
   for (int i = 0; i < ntiles; ++i) {
     const int j = g * nslots + t % nslots;
-    if (!mbar_wait(ready0 + 8u * j, (t / nslots) & 1, abort_flag, kErrReduceSlot)) break;
+    // Before the CTA's last tile the epilogue has slack (the slot is needed
+    // again only nslots tiles later): it pauses between polls instead of
+    // taking issue slots from the consumers on its sub-partition.
+    const bool waited = kEpiloguePauseNs > 0 && i + 1 < ntiles
+                            ? mbar_wait_idle(ready0 + 8u * j, (t / nslots) & 1, abort_flag,
+                                             kErrReduceSlot, kEpiloguePauseNs)
+                            : mbar_wait(ready0 + 8u * j, (t / nslots) & 1, abort_flag, kErrReduceSlot);
+    if (!waited) break;
     const int r0 = row_begin + i * RC;
     const int vals = min(RC, row_end - r0) * M;
     const float* slot = red + static_cast<size_t>(j) * p.wpg * vals_tile;
@@ -887,6 +915,14 @@ __device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Weight stages the step kernel's producer keeps in flight until the
+// consumers have staged the activations; afterwards the ring alone bounds it.
+// The activation loads, issued when the dependency wait returns, then queue
+// behind at most two stages of weights instead of a whole ring (gate-up
+// 18.1 -> 17.5 us, M = 2 14.3 -> 13.4 us; one stage in flight starves the
+// stream: lm-head 62 -> 72 us).
+constexpr int kMaxInflight = 2;
+
 // Producer of the step kernel (one thread): one stage per (tile, part), three
 // tensor copies completing on the stage's mbarrier.
 __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* smem,
@@ -902,12 +938,23 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
   const int R = kMmaRows * p.tr;
   int issued = 0, s = 0, step = 0, tile = t_begin;
   uint32_t ph = 0;
+  int sl = 0;                       // stage of unit i - kMaxInflight, and its phase
+  uint32_t phl = 0;
   for (int i = 0; i < nunits; ++i) {
     // the producer sleeps in the barrier until the stage is released (4 us
     // at most per call) so it refills the stage as soon as it is free
     if (i >= p.stages && !mbar_try_wait_for(empty0 + 8u * s, ph ^ 1u, 4000u) &&
         !mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, kErrStageFree))
       break;
+    if (kMaxInflight < p.stages && i >= kMaxInflight && abort_flag[1] == 0) {
+      // unit i - kMaxInflight must have landed; its stage is refilled only at
+      // unit i - kMaxInflight + stages > i, so the parity wait cannot alias
+      if (!mbar_wait(full0 + 8u * sl, phl, abort_flag, kErrStageData)) break;
+      if (++sl == p.stages) {
+        sl = 0;
+        phl ^= 1u;
+      }
+    }
     const uint32_t st = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes);
     const uint32_t bar = full0 + 8u * s;
     const int row0 = tile * R;
@@ -990,6 +1037,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       mbar_init(free0 + 8u * j, 1);
     }
     *abort_flag = 0;
+    abort_flag[1] = 0;                                   // activations staged
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -1021,23 +1069,40 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   // compile time, and the 16-byte pad puts the 8 blocks a quarter warp reads
   // at once (four rows per lane) or the 4 blocks a warp reads (two rows per
   // lane) in different bank groups).
-  wait_prerequisites();
+  // Each math's consumers compute their lane constants first and then stage
+  // the activations: the constants' parameter loads overlap the dependency
+  // wait instead of following the staging barrier.
   unsigned char* xp = smem + p.xp_offset;
   auto x_at = [&](int m, int rem) {
     return kMath == kMathMma ? m * p.xp_pitch + rem * 16
                              : (rem >> 2) * (64 * M + 16) + ((rem & 3) * M + m) * 16;
   };
-  {
+  auto stage_activations = [&]() {
+    wait_prerequisites();
     // 8 activations (one k group of a block) per element; K is a multiple of
     // 1024, so every row starts 16-byte aligned when x does.
     const int per_row = p.C * 4;
     if ((reinterpret_cast<uintptr_t>(p.x) & 15u) == 0) {
-      for (int m = 0; m < M; ++m)
-        for (int rem = threadIdx.x; rem < per_row; rem += W * 32) {
-          const uint4 v =
-              __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K) + rem);
-          *reinterpret_cast<uint4*>(xp + x_at(m, rem)) = pair_k4(v);
+      // The rows are contiguous: element e is row e / per_row.  A thread
+      // issues up to four loads before its first store, so the vector
+      // arrives in one round trip behind the weight stream, not several.
+      const uint4* xg = reinterpret_cast<const uint4*>(p.x);
+      const int total = M * per_row;
+      const int nthr = W * 32;
+      for (int e0 = threadIdx.x; e0 < total; e0 += 4 * nthr) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (e0 + u * nthr < total) v[u] = __ldg(xg + e0 + u * nthr);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = e0 + u * nthr;
+          if (e < total) {
+            const int m = M == 1 ? 0 : e / per_row;
+            *reinterpret_cast<uint4*>(xp + x_at(m, e - m * per_row)) = pair_k4(v[u]);
+          }
         }
+      }
     } else {
       for (int m = 0; m < M; ++m)
         for (int rem = threadIdx.x; rem < per_row; rem += W * 32) {
@@ -1062,7 +1127,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     // all consumer warps (named barrier 1; producer and epilogue do not take part)
     asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
-  }
+    if (threadIdx.x == 0) abort_flag[1] = 1;
+  };
   if constexpr (kMath == kMathMma) {
     const int gq = lane >> 2;                               // fragment row group
     const int tq = lane & 3;                                // fragment k group
@@ -1081,6 +1147,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int sc_hi = 8 * p.sc_sb * 16;                      // row row_l + 8
     const int zp_lane = p.zp_offset + row_l * p.zp_zb * 16;
     const int zp_hi = 8 * p.zp_zb * 16;
+    stage_activations();
 
     int s = 0;                                               // stage of the next unit
     uint32_t ph = 0;
@@ -1178,6 +1245,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     constexpr uint32_t kXBlock = 64 * M + 16;            // bytes per activation block
     const uint32_t x_lane = smem_u32(xp) + (8 * ks + j) * kXBlock;   // block 8 ks + j of step 0
     const uint32_t x_step = wk * 8 * kXBlock;
+    stage_activations();
     uint32_t sb = ring0, fb = full0, eb = empty0;         // stage s: data, full and empty barriers
     int s = 0;
     uint32_t ph = 0;
@@ -1316,6 +1384,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int wk = p.wk;
     const uint32_t x_lane = smem_u32(xp) + (8 * ks + 2 * q) * kXBlock;     // block 8 ks + 2 q
     const uint32_t x_step = wk * 8 * kXBlock;
+    stage_activations();
     uint32_t sb = ring0, fb = full0, eb = empty0;
     int s = 0;
     uint32_t ph = 0;

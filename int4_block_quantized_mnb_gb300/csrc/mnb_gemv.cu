@@ -265,24 +265,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return mbar_wait_slow(bar, parity, abort_flag, code);
 }
 
-// A wait with slack: polls with a pause of about `pause_ns` between polls, so
-// the waiting warp leaves its sub-partition's issue slots to the consumer
-// warps; bounded like mbar_wait.
-__device__ __noinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                            unsigned code, unsigned pause_ns) {
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      atomicCAS(&g_device_error, 0u, code);
-      return false;
-    }
-    __nanosleep(pause_ns);
-  }
-  return true;
-}
-
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar) {
   asm volatile(
@@ -525,9 +507,6 @@ __device__ __forceinline__ void run_producer(const Params& p, unsigned char* sme
 // stores them (or keeps them for the cluster reduction), then frees the slot.
 // Tile i belongs to group i % groups, its (i / groups)-th tile; each group has
 // `nslots` reduction slots.
-// Pause between the epilogue warp's polls before its last tile (0: none).
-constexpr unsigned kEpiloguePauseNs = 0;
-
 __device__ __forceinline__ void run_epilogue(const Params& p, const float* red, float* part,
                                              uint32_t ready0, uint32_t free0,
                                              volatile int* abort_flag, int row_begin,
@@ -538,14 +517,7 @@ __device__ __forceinline__ void run_epilogue(const Params& p, const float* red, 
   int g = 0, t = 0;
   for (int i = 0; i < ntiles; ++i) {
     const int j = g * nslots + t % nslots;
-    // Before the CTA's last tile the epilogue has slack (the slot is needed
-    // again only nslots tiles later): it pauses between polls instead of
-    // taking issue slots from the consumers on its sub-partition.
-    const bool waited = kEpiloguePauseNs > 0 && i + 1 < ntiles
-                            ? mbar_wait_idle(ready0 + 8u * j, (t / nslots) & 1, abort_flag,
-                                             kErrReduceSlot, kEpiloguePauseNs)
-                            : mbar_wait(ready0 + 8u * j, (t / nslots) & 1, abort_flag, kErrReduceSlot);
-    if (!waited) break;
+    if (!mbar_wait(ready0 + 8u * j, (t / nslots) & 1, abort_flag, kErrReduceSlot)) break;
     const int r0 = row_begin + i * RC;
     const int vals = min(RC, row_end - r0) * M;
     const float* slot = red + static_cast<size_t>(j) * p.wpg * vals_tile;

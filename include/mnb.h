@@ -100,10 +100,13 @@ typedef enum mnb_status {
  *   block    16, 32 (MNB_BLOCK), 64 or 128.  Block 32 with zero-points runs
  *            the kernels tuned for it, and so does block 32 without them
  *            where the TMA step kernel applies (constant zero-points of 8 in
- *            its stages); the other formats run one CUDA-core kernel of the
- *            same exact arithmetic, where split_k (0 = chosen by the
- *            library) is the number of warps that split each row's K range
- *            inside one CTA, at most 8.
+ *            its stages).  At M = 1 the step kernel also takes blocks 16, 64
+ *            and 128 where it applies (split_k 0 or 1, K a multiple of 1024
+ *            and, with zero-points, of 32 * block, so each zero-point row is
+ *            whole 16-byte chunks).  Elsewhere the other formats run one
+ *            CUDA-core kernel of the same exact arithmetic, where split_k
+ *            (0 = chosen by the library) is the number of warps that split
+ *            each row's K range inside one CTA, at most 8.
  *   out_dtype  an mnb_out_dtype.  It changes only the final store: for the
  *            same inputs and split_k the bf16 result equals the
  *            round-to-nearest-even bf16 narrowing of the fp16 result, bit
@@ -196,9 +199,8 @@ int mnb_cast_f16_to_bf16(const void *src, void *dst, size_t n, void *stream);
 /* split_k that mnb_gemv uses for split_k = 0 on the current device, for
  * 16-byte aligned scales and zp and without MNB_FLAG_TENSOR_CORES (1 whenever
  * the step kernel takes the launch: K a multiple of 1024 and staged
- * activations M * (2K + 64) bytes at most 66 KiB for M <= 3, 136 KiB for
- * M >= 4).  Writes it to *split_k.  Same shape checks and statuses as
- * mnb_gemv. */
+ * activations (K / 32) * (64 M + 16) bytes at most 136 KiB).  Writes it to
+ * *split_k.  Same shape checks and statuses as mnb_gemv. */
 int mnb_split_k_auto(int M, int N, int K, int *split_k);
 
 /* Smallest split_k mnb_gemv accepts for this M and K (one CTA covers at most

@@ -128,6 +128,7 @@ struct Params {
   int xp_offset;    // offset of the step kernel's staged activations
   int xp_pitch;     // bytes per activation row of those fragments
   int flag_offset;  // offset of the CTA abort flag
+  int blk;          // weights per quantization block (step kernel)
 };
 
 // ---------------------------------------------------------------- PTX glue --
@@ -225,6 +226,11 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
 __device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
   return v;
 }
 
@@ -897,6 +903,7 @@ constexpr int kMaxInflight = 2;
 
 // Producer of the step kernel (one thread): one stage per (tile, part), three
 // tensor copies completing on the stage's mbarrier.
+template <int kB>
 __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* smem,
                                                 uint32_t full0, uint32_t empty0,
                                                 volatile int* abort_flag, int t_begin,
@@ -934,8 +941,16 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.tx_bytes));
     tma_load_3d(st, tm_q, 0, row0, seg0, bar);
-    tma_load_3d(st + p.sc_offset, tm_sc, 0, seg0, row0, bar);
-    if (p.zp) tma_load_3d(st + p.zp_offset, tm_zp, 0, seg0 >> 2, row0, bar);
+    if constexpr (kB == 32) {
+      tma_load_3d(st + p.sc_offset, tm_sc, 0, seg0, row0, bar);
+      if (p.zp) tma_load_3d(st + p.zp_offset, tm_zp, 0, seg0 >> 2, row0, bar);
+    } else {
+      // the boxes start at the 8-scale and 32-block zero-point chunks holding
+      // the stage's first quantization block
+      const int bs0 = seg0 * (kMmaSeg / kB);
+      tma_load_3d(st + p.sc_offset, tm_sc, 0, bs0 >> 3, row0, bar);
+      if (p.zp) tma_load_3d(st + p.zp_offset, tm_zp, 0, bs0 >> 5, row0, bar);
+    }
     issued = i + 1;
     if (++step == p.steps) {
       step = 0;
@@ -967,7 +982,7 @@ enum StepMath : int { kMathFma = 0, kMathWide = 1, kMathMma = 2 };
 
 namespace {
 
-template <int M, int kMath>
+template <int M, int kMath, int kB = 32>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     mnb_gemv_step_kernel(const Params p, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_sc,
@@ -1017,7 +1032,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   if (warp == producer_warp) {
     if (lane == 0)
-      run_tc_producer(p, smem, full0, empty0, abort_flag, t_begin, ntiles * p.steps, &tm_q,
+      run_tc_producer<kB>(p, smem, full0, empty0, abort_flag, t_begin, ntiles * p.steps, &tm_q,
                       &tm_sc, &tm_zp);
     __syncwarp();
     return;
@@ -1050,6 +1065,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                              : (rem >> 2) * (64 * M + 16) + ((rem & 3) * M + m) * 16;
   };
   auto stage_activations = [&]() {
+    if (p.zp == nullptr) {
+      // symmetric format: the producer copies no zero-points; every stage's
+      // zero-point bytes hold 0x88 (zero-point 8 in both nibbles) for the
+      // whole launch, written before the dependency wait (they depend on no
+      // earlier grid) and before the barrier below, so before any consumer
+      // reads a stage
+      for (int s = 0; s < p.stages; ++s)
+        for (int i = threadIdx.x; i < p.zp_bytes / 16; i += W * 32)
+          *reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes + p.zp_offset +
+                                    16 * i) = make_uint4(0x88888888u, 0x88888888u, 0x88888888u,
+                                                         0x88888888u);
+    }
     wait_prerequisites();
     // 8 activations (one k group of a block) per element; K is a multiple of
     // 1024, so every row starts 16-byte aligned when x does.
@@ -1086,16 +1113,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           v.w = __ldg(src + 6) | (static_cast<uint32_t>(__ldg(src + 7)) << 16);
           *reinterpret_cast<uint4*>(xp + x_at(m, rem)) = pair_k4(v);
         }
-    }
-    if (p.zp == nullptr) {
-      // symmetric format: the producer copies no zero-points; every stage's
-      // zero-point bytes hold 0x88 (zero-point 8 in both nibbles) for the
-      // whole launch, written here before any consumer reads a stage
-      for (int s = 0; s < p.stages; ++s)
-        for (int i = threadIdx.x; i < p.zp_bytes / 16; i += W * 32)
-          *reinterpret_cast<uint4*>(smem + static_cast<size_t>(s) * p.stage_bytes + p.zp_offset +
-                                    16 * i) = make_uint4(0x88888888u, 0x88888888u, 0x88888888u,
-                                                         0x88888888u);
     }
     // all consumer warps (named barrier 1; producer and epilogue do not take part)
     asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
@@ -1330,155 +1347,346 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       if (lane == 0) mbar_arrive(ready0 + 8u * js);
     }
   } else {
-    // CUDA-core math for larger M.  Lane (q, rr) = (lane >> 3, lane & 7) takes
-    // rows 16 rho + rr and 16 rho + rr + 8 and the block pair (2q, 2q + 1) of
-    // the warp's segment of every stage.  An activation load (16 bytes of one
-    // 8-k group, shared by the eight lanes of a quarter warp) feeds both rows,
-    // which balances shared-memory bandwidth against the FMA pipe; a lane holds
-    // 2M accumulators, 2M block sums and one group's 4M activation registers.
-    // Activation offsets inside a block are compile-time constants; only the
-    // block base moves (by W_k segments a step).
-    const int rr = lane & 7;
-    const int q = lane >> 3;
-    const int r0 = rho * kMmaRows + rr;                  // rows r0 and r0 + 8 (both rr mod 8)
-    // block 2q + e of row r0; row r0 + 8 is 1024 bytes on
-    const uint32_t q_lane0 = (R * ks + r0) * 128 + 16 * ((2 * q) ^ rr);
-    const uint32_t q_lane1 = (R * ks + r0) * 128 + 16 * ((2 * q + 1) ^ rr);
-    const uint32_t sc_lane = p.sc_offset + (r0 * p.sc_sb + ks) * 16 + 4 * q;   // scales of the pair
-    const uint32_t sc_row8 = 8 * p.sc_sb * 16;
-    const uint32_t zp_lane = p.zp_offset + r0 * p.zp_zb * 16 + q;            // its zero-point byte
-    const uint32_t zp_row8 = 8 * p.zp_zb * 16;
-    constexpr uint32_t kXBlock = 64 * M + 16;                            // bytes per activation block
-    const uint32_t ring0 = smem_u32(smem);
-    const uint32_t stage_bytes = p.stage_bytes;
-    const int stages = p.stages;
-    const int steps = p.steps;
-    const int wk = p.wk;
-    const uint32_t x_lane = smem_u32(xp) + (8 * ks + 2 * q) * kXBlock;     // block 8 ks + 2 q
-    const uint32_t x_step = wk * 8 * kXBlock;
-    stage_activations();
-    uint32_t sb = ring0, fb = full0, eb = empty0;
-    int s = 0;
-    uint32_t ph = 0;
-    bool run = true;
-    for (int t = 0; t < ntiles && run; ++t) {
-      float acc[2][M];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
-      uint32_t xa = x_lane;
-      uint32_t zr = 0;                                    // first segment of the stage, mod 4
-      for (int step = 0; step < steps; ++step) {
-        if (!mbar_wait(fb, ph, abort_flag, kErrStageData)) {
-          run = false;
-          break;
-        }
-        const uint32_t zrow = sb + zp_lane + 4 * (zr + ks);
-        uint32_t sw[2], zw[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          sw[i] = lds_u32(sb + sc_lane + i * sc_row8);
-          zw[i] = lds_u8(zrow + i * zp_row8) * 0x00010001u;   // the pair's zp byte, both halves
-        }
-        static_for<2>([&](auto ec) {                      // block 2q + e
-          constexpr int e = decltype(ec)::value;
-          // this block's codes and bias words for both rows (one block at a
-          // time keeps the wide M within the register budget)
-          const uint32_t qa = sb + (e ? q_lane1 : q_lane0);
-          uint4 w[2];
-          uint32_t zl[2], zh[2];
-          w[0] = lds_v4_at<0>(qa);
-          w[1] = lds_v4_at<1024>(qa);
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            if (e == 0) {
-              zl[i] = and_or(zw[i], 0x000F000Fu, 0x64006400u);        // 1024 + z_even
-              zh[i] = hsub2(zl[i], 0x63806380u);                       //   64 + z_even
-            } else {
-              zh[i] = and_or(zw[i], 0x00F000F0u, 0x54005400u);        //   64 + z_odd
-              zl[i] = hadd2(zh[i], 0x63806380u);                       // 1024 + z_odd
-            }
-          }
-          float bs[2][M];
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int m = 0; m < M; ++m) bs[i][m] = 0.f;
-          static_for<4>([&](auto gc) {
-            constexpr int g = decltype(gc)::value;
-            // both rows' q - zp pairs of this 8-k group, then one activation
-            // row at a time
-            uint32_t d[2][4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const uint4 wv = w[i];
-              const uint32_t word = g == 0 ? wv.x : g == 1 ? wv.y : g == 2 ? wv.z : wv.w;
-              const uint32_t w8 = word >> 8;
-              d[i][0] = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl[i]);   // k0, k4
-              d[i][1] = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh[i]);   // k1, k5
-              d[i][2] = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl[i]);     // k2, k6
-              d[i][3] = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh[i]);     // k3, k7
-            }
-            static_for<M>([&](auto mc) {
-              constexpr int m = decltype(mc)::value;
-              const uint4 xv = lds_v4_at<e * kXBlock + (g * M + m) * 16>(xa);
-#pragma unroll
-              for (int i = 0; i < 2; ++i) {
-                bs[i][m] = fma2_f16_f32(xv.x, d[i][0], bs[i][m]);
-                bs[i][m] = fma2_f16_f32(xv.y, d[i][1], bs[i][m]);
-                bs[i][m] = fma2_f16_f32(xv.z, d[i][2], bs[i][m]);
-                bs[i][m] = fma2_f16_f32(xv.w, d[i][3], bs[i][m]);
-              }
-            });
-          });
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const float sc = half_word_to_float(sw[i], e);
-#pragma unroll
-            for (int m = 0; m < M; ++m) acc[i][m] = fmaf(bs[i][m], sc, acc[i][m]);
-          }
-        });
-        __syncwarp();
-        if (lane == 0) mbar_arrive(eb);
-        if (++s == stages) {
-          s = 0;
-          sb = ring0;
-          fb = full0;
-          eb = empty0;
-          ph ^= 1u;
-        } else {
-          sb += stage_bytes;
-          fb += 8u;
-          eb += 8u;
-        }
-        xa += x_step;
-        zr = (zr + wk) & 3u;
-      }
-      if (!run) break;
-      // the four block pairs of each row's segment, in a fixed butterfly order
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-          float v = acc[i][m];
-          v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-          v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
-          acc[i][m] = v;
-        }
-      const int js = t % nslots;
-      if (t >= nslots && !mbar_wait(free0 + 8u * js, ((t / nslots) - 1) & 1, abort_flag,
-                                    kErrReduceSlot))
-        break;
-      if (q == 0) {
-        float* slot = red + (static_cast<size_t>(js) * p.wpg + ks) * vals;
+    if constexpr (kB == 32) {
+      // CUDA-core math for larger M.  Lane (q, rr) = (lane >> 3, lane & 7) takes
+      // rows 16 rho + rr and 16 rho + rr + 8 and the block pair (2q, 2q + 1) of
+      // the warp's segment of every stage.  An activation load (16 bytes of one
+      // 8-k group, shared by the eight lanes of a quarter warp) feeds both rows,
+      // which balances shared-memory bandwidth against the FMA pipe; a lane holds
+      // 2M accumulators, 2M block sums and one group's 4M activation registers.
+      // Activation offsets inside a block are compile-time constants; only the
+      // block base moves (by W_k segments a step).
+      const int rr = lane & 7;
+      const int q = lane >> 3;
+      const int r0 = rho * kMmaRows + rr;                  // rows r0 and r0 + 8 (both rr mod 8)
+      // block 2q + e of row r0; row r0 + 8 is 1024 bytes on
+      const uint32_t q_lane0 = (R * ks + r0) * 128 + 16 * ((2 * q) ^ rr);
+      const uint32_t q_lane1 = (R * ks + r0) * 128 + 16 * ((2 * q + 1) ^ rr);
+      const uint32_t sc_lane = p.sc_offset + (r0 * p.sc_sb + ks) * 16 + 4 * q;   // scales of the pair
+      const uint32_t sc_row8 = 8 * p.sc_sb * 16;
+      const uint32_t zp_lane = p.zp_offset + r0 * p.zp_zb * 16 + q;            // its zero-point byte
+      const uint32_t zp_row8 = 8 * p.zp_zb * 16;
+      constexpr uint32_t kXBlock = 64 * M + 16;                            // bytes per activation block
+      const uint32_t ring0 = smem_u32(smem);
+      const uint32_t stage_bytes = p.stage_bytes;
+      const int stages = p.stages;
+      const int steps = p.steps;
+      const int wk = p.wk;
+      const uint32_t x_lane = smem_u32(xp) + (8 * ks + 2 * q) * kXBlock;     // block 8 ks + 2 q
+      const uint32_t x_step = wk * 8 * kXBlock;
+      stage_activations();
+      uint32_t sb = ring0, fb = full0, eb = empty0;
+      int s = 0;
+      uint32_t ph = 0;
+      bool run = true;
+      for (int t = 0; t < ntiles && run; ++t) {
+        float acc[2][M];
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
-          for (int m = 0; m < M; ++m) slot[(r0 + 8 * i) * M + m] = acc[i][m];
+          for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
+        uint32_t xa = x_lane;
+        uint32_t zr = 0;                                    // first segment of the stage, mod 4
+        for (int step = 0; step < steps; ++step) {
+          if (!mbar_wait(fb, ph, abort_flag, kErrStageData)) {
+            run = false;
+            break;
+          }
+          const uint32_t zrow = sb + zp_lane + 4 * (zr + ks);
+          uint32_t sw[2], zw[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            sw[i] = lds_u32(sb + sc_lane + i * sc_row8);
+            zw[i] = lds_u8(zrow + i * zp_row8) * 0x00010001u;   // the pair's zp byte, both halves
+          }
+          static_for<2>([&](auto ec) {                      // block 2q + e
+            constexpr int e = decltype(ec)::value;
+            // this block's codes and bias words for both rows (one block at a
+            // time keeps the wide M within the register budget)
+            const uint32_t qa = sb + (e ? q_lane1 : q_lane0);
+            uint4 w[2];
+            uint32_t zl[2], zh[2];
+            w[0] = lds_v4_at<0>(qa);
+            w[1] = lds_v4_at<1024>(qa);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              if (e == 0) {
+                zl[i] = and_or(zw[i], 0x000F000Fu, 0x64006400u);        // 1024 + z_even
+                zh[i] = hsub2(zl[i], 0x63806380u);                       //   64 + z_even
+              } else {
+                zh[i] = and_or(zw[i], 0x00F000F0u, 0x54005400u);        //   64 + z_odd
+                zl[i] = hadd2(zh[i], 0x63806380u);                       // 1024 + z_odd
+              }
+            }
+            float bs[2][M];
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+              for (int m = 0; m < M; ++m) bs[i][m] = 0.f;
+            static_for<4>([&](auto gc) {
+              constexpr int g = decltype(gc)::value;
+              // both rows' q - zp pairs of this 8-k group, then one activation
+              // row at a time
+              uint32_t d[2][4];
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                const uint4 wv = w[i];
+                const uint32_t word = g == 0 ? wv.x : g == 1 ? wv.y : g == 2 ? wv.z : wv.w;
+                const uint32_t w8 = word >> 8;
+                d[i][0] = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), zl[i]);   // k0, k4
+                d[i][1] = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), zh[i]);   // k1, k5
+                d[i][2] = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), zl[i]);     // k2, k6
+                d[i][3] = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), zh[i]);     // k3, k7
+              }
+              static_for<M>([&](auto mc) {
+                constexpr int m = decltype(mc)::value;
+                const uint4 xv = lds_v4_at<e * kXBlock + (g * M + m) * 16>(xa);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                  bs[i][m] = fma2_f16_f32(xv.x, d[i][0], bs[i][m]);
+                  bs[i][m] = fma2_f16_f32(xv.y, d[i][1], bs[i][m]);
+                  bs[i][m] = fma2_f16_f32(xv.z, d[i][2], bs[i][m]);
+                  bs[i][m] = fma2_f16_f32(xv.w, d[i][3], bs[i][m]);
+                }
+              });
+            });
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const float sc = half_word_to_float(sw[i], e);
+#pragma unroll
+              for (int m = 0; m < M; ++m) acc[i][m] = fmaf(bs[i][m], sc, acc[i][m]);
+            }
+          });
+          __syncwarp();
+          if (lane == 0) mbar_arrive(eb);
+          if (++s == stages) {
+            s = 0;
+            sb = ring0;
+            fb = full0;
+            eb = empty0;
+            ph ^= 1u;
+          } else {
+            sb += stage_bytes;
+            fb += 8u;
+            eb += 8u;
+          }
+          xa += x_step;
+          zr = (zr + wk) & 3u;
+        }
+        if (!run) break;
+        // the four block pairs of each row's segment, in a fixed butterfly order
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int m = 0; m < M; ++m) {
+            float v = acc[i][m];
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+            acc[i][m] = v;
+          }
+        const int js = t % nslots;
+        if (t >= nslots && !mbar_wait(free0 + 8u * js, ((t / nslots) - 1) & 1, abort_flag,
+                                      kErrReduceSlot))
+          break;
+        if (q == 0) {
+          float* slot = red + (static_cast<size_t>(js) * p.wpg + ks) * vals;
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int m = 0; m < M; ++m) slot[(r0 + 8 * i) * M + m] = acc[i][m];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ready0 + 8u * js);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ready0 + 8u * js);
+    } else {
+      // Blocks of kB = 16, 64 or 128 weights (M = 1): the lane layout of
+      // block 32 above, with a segment holding kNbs blocks and the lane's
+      // 64 k starting at block lane_blk of the warp's segment.  A stage's
+      // scale box starts at the 8-scale chunk holding its first block bs0,
+      // its zero-point box at the 32-block chunk holding it: a lane's scale
+      // sits 2 (bs0 % 8 + ks kNbs + lane_blk) bytes into its row of the box,
+      // its zero-point byte (bs0 % 32 + ks kNbs + lane_blk) / 2 bytes in.
+      // kB >= 64: one block covers both 32-k units (one sum, one scale, one
+      // nibble); kB = 16: each unit holds two blocks (words 0-1 and 2-3), so
+      // two sums, two scales and both nibbles of one zero-point byte.
+      static_assert(kB == 16 || kB == 64 || kB == 128, "block size");
+      constexpr int kNbs = 256 / kB;
+      const int rr = lane & 7;
+      const int q = lane >> 3;
+      const int r0 = rho * kMmaRows + rr;                  // rows r0 and r0 + 8
+      const int lane_blk = (64 * q) / kB;
+      const uint32_t q_lane0 = (R * ks + r0) * 128 + 16 * ((2 * q) ^ rr);
+      const uint32_t q_lane1 = (R * ks + r0) * 128 + 16 * ((2 * q + 1) ^ rr);
+      const uint32_t sc_lane = p.sc_offset + r0 * p.sc_sb * 16 + 2 * (ks * kNbs + lane_blk);
+      const uint32_t sc_row8 = 8 * p.sc_sb * 16;
+      const uint32_t zp_lane = p.zp_offset + r0 * p.zp_zb * 16 + (ks * kNbs + lane_blk) / 2;
+      const uint32_t zp_row8 = 8 * p.zp_zb * 16;
+      const uint32_t zsh = 4 * (lane_blk & 1);             // kB >= 64: the block's nibble
+      constexpr uint32_t kXBlock = 64 * M + 16;
+      const uint32_t ring0 = smem_u32(smem);
+      const uint32_t stage_bytes = p.stage_bytes;
+      const int stages = p.stages;
+      const int steps = p.steps;
+      const int wk = p.wk;
+      const uint32_t x_lane = smem_u32(xp) + (8 * ks + 2 * q) * kXBlock;
+      const uint32_t x_step = wk * 8 * kXBlock;
+      stage_activations();
+      uint32_t sb = ring0, fb = full0, eb = empty0;
+      int s = 0;
+      uint32_t ph = 0;
+      bool run = true;
+      for (int t = 0; t < ntiles && run; ++t) {
+        float acc[2][M];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
+        uint32_t xa = x_lane;
+        uint32_t bsm = 0;                                 // first block of the stage, mod 32
+        for (int step = 0; step < steps; ++step) {
+          if (!mbar_wait(fb, ph, abort_flag, kErrStageData)) {
+            run = false;
+            break;
+          }
+          const uint32_t sca = sb + sc_lane + 2 * (bsm & 7u);
+          const uint32_t zpa = sb + zp_lane + (bsm >> 1);
+          // per row: kB >= 64 one scale and the block's zero-point nibble;
+          // kB = 16 four scales (two words) and two zero-point bytes
+          uint32_t sw[2], zw[2], sw2[2], zw2[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if constexpr (kB == 16) {
+              const uint2 v = lds_v2(sca + i * sc_row8);
+              sw[i] = v.x;                                  // blocks 4q, 4q + 1
+              sw2[i] = v.y;                                 // blocks 4q + 2, 4q + 3
+              const uint32_t zz = lds_u16(zpa + i * zp_row8);
+              zw[i] = (zz & 0xFFu) * 0x00010001u;
+              zw2[i] = (zz >> 8) * 0x00010001u;
+            } else {
+              sw[i] = lds_u16(sca + i * sc_row8);
+              zw[i] = ((lds_u8(zpa + i * zp_row8) >> zsh) & 0xFu) * 0x00010001u;
+            }
+          }
+          float bsw[2][M];                                // kB >= 64: the block's sum
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int m = 0; m < M; ++m) bsw[i][m] = 0.f;
+          static_for<2>([&](auto ec) {                    // 32-k unit 2q + e
+            constexpr int e = decltype(ec)::value;
+            const uint32_t qa = sb + (e ? q_lane1 : q_lane0);
+            uint4 w[2];
+            uint32_t zl[2], zh[2], zl2[2], zh2[2];
+            w[0] = lds_v4_at<0>(qa);
+            w[1] = lds_v4_at<1024>(qa);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              if constexpr (kB == 16) {
+                const uint32_t zb = e ? zw2[i] : zw[i];
+                zl[i] = and_or(zb, 0x000F000Fu, 0x64006400u);    // first block: 1024 + z
+                zh[i] = hsub2(zl[i], 0x63806380u);                //                64 + z
+                zh2[i] = and_or(zb, 0x00F000F0u, 0x54005400u);   // second block:  64 + z
+                zl2[i] = hadd2(zh2[i], 0x63806380u);              //              1024 + z
+              } else {
+                zl[i] = zw[i] | 0x64006400u;                      // 1024 + z
+                zh[i] = hsub2(zl[i], 0x63806380u);                //   64 + z
+              }
+            }
+            float bs[2][M], bs2[2][M];                    // kB = 16: the unit's two sums
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+              for (int m = 0; m < M; ++m) bs[i][m] = bs2[i][m] = 0.f;
+            static_for<4>([&](auto gc) {
+              constexpr int g = decltype(gc)::value;
+              constexpr bool second = kB == 16 && g >= 2;
+              uint32_t d[2][4];
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                const uint4 wv = w[i];
+                const uint32_t word = g == 0 ? wv.x : g == 1 ? wv.y : g == 2 ? wv.z : wv.w;
+                const uint32_t w8 = word >> 8;
+                const uint32_t l = second ? zl2[i] : zl[i], h = second ? zh2[i] : zh[i];
+                d[i][0] = hsub2(and_or(word, 0x000F000Fu, 0x64006400u), l);   // k0, k4
+                d[i][1] = hsub2(and_or(word, 0x00F000F0u, 0x54005400u), h);   // k1, k5
+                d[i][2] = hsub2(and_or(w8, 0x000F000Fu, 0x64006400u), l);     // k2, k6
+                d[i][3] = hsub2(and_or(w8, 0x00F000F0u, 0x54005400u), h);     // k3, k7
+              }
+              static_for<M>([&](auto mc) {
+                constexpr int m = decltype(mc)::value;
+                const uint4 xv = lds_v4_at<e * kXBlock + (g * M + m) * 16>(xa);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                  float& b = kB >= 64 ? bsw[i][m] : second ? bs2[i][m] : bs[i][m];
+                  b = fma2_f16_f32(xv.x, d[i][0], b);
+                  b = fma2_f16_f32(xv.y, d[i][1], b);
+                  b = fma2_f16_f32(xv.z, d[i][2], b);
+                  b = fma2_f16_f32(xv.w, d[i][3], b);
+                }
+              });
+            });
+            if constexpr (kB == 16) {
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                const uint32_t sp = e ? sw2[i] : sw[i];
+                const float sa = half_word_to_float(sp, 0), sc2 = half_word_to_float(sp, 1);
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                  acc[i][m] = fmaf(bs[i][m], sa, acc[i][m]);
+                  acc[i][m] = fmaf(bs2[i][m], sc2, acc[i][m]);
+                }
+              }
+            }
+          });
+          if constexpr (kB >= 64) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const float sc = half_word_to_float(sw[i], 0);
+#pragma unroll
+              for (int m = 0; m < M; ++m) acc[i][m] = fmaf(bsw[i][m], sc, acc[i][m]);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(eb);
+          if (++s == stages) {
+            s = 0;
+            sb = ring0;
+            fb = full0;
+            eb = empty0;
+            ph ^= 1u;
+          } else {
+            sb += stage_bytes;
+            fb += 8u;
+            eb += 8u;
+          }
+          xa += x_step;
+          bsm = (bsm + wk * kNbs) & 31u;
+        }
+        if (!run) break;
+        // the four 64-k pieces of each row's segment, in a fixed butterfly order
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int m = 0; m < M; ++m) {
+            float v = acc[i][m];
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+            v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+            acc[i][m] = v;
+          }
+        const int js = t % nslots;
+        if (t >= nslots && !mbar_wait(free0 + 8u * js, ((t / nslots) - 1) & 1, abort_flag,
+                                      kErrReduceSlot))
+          break;
+        if (q == 0) {
+          float* slot = red + (static_cast<size_t>(js) * p.wpg + ks) * vals;
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int m = 0; m < M; ++m) slot[(r0 + 8 * i) * M + m] = acc[i][m];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ready0 + 8u * js);
+      }
     }
   }
 }
@@ -1733,6 +1941,13 @@ bool step_shape(int M, int K, bool tensor_cores) {
   return K % 1024 == 0 && K <= 65536 && step_x_bytes(M, K / kBlock, math) <= limit;
 }
 
+// Formats the step kernel takes besides block 32: blocks 16, 64 and 128 at
+// M = 1 on the CUDA-core math, where the zero-point rows (K / (2 block) bytes)
+// are whole 16-byte chunks for the tensor copies.
+bool step_takes_block(int block, int K, const void* zp) {
+  return (block == 16 || block == 64 || block == 128) && (zp == nullptr || K % (32 * block) == 0);
+}
+
 bool use_step(int M, int K, int split_k, const void* scales, const void* zp,
               bool tensor_cores) {
   return (split_k == 0 || split_k == 1) && step_shape(M, K, tensor_cores) &&
@@ -1756,7 +1971,14 @@ MmaFn step_kernel_for(int M) {
   }
 }
 
-MmaFn pick_step_kernel(int M, int math) {
+MmaFn pick_step_kernel(int M, int math, int block) {
+  if (block != kBlock) {  // M = 1, CUDA-core math (step_takes_block)
+    switch (block) {
+      case 16: return &mnb_gemv_step_kernel<1, kMathWide, 16>;
+      case 64: return &mnb_gemv_step_kernel<1, kMathWide, 64>;
+      default: return &mnb_gemv_step_kernel<1, kMathWide, 128>;
+    }
+  }
   if (math == kMathMma) return step_kernel_for<kMathMma>(M);
   if (math == kMathWide) return step_kernel_for<kMathWide>(M);
   switch (M) {            // four rows per lane: kStepFmaMinM <= M <= kStepFmaMaxM
@@ -1773,8 +1995,9 @@ int odd_at_least(int v) { return v | 1; }
 // the best and that keeps as many SMs busy; K slices: the largest divisor of
 // K / 256 up to 16 / tr (at least 4 where K allows, so a stage's zero-point
 // chunk is never re-read).  A stage always holds about 32 KB of codes.
-int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, int math, Plan* plan) {
+int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, int math, int block, Plan* plan) {
   Params& p = plan->p;
+  p.blk = block;
   p.M = M;
   p.N = N;
   p.K = K;
@@ -1807,15 +2030,20 @@ int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, int math, Plan* pl
   int wk = std::min(kMmaWarps / tr, S);
   while (S % wk) --wk;
   const int R = kMmaRows * tr;
-  int zspan = 1;                                   // zero-point chunks one stage spans
-  for (int st = 0; st < S / wk; ++st)
-    zspan = std::max(zspan, (((st + 1) * wk - 1) >> 2) - ((st * wk) >> 2) + 1);
+  // 8-scale and 32-block zero-point chunks one stage spans
+  const int nbs = kMmaSeg / block;
+  int sspan = 1, zspan = 1;
+  for (int st = 0; st < S / wk; ++st) {
+    const int b0 = st * wk * nbs, b1 = (st + 1) * wk * nbs - 1;
+    sspan = std::max(sspan, (b1 >> 3) - (b0 >> 3) + 1);
+    zspan = std::max(zspan, (b1 >> 5) - (b0 >> 5) + 1);
+  }
   p.tr = tr;
   p.wk = wk;
   p.steps = S / wk;
   p.wtc = wk * tr;
   p.wpg = wk;                                      // partials per output for the epilogue
-  p.sc_sb = odd_at_least(wk);
+  p.sc_sb = odd_at_least(sspan);
   p.zp_zb = odd_at_least(zspan);
   p.q_bytes = R * wk * 128;
   p.sc_bytes = round_up(R * p.sc_sb * 16, 128);
@@ -1867,7 +2095,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 
 struct MapEntry {
   const void* ptr = nullptr;
-  int kind = -1, N = 0, K = 0, tr = 0, wk = 0;
+  int kind = -1, N = 0, K = 0, tr = 0, wk = 0, blk = 0;
   CUtensorMap map;
 };
 
@@ -1895,18 +2123,21 @@ int encode_map(MapKind kind, const void* ptr, const Params& p, CUtensorMap* out)
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else if (kind == kMapScales) {
-    // (scale in 8-scale chunk, chunk, row)
-    const cuuint64_t dims[3] = {8, K / 256, N};
-    const cuuint64_t strides[2] = {16, K / 16};
+    // (scale in 8-scale chunk, chunk, row): rows 2 K / blk bytes apart
+    const cuuint64_t B = static_cast<cuuint64_t>(p.blk);
+    const cuuint64_t dims[3] = {8, K / (8 * B), N};
+    const cuuint64_t strides[2] = {16, 2 * K / B};
     const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(p.sc_sb),
                                static_cast<cuuint32_t>(kMmaRows * p.tr)};
     r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, base, dims, strides, box, ones,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
-    // (byte in 16-byte chunk, chunk, row)
-    const cuuint64_t dims[3] = {16, K / 1024, N};
-    const cuuint64_t strides[2] = {16, K / 64};
+    // (byte in 16-byte chunk, chunk, row): rows K / (2 blk) bytes apart, a
+    // multiple of 16 where the step kernel takes the format
+    const cuuint64_t B = static_cast<cuuint64_t>(p.blk);
+    const cuuint64_t dims[3] = {16, K / (32 * B), N};
+    const cuuint64_t strides[2] = {16, K / (2 * B)};
     const cuuint32_t box[3] = {16, static_cast<cuuint32_t>(p.zp_zb),
                                static_cast<cuuint32_t>(kMmaRows * p.tr)};
     r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, ones,
@@ -1931,7 +2162,7 @@ int tensor_map(MapKind kind, const void* ptr, const Params& p, CUtensorMap* out)
   }
   for (const MapEntry& m : g_maps)
     if (m.ptr == ptr && m.kind == kind && m.N == p.N && m.K == p.K && m.tr == p.tr &&
-        m.wk == p.wk) {
+        m.wk == p.wk && m.blk == p.blk) {
       *out = m.map;
       return MNB_OK;
     }
@@ -1947,6 +2178,7 @@ int tensor_map(MapKind kind, const void* ptr, const Params& p, CUtensorMap* out)
   slot.K = p.K;
   slot.tr = p.tr;
   slot.wk = p.wk;
+  slot.blk = p.blk;
   g_map_next = (g_map_next + 1) % kMapCache;
   *out = slot.map;
   return MNB_OK;
@@ -2041,17 +2273,18 @@ int dispatch(const void* x, const uint8_t* qweight, const void* scales, const ui
   if ((st = device_info(&dev)) != MNB_OK) return st;
   const bool tc = (flags & MNB_FLAG_TENSOR_CORES) != 0;
   const int math = step_math(M, tc);
-  bool step = block == kBlock && use_step(M, K, split_k, scales, zp, tc);
+  const bool step_format = block == kBlock || (M == 1 && !tc && step_takes_block(block, K, zp));
+  bool step = step_format && use_step(M, K, split_k, scales, zp, tc);
   Plan plan{};
-  if (step && make_mma_plan(dev, M, N, K, math, &plan) != MNB_OK) {
+  if (step && make_mma_plan(dev, M, N, K, math, block, &plan) != MNB_OK) {
     step = false;                                 // no stage layout fits: row-tile kernel
     plan = Plan{};
   }
-  // block 32 without zero-points runs the step kernel where it applies (its
-  // stages then hold constant zero-points of 8); the other formats, and the
-  // symmetric format where the step kernel does not apply, run one CUDA-core
-  // kernel for all of them
-  if (block != kBlock || (zp == nullptr && !step)) {
+  // the step kernel takes block 32 with or without zero-points (its stages
+  // then hold constant zero-points of 8) and, at M = 1, blocks 16, 64 and
+  // 128; the other formats, and the symmetric format where the step kernel
+  // does not apply, run one CUDA-core kernel for all of them
+  if (!step && (block != kBlock || zp == nullptr)) {
     // the other formats of the family: one CUDA-core kernel for all of them
     if ((st = launch_general(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,
                              split_k, dev.sms, static_cast<cudaStream_t>(stream), query)) != MNB_OK ||
@@ -2075,7 +2308,7 @@ int dispatch(const void* x, const uint8_t* qweight, const void* scales, const ui
   p.out_bf16 = out_dtype == MNB_OUT_BF16;
   p.weights_ready = (flags & MNB_FLAG_WEIGHTS_READY) ? 1 : 0;
 
-  const void* fn = step ? reinterpret_cast<const void*>(pick_step_kernel(M, math))
+  const void* fn = step ? reinterpret_cast<const void*>(pick_step_kernel(M, math, block))
                         : reinterpret_cast<const void*>(pick_kernel(M, ks));
   if (query) {
     query->fn = fn;

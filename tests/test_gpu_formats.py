@@ -22,6 +22,18 @@ def built():
     mnb.load()
 
 
+def expects_step(M, K, block, symmetric):
+    """Which kernel a default launch of this format takes: the step kernel for
+    block 32 without zero-points at K a multiple of 1024, and at M = 1 for
+    blocks 16, 64 and 128 when K is a multiple of 1024 and the zero-point rows
+    (K / (2 block) bytes) are whole 16-byte chunks; else the general kernel."""
+    if K % 1024:
+        return False
+    if block == 32:
+        return symmetric
+    return M == 1 and (symmetric or K % (32 * block) == 0)
+
+
 def _run_both(inp, symmetric, split=0):
     dev = _gpu.to_device(inp, symmetric=symmetric)
     y16 = _gpu.bits(_gpu.run(dev, "f16", split, block=inp.block))
@@ -39,13 +51,8 @@ def test_small_shapes(block, symmetric, M, N, K):
     c0 = mnb.counters()
     _run_both(inp, symmetric)
     c1 = mnb.counters()
-    if block == 32:
-        # symmetric block 32: the step kernel where it applies (K a multiple
-        # of 1024, no K split), else the general kernel
-        step = K % 1024 == 0
-        assert c1[13] - c0[13] == (2 if step else 0) and c1[15] - c0[15] == (0 if step else 2)
-    else:
-        assert c1[15] - c0[15] == 2
+    step = expects_step(M, K, block, symmetric)
+    assert c1[13] - c0[13] == (2 if step else 0) and c1[15] - c0[15] == (0 if step else 2)
 
 
 @pytest.mark.parametrize("block,symmetric", FORMATS, ids=FORMAT_IDS)
@@ -58,13 +65,60 @@ def test_every_split(block, symmetric, split):
 
 @pytest.mark.parametrize("M,N,K,block,symmetric", [
     (1, 4096, 4096, 16, False), (1, 4096, 4096, 64, True), (1, 4096, 4096, 128, False),
-    (1, 4096, 4096, 32, True), (1, 27648, 5120, 64, False), (8, 8192, 8192, 16, True),
+    (1, 4096, 4096, 32, True), (1, 27648, 5120, 64, False), (1, 27648, 5120, 64, True),
+    (1, 151936, 4096, 128, False), (1, 151936, 4096, 16, True), (8, 8192, 8192, 16, True),
     (4, 8192, 8192, 128, True),
 ])
 def test_full_size(M, N, K, block, symmetric):
-    """Decode-layer sizes, every output element compared with the oracle."""
+    """Decode-layer sizes, every output element compared with the oracle, on
+    the kernel the format takes there."""
     inp = make_inputs(M, N, K, seed=N + block, block=block)
+    c0 = mnb.counters()[13]
     _run_both(inp, symmetric)
+    assert mnb.counters()[13] - c0 == (2 if expects_step(M, K, block, symmetric) else 0)
+
+
+# (block, symmetric, N, K): tiles of 16, 32 and 64 rows, ragged N, stages of 3
+# to 16 segments (K = 5120 at N = 4864 takes 32-row tiles and 5 segments a
+# stage, so the scale and zero-point boxes start inside a chunk), and the
+# largest K whose activations stage
+STEP_FORMATS = [
+    (16, False, 1, 1024), (16, False, 77, 3072), (16, False, 4864, 5120), (16, True, 1000, 1024),
+    (16, True, 4864, 5120), (64, False, 77, 2048), (64, False, 4864, 4096), (64, False, 1000, 6144),
+    (64, False, 300, 12288), (64, True, 77, 1024), (64, True, 4864, 5120), (128, False, 1, 4096),
+    (128, False, 4864, 8192), (128, False, 1000, 12288), (128, True, 77, 1024),
+    (128, True, 4864, 5120), (128, True, 300, 3072), (64, False, 33, 53248),
+]
+
+
+@pytest.mark.parametrize("block,symmetric,N,K", STEP_FORMATS)
+def test_step_kernel_formats(block, symmetric, N, K):
+    """Blocks 16, 64 and 128 at M = 1 on the step kernel: its scale and
+    zero-point boxes follow the block size; every element against the
+    oracle, both output dtypes."""
+    assert expects_step(1, K, block, symmetric)
+    info = mnb.launch_info(1, N, K, block=block, symmetric=symmetric)
+    assert "step kernel (CUDA-core" in info["kernel"], info
+    inp = make_inputs(1, N, K, seed=N + K + block, block=block)
+    c0 = mnb.counters()[13]
+    _run_both(inp, symmetric)
+    assert mnb.counters()[13] - c0 == 2
+
+
+@pytest.mark.parametrize("block", [64, 128])
+def test_step_kernel_format_limits(block):
+    """With zero-points, block 64 needs K a multiple of 2048 and block 128 of
+    4096 for the step kernel; other K run the general kernel, with the same
+    bound."""
+    K = 32 * block + 1024
+    assert not expects_step(1, K, block, False) and expects_step(1, K, block, True)
+    inp = make_inputs(1, 130, K, seed=block, block=block)
+    for symmetric in (False, True):
+        c0 = mnb.counters()
+        _run_both(inp, symmetric)
+        c1 = mnb.counters()
+        assert c1[13] - c0[13] == (2 if symmetric else 0)
+        assert c1[15] - c0[15] == (0 if symmetric else 2)
 
 
 @pytest.mark.parametrize("block", [16, 64, 128])

@@ -100,10 +100,11 @@ typedef enum mnb_status {
  *   block    16, 32 (MNB_BLOCK), 64 or 128.  Block 32 with zero-points runs
  *            the kernels tuned for it, and so does block 32 without them
  *            where the TMA step kernel applies (constant zero-points of 8 in
- *            its stages).  At M = 1 the step kernel also takes blocks 16, 64
- *            and 128 where it applies (split_k 0 or 1, K a multiple of 1024
- *            and, with zero-points, of 32 * block, so each zero-point row is
- *            whole 16-byte chunks).  Elsewhere the other formats run one
+ *            its stages).  The step kernel also takes blocks 16, 64 and 128
+ *            where it applies (no tensor-core flag, split_k 0 or 1, K a
+ *            multiple of 1024 and, with zero-points, of 32 * block, so each
+ *            zero-point row is whole 16-byte chunks, and the staged
+ *            activations fit).  Elsewhere the other formats run one
  *            CUDA-core kernel of the same exact arithmetic, where split_k
  *            (0 = chosen by the library) is the number of warps that split
  *            each row's K range inside one CTA, at most 8.

@@ -1499,7 +1499,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         if (lane == 0) mbar_arrive(ready0 + 8u * js);
       }
     } else {
-      // Blocks of kB = 16, 64 or 128 weights (M = 1): the lane layout of
+      // Blocks of kB = 16, 64 or 128 weights: the lane layout of
       // block 32 above, with a segment holding kNbs blocks and the lane's
       // 64 k starting at block lane_blk of the warp's segment.  A stage's
       // scale box starts at the 8-scale chunk holding its first block bs0,
@@ -1941,9 +1941,10 @@ bool step_shape(int M, int K, bool tensor_cores) {
   return K % 1024 == 0 && K <= 65536 && step_x_bytes(M, K / kBlock, math) <= limit;
 }
 
-// Formats the step kernel takes besides block 32: blocks 16, 64 and 128 at
-// M = 1 on the CUDA-core math, where the zero-point rows (K / (2 block) bytes)
-// are whole 16-byte chunks for the tensor copies.
+// Formats the step kernel takes besides block 32: blocks 16, 64 and 128 on
+// the CUDA-core math with two rows per lane (for every M), where the
+// zero-point rows (K / (2 block) bytes) are whole 16-byte chunks for the
+// tensor copies.
 bool step_takes_block(int block, int K, const void* zp) {
   return (block == 16 || block == 64 || block == 128) && (zp == nullptr || K % (32 * block) == 0);
 }
@@ -1957,26 +1958,26 @@ bool use_step(int M, int K, int split_k, const void* scales, const void* zp,
 
 using MmaFn = void (*)(const Params, const CUtensorMap, const CUtensorMap, const CUtensorMap);
 
-template <int kMath>
+template <int kMath, int kB = kBlock>
 MmaFn step_kernel_for(int M) {
   switch (M) {
-    case 1: return &mnb_gemv_step_kernel<1, kMath>;
-    case 2: return &mnb_gemv_step_kernel<2, kMath>;
-    case 3: return &mnb_gemv_step_kernel<3, kMath>;
-    case 4: return &mnb_gemv_step_kernel<4, kMath>;
-    case 5: return &mnb_gemv_step_kernel<5, kMath>;
-    case 6: return &mnb_gemv_step_kernel<6, kMath>;
-    case 7: return &mnb_gemv_step_kernel<7, kMath>;
-    default: return &mnb_gemv_step_kernel<8, kMath>;
+    case 1: return &mnb_gemv_step_kernel<1, kMath, kB>;
+    case 2: return &mnb_gemv_step_kernel<2, kMath, kB>;
+    case 3: return &mnb_gemv_step_kernel<3, kMath, kB>;
+    case 4: return &mnb_gemv_step_kernel<4, kMath, kB>;
+    case 5: return &mnb_gemv_step_kernel<5, kMath, kB>;
+    case 6: return &mnb_gemv_step_kernel<6, kMath, kB>;
+    case 7: return &mnb_gemv_step_kernel<7, kMath, kB>;
+    default: return &mnb_gemv_step_kernel<8, kMath, kB>;
   }
 }
 
 MmaFn pick_step_kernel(int M, int math, int block) {
-  if (block != kBlock) {  // M = 1, CUDA-core math (step_takes_block)
+  if (block != kBlock) {  // two rows per lane (step_takes_block)
     switch (block) {
-      case 16: return &mnb_gemv_step_kernel<1, kMathWide, 16>;
-      case 64: return &mnb_gemv_step_kernel<1, kMathWide, 64>;
-      default: return &mnb_gemv_step_kernel<1, kMathWide, 128>;
+      case 16: return step_kernel_for<kMathWide, 16>(M);
+      case 64: return step_kernel_for<kMathWide, 64>(M);
+      default: return step_kernel_for<kMathWide, 128>(M);
     }
   }
   if (math == kMathMma) return step_kernel_for<kMathMma>(M);
@@ -2272,8 +2273,8 @@ int dispatch(const void* x, const uint8_t* qweight, const void* scales, const ui
   DeviceInfo dev;
   if ((st = device_info(&dev)) != MNB_OK) return st;
   const bool tc = (flags & MNB_FLAG_TENSOR_CORES) != 0;
-  const int math = step_math(M, tc);
-  const bool step_format = block == kBlock || (M == 1 && !tc && step_takes_block(block, K, zp));
+  const int math = block == kBlock ? step_math(M, tc) : kMathWide;
+  const bool step_format = block == kBlock || (!tc && step_takes_block(block, K, zp));
   bool step = step_format && use_step(M, K, split_k, scales, zp, tc);
   Plan plan{};
   if (step && make_mma_plan(dev, M, N, K, math, block, &plan) != MNB_OK) {
@@ -2281,9 +2282,9 @@ int dispatch(const void* x, const uint8_t* qweight, const void* scales, const ui
     plan = Plan{};
   }
   // the step kernel takes block 32 with or without zero-points (its stages
-  // then hold constant zero-points of 8) and, at M = 1, blocks 16, 64 and
-  // 128; the other formats, and the symmetric format where the step kernel
-  // does not apply, run one CUDA-core kernel for all of them
+  // then hold constant zero-points of 8) and blocks 16, 64 and 128 (two rows
+  // per lane for every M); where it does not apply, the other formats and the
+  // symmetric format run one CUDA-core kernel for all of them
   if (!step && (block != kBlock || zp == nullptr)) {
     // the other formats of the family: one CUDA-core kernel for all of them
     if ((st = launch_general(x, qweight, scales, zp, y, M, N, K, block, out_dtype == MNB_OUT_BF16,

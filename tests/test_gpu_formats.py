@@ -24,14 +24,25 @@ def built():
 
 def expects_step(M, K, block, symmetric):
     """Which kernel a default launch of this format takes: the step kernel for
-    block 32 without zero-points at K a multiple of 1024, and at M = 1 for
-    blocks 16, 64 and 128 when K is a multiple of 1024 and the zero-point rows
-    (K / (2 block) bytes) are whole 16-byte chunks; else the general kernel."""
-    if K % 1024:
+    block 32 without zero-points at K a multiple of 1024, and for blocks 16,
+    64 and 128 when K is a multiple of 1024 and the zero-point rows
+    (K / (2 block) bytes) are whole 16-byte chunks (and the staged activations,
+    K / 32 * (64 M + 16) bytes, fit in 136 KiB); else the general kernel."""
+    if K % 1024 or K // 32 * (64 * M + 16) > 136 * 1024:
         return False
     if block == 32:
         return symmetric
-    return M == 1 and (symmetric or K % (32 * block) == 0)
+    return symmetric or K % (32 * block) == 0
+
+
+def takes_step(M, N, K, block, symmetric):
+    """Whether a default launch runs the step kernel, as the library reports
+    it; never outside the routing conditions of expects_step (inside them the
+    stage ring may still not fit beside the activations, and the launch then
+    runs the general kernel)."""
+    step = "step kernel" in mnb.launch_info(M, N, K, block=block, symmetric=symmetric)["kernel"]
+    assert not step or expects_step(M, K, block, symmetric), (M, N, K, block, symmetric)
+    return step
 
 
 def _run_both(inp, symmetric, split=0):
@@ -51,7 +62,7 @@ def test_small_shapes(block, symmetric, M, N, K):
     c0 = mnb.counters()
     _run_both(inp, symmetric)
     c1 = mnb.counters()
-    step = expects_step(M, K, block, symmetric)
+    step = takes_step(M, N, K, block, symmetric)
     assert c1[13] - c0[13] == (2 if step else 0) and c1[15] - c0[15] == (0 if step else 2)
 
 
@@ -75,7 +86,7 @@ def test_full_size(M, N, K, block, symmetric):
     inp = make_inputs(M, N, K, seed=N + block, block=block)
     c0 = mnb.counters()[13]
     _run_both(inp, symmetric)
-    assert mnb.counters()[13] - c0 == (2 if expects_step(M, K, block, symmetric) else 0)
+    assert mnb.counters()[13] - c0 == (2 if takes_step(M, N, K, block, symmetric) else 0)
 
 
 # (block, symmetric, N, K): tiles of 16, 32 and 64 rows, ragged N, stages of 3
@@ -103,6 +114,26 @@ def test_step_kernel_formats(block, symmetric, N, K):
     c0 = mnb.counters()[13]
     _run_both(inp, symmetric)
     assert mnb.counters()[13] - c0 == 2
+
+
+@pytest.mark.parametrize("block,symmetric", [(16, False), (16, True), (64, False), (64, True),
+                                             (128, False), (128, True)])
+@pytest.mark.parametrize("M,N,K", [(2, 300, 4096), (3, 77, 8192), (4, 4864, 5120), (8, 1000, 8192)])
+def test_step_kernel_formats_small_batch(block, symmetric, M, N, K):
+    """The other block sizes at M = 2 to 8 on the step kernel's two-row
+    layout, where the format's K allows it; every element of both dtypes."""
+    if K % block:
+        pytest.skip("K not a multiple of the block size")
+    inp = make_inputs(M, N, K, seed=M * 100 + N + block, block=block)
+    c0 = mnb.counters()[13]
+    _run_both(inp, symmetric)
+    step = takes_step(M, N, K, block, symmetric)
+    assert mnb.counters()[13] - c0 == (2 if step else 0)
+    if step:
+        assert "two rows per lane" in mnb.launch_info(M, N, K, block=block,
+                                                      symmetric=symmetric)["kernel"]
+    if M <= 4 and expects_step(M, K, block, symmetric):
+        assert step                                    # the ring fits at these sizes
 
 
 @pytest.mark.parametrize("block", [64, 128])

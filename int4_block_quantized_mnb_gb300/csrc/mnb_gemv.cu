@@ -129,6 +129,7 @@ struct Params {
   int xp_pitch;     // bytes per activation row of those fragments
   int flag_offset;  // offset of the CTA abort flag
   int blk;          // weights per quantization block (step kernel)
+  int zp_async;     // step kernel, blocks 64/128: zero-points by per-thread copies
 };
 
 // ---------------------------------------------------------------- PTX glue --
@@ -880,6 +881,22 @@ __global__ void __launch_bounds__(max_threads(M), 1) mnb_gemv_rowtile_kernel(con
 //           (r * zp_zb + G / 4 - first chunk) * 16 + 4 (G % 4); zp_zb odd.
 // Rows past N are zero-filled by the copies and never stored.
 
+// Per-thread asynchronous copies of 4 or 8 bytes, and the arrival on an
+// mbarrier once all of the thread's earlier copies have landed (the barrier's
+// expected count includes it: .noinc).
+template <int kBytes>
+__device__ __forceinline__ void cp_async_small(uint32_t dst, const void* src) {
+  static_assert(kBytes == 4 || kBytes == 8, "cp.async size");
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(kBytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint32_t bar) {
   asm volatile(
@@ -909,7 +926,7 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
                                                 volatile int* abort_flag, int t_begin,
                                                 int nunits, const CUtensorMap* tm_q,
                                                 const CUtensorMap* tm_sc,
-                                                const CUtensorMap* tm_zp) {
+                                                const CUtensorMap* tm_zp, int lane) {
   prefetch_tensor_map(tm_q);
   prefetch_tensor_map(tm_sc);
   prefetch_tensor_map(tm_zp);
@@ -938,9 +955,11 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
     const uint32_t bar = full0 + 8u * s;
     const int row0 = tile * R;
     const int seg0 = step * p.wk;
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.tx_bytes));
-    tma_load_3d(st, tm_q, 0, row0, seg0, bar);
+    if (kB == 32 || lane == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.tx_bytes));
+      tma_load_3d(st, tm_q, 0, row0, seg0, bar);
+    }
     if constexpr (kB == 32) {
       tma_load_3d(st + p.sc_offset, tm_sc, 0, seg0, row0, bar);
       if (p.zp) tma_load_3d(st + p.zp_offset, tm_zp, 0, seg0 >> 2, row0, bar);
@@ -948,8 +967,34 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
       // the boxes start at the 8-scale and 32-block zero-point chunks holding
       // the stage's first quantization block
       const int bs0 = seg0 * (kMmaSeg / kB);
-      tma_load_3d(st + p.sc_offset, tm_sc, 0, bs0 >> 3, row0, bar);
-      if (p.zp) tma_load_3d(st + p.zp_offset, tm_zp, 0, bs0 >> 5, row0, bar);
+      if (lane == 0) {
+        tma_load_3d(st + p.sc_offset, tm_sc, 0, bs0 >> 3, row0, bar);
+        if (p.zp && !p.zp_async) tma_load_3d(st + p.zp_offset, tm_zp, 0, bs0 >> 5, row0, bar);
+      }
+      if constexpr (kB >= 64) {
+        if (p.zp_async) {
+          // Zero-point rows of K / (2 kB) bytes that are not whole 16-byte
+          // chunks (no tensor map): the whole warp copies, row by row, the
+          // 8-byte (kB = 64) or 4-byte (kB = 128) words holding the stage's
+          // zero-point bytes to the places the tensor copy would use (row r's
+          // box starts at byte b_lo of the row); each lane then arrives on
+          // the stage's full barrier once its copies have landed.
+          constexpr int kW = kB == 64 ? 8 : 4;
+          const int rowbytes = p.K / (2 * kB);
+          const int b_lo = 16 * (bs0 >> 5);
+          const int need_lo = (bs0 >> 1) / kW * kW;
+          const int need_hi = min(rowbytes, ((bs0 + p.wk * (kMmaSeg / kB)) / 2 + kW - 1) / kW * kW);
+          const int words = (need_hi - need_lo) / kW;
+          const int rows = min(R, p.N - row0);
+          const uint32_t dst0 = st + p.zp_offset + (need_lo - b_lo);
+          const uint8_t* src0 = p.zp + need_lo;
+          for (int r = lane; r < rows; r += 32)
+            for (int w = 0; w < words; ++w)
+              cp_async_small<kW>(dst0 + r * p.zp_zb * 16 + w * kW,
+                                 src0 + static_cast<size_t>(row0 + r) * rowbytes + w * kW);
+          cp_async_arrive_noinc(bar);
+        }
+      }
     }
     issued = i + 1;
     if (++step == p.steps) {
@@ -960,6 +1005,9 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
       s = 0;
       ph ^= 1u;
     }
+  }
+  if constexpr (kB >= 64) {
+    if (p.zp_async) cp_async_wait_all();
   }
   for (int i = max(0, issued - p.stages); i < issued; ++i) {
     const int si = i % p.stages;
@@ -1015,8 +1063,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int row_end = min(p.N, t_end * R);
 
   if (threadIdx.x == 0) {
+    // full: the producer's expect_tx arrival, plus one per producer lane
+    // when the zero-points come by per-thread copies
+    const uint32_t full_count = kB >= 64 && p.zp_async ? 33u : 1u;
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(full0 + 8u * s, 1);
+      mbar_init(full0 + 8u * s, full_count);
       mbar_init(empty0 + 8u * s, W);
     }
     for (int j = 0; j < nslots; ++j) {
@@ -1031,9 +1082,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   allow_dependents();
 
   if (warp == producer_warp) {
-    if (lane == 0)
+    if (lane == 0 || (kB >= 64 && p.zp_async))
       run_tc_producer<kB>(p, smem, full0, empty0, abort_flag, t_begin, ntiles * p.steps, &tm_q,
-                      &tm_sc, &tm_zp);
+                          &tm_sc, &tm_zp, lane);
     __syncwarp();
     return;
   }
@@ -1942,11 +1993,12 @@ bool step_shape(int M, int K, bool tensor_cores) {
 }
 
 // Formats the step kernel takes besides block 32: blocks 16, 64 and 128 on
-// the CUDA-core math with two rows per lane (for every M), where the
-// zero-point rows (K / (2 block) bytes) are whole 16-byte chunks for the
-// tensor copies.
-bool step_takes_block(int block, int K, const void* zp) {
-  return (block == 16 || block == 64 || block == 128) && (zp == nullptr || K % (32 * block) == 0);
+// the CUDA-core math with two rows per lane (for every M).  Their zero-point
+// rows (K / (2 block) bytes) come by tensor copies where they are whole
+// 16-byte chunks (always for block 16) and by per-thread copies otherwise.
+bool step_takes_block(int block) { return block == 16 || block == 64 || block == 128; }
+bool zp_by_thread_copies(int block, int K, const void* zp) {
+  return zp != nullptr && block >= 64 && K % (32 * block) != 0;
 }
 
 bool use_step(int M, int K, int split_k, const void* scales, const void* zp,
@@ -2274,7 +2326,7 @@ int dispatch(const void* x, const uint8_t* qweight, const void* scales, const ui
   if ((st = device_info(&dev)) != MNB_OK) return st;
   const bool tc = (flags & MNB_FLAG_TENSOR_CORES) != 0;
   const int math = block == kBlock ? step_math(M, tc) : kMathWide;
-  const bool step_format = block == kBlock || (!tc && step_takes_block(block, K, zp));
+  const bool step_format = block == kBlock || (!tc && step_takes_block(block));
   bool step = step_format && use_step(M, K, split_k, scales, zp, tc);
   Plan plan{};
   if (step && make_mma_plan(dev, M, N, K, math, block, &plan) != MNB_OK) {
@@ -2308,6 +2360,7 @@ int dispatch(const void* x, const uint8_t* qweight, const void* scales, const ui
   p.y = y;
   p.out_bf16 = out_dtype == MNB_OUT_BF16;
   p.weights_ready = (flags & MNB_FLAG_WEIGHTS_READY) ? 1 : 0;
+  p.zp_async = step && zp_by_thread_copies(block, K, zp) ? 1 : 0;
 
   const void* fn = step ? reinterpret_cast<const void*>(pick_step_kernel(M, math, block))
                         : reinterpret_cast<const void*>(pick_kernel(M, ks));
@@ -2329,10 +2382,11 @@ int dispatch(const void* x, const uint8_t* qweight, const void* scales, const ui
     if ((st = tensor_map(kMapCodes, qweight, p, &maps[0])) != MNB_OK ||
         (st = tensor_map(kMapScales, scales, p, &maps[1])) != MNB_OK)
       return st;
-    if (zp) {
+    if (zp && !p.zp_async) {
       if ((st = tensor_map(kMapZeros, zp, p, &maps[2])) != MNB_OK) return st;
     } else {
-      maps[2] = maps[1];                          // never copied from (no zero-points)
+      // never copied from: no zero-points, or zero-points by per-thread copies
+      maps[2] = maps[1];
       p.tx_bytes -= kMmaRows * p.tr * p.zp_zb * 16;
     }
   }

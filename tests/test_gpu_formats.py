@@ -23,16 +23,13 @@ def built():
 
 
 def expects_step(M, K, block, symmetric):
-    """Which kernel a default launch of this format takes: the step kernel for
-    block 32 without zero-points at K a multiple of 1024, and for blocks 16,
-    64 and 128 when K is a multiple of 1024 and the zero-point rows
-    (K / (2 block) bytes) are whole 16-byte chunks (and the staged activations,
-    K / 32 * (64 M + 16) bytes, fit in 136 KiB); else the general kernel."""
+    """Which kernel a default launch of this format may take: the step kernel
+    for block 32 without zero-points and for blocks 16, 64 and 128 with or
+    without them, when K is a multiple of 1024 and the staged activations,
+    K / 32 * (64 M + 16) bytes, fit in 136 KiB; else the general kernel."""
     if K % 1024 or K // 32 * (64 * M + 16) > 136 * 1024:
         return False
-    if block == 32:
-        return symmetric
-    return symmetric or K % (32 * block) == 0
+    return block != 32 or symmetric
 
 
 def takes_step(M, N, K, block, symmetric):
@@ -99,6 +96,10 @@ STEP_FORMATS = [
     (64, False, 300, 12288), (64, True, 77, 1024), (64, True, 4864, 5120), (128, False, 1, 4096),
     (128, False, 4864, 8192), (128, False, 1000, 12288), (128, True, 77, 1024),
     (128, True, 4864, 5120), (128, True, 300, 3072), (64, False, 33, 53248),
+    # zero-point rows that are not whole 16-byte chunks: per-thread copies
+    (64, False, 4864, 5120), (64, False, 27648, 5120), (64, False, 77, 1024), (64, False, 300, 3072),
+    (128, False, 4864, 5120), (128, False, 77, 1024), (128, False, 1000, 3072),
+    (128, False, 130, 6144), (64, False, 33, 54272),
 ]
 
 
@@ -137,19 +138,18 @@ def test_step_kernel_formats_small_batch(block, symmetric, M, N, K):
 
 
 @pytest.mark.parametrize("block", [64, 128])
-def test_step_kernel_format_limits(block):
-    """With zero-points, block 64 needs K a multiple of 2048 and block 128 of
-    4096 for the step kernel; other K run the general kernel, with the same
-    bound."""
-    K = 32 * block + 1024
-    assert not expects_step(1, K, block, False) and expects_step(1, K, block, True)
-    inp = make_inputs(1, 130, K, seed=block, block=block)
-    for symmetric in (False, True):
-        c0 = mnb.counters()
-        _run_both(inp, symmetric)
-        c1 = mnb.counters()
-        assert c1[13] - c0[13] == (2 if symmetric else 0)
-        assert c1[15] - c0[15] == (0 if symmetric else 2)
+def test_zero_points_by_thread_copies(block):
+    """Blocks 64 and 128 with zero-points at K not a multiple of 32 * block:
+    the zero-point rows are not whole 16-byte chunks, so the producer warp
+    copies them per thread; against the symmetric format and K where the
+    tensor copy applies, on the same step kernel, every element."""
+    for K in (32 * block + 1024, 32 * block):
+        inp = make_inputs(1, 130, K, seed=block + K, block=block)
+        for symmetric in (False, True):
+            assert takes_step(1, 130, K, block, symmetric)
+            c0 = mnb.counters()[13]
+            _run_both(inp, symmetric)
+            assert mnb.counters()[13] - c0 == 2
 
 
 @pytest.mark.parametrize("block", [16, 64, 128])

@@ -206,6 +206,29 @@ def test_weights_ready_chain_matches_plain_calls():
         assert torch.isfinite(a.float()).all()
 
 
+def test_weights_ready_chain_with_zero_point_copies():
+    """A chain of K = N = 5120 layers, each reading the previous output with
+    the early-weights promise: blocks 64 and 128 take their zero-points by
+    per-thread copies, blocks 16 and 32 by tensor copies; the bits equal plain
+    calls."""
+    layers = [(64, False), (128, False), (16, False), (32, False), (64, False)]
+    devs = [_gpu.to_device(make_inputs(1, 5120, 5120, seed=80 + i, block=b), symmetric=sym)
+            for i, (b, sym) in enumerate(layers)]
+    for b, sym in layers:
+        assert takes_step(1, 5120, 5120, b, sym)
+    x = devs[0][0]
+    ref, got = [x], [x]
+    for (b, _), (_, q, s, z) in zip(layers, devs):
+        ref.append(mnb.gemv(ref[-1], q, s, z, "f16", block=b))
+    torch.cuda.synchronize()
+    for (b, _), (_, q, s, z) in zip(layers, devs):
+        got.append(mnb.gemv(got[-1], q, s, z, "f16", block=b, weights_ready=True))
+    torch.cuda.synchronize()
+    for a, c in zip(ref[1:], got[1:]):
+        assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+    assert mnb.device_error() == 0
+
+
 @pytest.mark.parametrize("tc", [False, True], ids=["default", "tensor_cores"])
 @pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (1, 27648, 5120), (2, 300, 8192), (4, 1000, 2048),
                                    (8, 8192, 8192), (1, 1, 1024), (3, 129, 3072)])

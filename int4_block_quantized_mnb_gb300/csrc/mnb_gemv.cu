@@ -1438,6 +1438,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
         uint32_t xa = x_lane;
         uint32_t zr = 0;                                    // first segment of the stage, mod 4
+        // two stages per loop pass and a branch-free ring advance: the
+        // compiler overlaps one stage's loads and waits with the previous
+        // stage's arithmetic (lm-head 62.4 -> 60.5 us, gate-up 17.4 -> 17.0)
+#pragma unroll 2
         for (int step = 0; step < steps; ++step) {
           if (!mbar_wait(fb, ph, abort_flag, kErrStageData)) {
             run = false;
@@ -1510,16 +1514,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           });
           __syncwarp();
           if (lane == 0) mbar_arrive(eb);
-          if (++s == stages) {
-            s = 0;
-            sb = ring0;
-            fb = full0;
-            eb = empty0;
-            ph ^= 1u;
-          } else {
-            sb += stage_bytes;
-            fb += 8u;
-            eb += 8u;
+          {
+            const bool wrap = ++s == stages;
+            s = wrap ? 0 : s;
+            sb = wrap ? ring0 : sb + stage_bytes;
+            fb = wrap ? full0 : fb + 8u;
+            eb = wrap ? empty0 : eb + 8u;
+            ph ^= wrap ? 1u : 0u;
           }
           xa += x_step;
           zr = (zr + wk) & 3u;
@@ -1594,6 +1595,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           for (int m = 0; m < M; ++m) acc[i][m] = 0.f;
         uint32_t xa = x_lane;
         uint32_t bsm = 0;                                 // first block of the stage, mod 32
+        // two stages per pass, branch-free ring advance (as for block 32)
+#pragma unroll 2
         for (int step = 0; step < steps; ++step) {
           if (!mbar_wait(fb, ph, abort_flag, kErrStageData)) {
             run = false;
@@ -1699,16 +1702,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(eb);
-          if (++s == stages) {
-            s = 0;
-            sb = ring0;
-            fb = full0;
-            eb = empty0;
-            ph ^= 1u;
-          } else {
-            sb += stage_bytes;
-            fb += 8u;
-            eb += 8u;
+          {
+            const bool wrap = ++s == stages;
+            s = wrap ? 0 : s;
+            sb = wrap ? ring0 : sb + stage_bytes;
+            fb = wrap ? full0 : fb + 8u;
+            eb = wrap ? empty0 : eb + 8u;
+            ph ^= wrap ? 1u : 0u;
           }
           xa += x_step;
           bsm = (bsm + wk * kNbs) & 31u;

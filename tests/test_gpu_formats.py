@@ -23,13 +23,12 @@ def built():
 
 
 def expects_step(M, K, block, symmetric):
-    """Which kernel a default launch of this format may take: the step kernel
-    for block 32 without zero-points and for blocks 16, 64 and 128 with or
-    without them, when K is a multiple of 1024 and the staged activations,
-    K / 32 * (64 M + 16) bytes, fit in 136 KiB; else the general kernel."""
-    if K % 1024 or K // 32 * (64 * M + 16) > 136 * 1024:
-        return False
-    return block != 32 or symmetric
+    """Whether a default launch of this format may take the step kernel:
+    every block size, with or without zero-points, when K is a multiple of
+    1024 and the staged activations, K / 32 * (64 M + 16) bytes, fit in
+    136 KiB; else the general kernel (or, for block 32 with zero-points, the
+    row-tile kernel)."""
+    return K % 1024 == 0 and K // 32 * (64 * M + 16) <= 136 * 1024
 
 
 def takes_step(M, N, K, block, symmetric):

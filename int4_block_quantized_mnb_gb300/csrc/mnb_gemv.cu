@@ -1290,6 +1290,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     bool run = true;
+    int js = 0;                                          // reduction slot of tile t
+    uint32_t jround = 0;                                 // and t / nslots
     for (int t = 0; t < ntiles && run; ++t) {
       float acc[4][M];
 #pragma unroll
@@ -1383,8 +1385,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
           acc[i][m] = v;
         }
-      const int js = t % nslots;
-      if (t >= nslots && !mbar_wait(free0 + 8u * js, ((t / nslots) - 1) & 1, abort_flag,
+      if (jround > 0 && !mbar_wait(free0 + 8u * js, (jround - 1) & 1u, abort_flag,
                                     kErrReduceSlot))
         break;
       if (j == 0) {
@@ -1396,6 +1397,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(ready0 + 8u * js);
+      if (++js == nslots) {
+        js = 0;
+        ++jround;
+      }
     }
   } else {
     if constexpr (kB == 32) {
@@ -1430,6 +1435,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       bool run = true;
+      int js = 0;                                          // reduction slot of tile t
+      uint32_t jround = 0;                                 // and t / nslots
       for (int t = 0; t < ntiles && run; ++t) {
         float acc[2][M];
 #pragma unroll
@@ -1536,8 +1543,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
             acc[i][m] = v;
           }
-        const int js = t % nslots;
-        if (t >= nslots && !mbar_wait(free0 + 8u * js, ((t / nslots) - 1) & 1, abort_flag,
+        if (jround > 0 && !mbar_wait(free0 + 8u * js, (jround - 1) & 1u, abort_flag,
                                       kErrReduceSlot))
           break;
         if (q == 0) {
@@ -1549,6 +1555,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(ready0 + 8u * js);
+        if (++js == nslots) {
+          js = 0;
+          ++jround;
+        }
       }
     } else {
       // Blocks of kB = 16, 64 or 128 weights: the lane layout of
@@ -1587,6 +1597,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       bool run = true;
+      int js = 0;                                          // reduction slot of tile t
+      uint32_t jround = 0;                                 // and t / nslots
       for (int t = 0; t < ntiles && run; ++t) {
         float acc[2][M];
 #pragma unroll
@@ -1724,8 +1736,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
             acc[i][m] = v;
           }
-        const int js = t % nslots;
-        if (t >= nslots && !mbar_wait(free0 + 8u * js, ((t / nslots) - 1) & 1, abort_flag,
+        if (jround > 0 && !mbar_wait(free0 + 8u * js, (jround - 1) & 1u, abort_flag,
                                       kErrReduceSlot))
           break;
         if (q == 0) {
@@ -1737,6 +1748,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(ready0 + 8u * js);
+        if (++js == nslots) {
+          js = 0;
+          ++jround;
+        }
       }
     }
   }

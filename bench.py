@@ -179,6 +179,41 @@ def recorded_traffic(workload):
     return int(v) if v else None
 
 
+def parse_cpulist(text):
+    """The CPU set of a sysfs cpulist ("0-3,8,10-11")."""
+    cpus = set()
+    for part in text.strip().split(","):
+        if part:
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+    return cpus
+
+
+def gpu_local_cpus(props):
+    """The host CPUs of the NUMA node the GPU is attached to (sysfs, by the
+    PCI bus id nvidia-smi reports for the device's UUID), or None.  Pinned
+    host buffers allocated from those CPUs land in that node's memory, next
+    to the GPU's link."""
+    exe = shutil.which("nvidia-smi")
+    uuid = str(getattr(props, "uuid", "") or "")
+    if exe is None or not uuid:
+        return None
+    if not uuid.startswith("GPU-"):
+        uuid = "GPU-" + uuid
+    try:
+        bus = subprocess.run([exe, "--query-gpu=pci.bus_id", "--format=csv,noheader", "-i", uuid],
+                             capture_output=True, text=True, timeout=20).stdout.strip()
+        dom, rest = bus.split(":", 1)
+        dev = f"{int(dom, 16):04x}:{rest}".lower()
+        node = int(open(f"/sys/bus/pci/devices/{dev}/numa_node").read().strip())
+        if node < 0:
+            return None
+        cpus = parse_cpulist(open(f"/sys/devices/system/node/node{node}/cpulist").read())
+        return (node, cpus) if cpus else None
+    except (OSError, ValueError, subprocess.SubprocessError):
+        return None
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
 
@@ -733,9 +768,18 @@ def main():
     achieved = bytes_call / per_launch_s / 1e9
     info = launch_record(mnb, w, outs[0], tc, w_block(w), w_zp(w, inp) is None, pm)
 
-    # End to end through the public API with pinned host buffers.
+    # End to end through the public API with pinned host buffers, allocated
+    # and touched from the CPUs of the GPU's own NUMA node.
     e2e = None
     if not args.no_e2e:
+        local = gpu_local_cpus(props)
+        saved_affinity = None
+        if local is not None and hasattr(os, "sched_setaffinity"):
+            try:
+                saved_affinity = os.sched_getaffinity(0)
+                os.sched_setaffinity(0, local[1])
+            except OSError:
+                saved_affinity = None
         hx = torch.from_numpy(inp.x.view(np.int16).copy()).view(torch.float16).pin_memory()
         hq = torch.from_numpy(inp.qweight).pin_memory()
         hs = torch.from_numpy(inp.scales.view(np.int16).copy()).view(torch.float16).pin_memory()
@@ -771,8 +815,11 @@ def main():
             e1.record(stream)
         torch.cuda.synchronize(dev)
         te = e0.elapsed_time(e1) / 1e3
+        if saved_affinity is not None:
+            os.sched_setaffinity(0, saved_affinity)
         e2e = {"value": bytes_call * L * E / te / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": E}
+               "d2h_bytes_per_step": d2h, "steps": E,
+               "host_numa_node": None if local is None else local[0]}
         del dq, ds, dx, dz
 
     # One sub-record per decode configuration (default format only).

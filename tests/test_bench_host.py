@@ -111,3 +111,13 @@ def test_pages_context_quotes_the_a100_figures():
     c = bench.PAGES_CONTEXT
     assert c["gate_up_gemv"]["us_per_call"] == 26.69 and c["gate_up_gemv"]["dram_tb_per_s"] == 2.267
     assert c["decode_64_tokens_bf16"]["cast_half_launches"] == [3024, 2398]
+
+
+def test_cpulist_and_gpu_numa_lookup():
+    """The e2e arm's host-buffer placement: sysfs cpulists parse, and a
+    device without a UUID (or a host without nvidia-smi) gives no placement."""
+    import types
+    import bench
+    assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench.parse_cpulist("") == set()
+    assert bench.gpu_local_cpus(types.SimpleNamespace(uuid="")) is None

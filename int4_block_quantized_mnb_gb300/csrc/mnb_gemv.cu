@@ -1023,9 +1023,10 @@ __device__ __forceinline__ void run_tc_producer(const Params& p, unsigned char* 
   }
 }
 
-// Math of the step kernel: CUDA-core with four rows per lane (small M),
-// CUDA-core with two rows per lane and shared activation loads (larger M), or
-// tensor-core (on request).
+// Math of the step kernel: CUDA-core with four rows per lane (M = 2, 3),
+// CUDA-core with two rows per lane and shared activation loads (M = 1 and
+// M >= 4, and every M for blocks 16, 64 and 128), or tensor-core (on
+// request).
 enum StepMath : int { kMathFma = 0, kMathWide = 1, kMathMma = 2 };
 
 namespace {
@@ -1404,10 +1405,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
   } else {
     if constexpr (kB == 32) {
-      // CUDA-core math for larger M.  Lane (q, rr) = (lane >> 3, lane & 7) takes
-      // rows 16 rho + rr and 16 rho + rr + 8 and the block pair (2q, 2q + 1) of
-      // the warp's segment of every stage.  An activation load (16 bytes of one
-      // 8-k group, shared by the eight lanes of a quarter warp) feeds both rows,
+      // CUDA-core math, two rows per lane (M = 1 and M >= 4).  Lane (q, rr) =
+      // (lane >> 3, lane & 7) takes rows 16 rho + rr and 16 rho + rr + 8 and the
+      // block pair (2q, 2q + 1) of the warp's segment of every stage.  An
+      // activation load (16 bytes of one 8-k group, shared by the eight lanes
+      // of a quarter warp) feeds both rows,
       // which balances shared-memory bandwidth against the FMA pipe; a lane holds
       // 2M accumulators, 2M block sums and one group's 4M activation registers.
       // Activation offsets inside a block are compile-time constants; only the

@@ -102,8 +102,8 @@ typedef enum mnb_status {
  *            where the TMA step kernel applies (constant zero-points of 8 in
  *            its stages).  The step kernel also takes blocks 16, 64 and 128
  *            where it applies (no tensor-core flag, split_k 0 or 1, K a
- *            multiple of 1024, and the staged activations and two stages
- *            fit).  Elsewhere the other formats run one
+ *            multiple of 1024, and the staged activations fit).  Elsewhere
+ *            the other formats run one
  *            CUDA-core kernel of the same exact arithmetic, where split_k
  *            (0 = chosen by the library) is the number of warps that split
  *            each row's K range inside one CTA, at most 8.

@@ -2097,41 +2097,47 @@ int make_mma_plan(const DeviceInfo& dev, int M, int N, int K, int math, int bloc
       tr = c;
     }
   }
-  int wk = std::min(kMmaWarps / tr, S);
-  while (S % wk) --wk;
   const int R = kMmaRows * tr;
-  // 8-scale and 32-block zero-point chunks one stage spans
-  const int nbs = kMmaSeg / block;
-  int sspan = 1, zspan = 1;
-  for (int st = 0; st < S / wk; ++st) {
-    const int b0 = st * wk * nbs, b1 = (st + 1) * wk * nbs - 1;
-    sspan = std::max(sspan, (b1 >> 3) - (b0 >> 3) + 1);
-    zspan = std::max(zspan, (b1 >> 5) - (b0 >> 5) + 1);
-  }
-  p.tr = tr;
-  p.wk = wk;
-  p.steps = S / wk;
-  p.wtc = wk * tr;
-  p.wpg = wk;                                      // partials per output for the epilogue
-  p.sc_sb = odd_at_least(sspan);
-  p.zp_zb = odd_at_least(zspan);
-  p.q_bytes = R * wk * 128;
-  p.sc_bytes = round_up(R * p.sc_sb * 16, 128);
-  p.zp_bytes = round_up(R * p.zp_zb * 16, 128);
-  p.sc_offset = p.q_bytes;
-  p.zp_offset = p.q_bytes + p.sc_bytes;
-  p.tx_bytes = R * (wk * 128 + p.sc_sb * 16 + p.zp_zb * 16);
-  p.stage_bytes = round_up(p.q_bytes + p.sc_bytes + p.zp_bytes, 1024);
-  // four reduction slots, or two when four would leave fewer than three stages
+  // K slices: the largest divisor of S up to 16 / tr; where the stages then
+  // do not fit twice beside the activations (block 16's large scale boxes
+  // at large M K), the next smaller divisor
   int nslots = kSlotsPerGroup, red_bytes = 0;
-  for (;;) {
-    red_bytes = round_up(nslots * wk * R * M * 4, 16);
-    const int fixed = x_bytes + red_bytes + 8 * 2 * nslots + 16;
-    p.stages = std::min(kMaxStages, (budget - fixed) / (p.stage_bytes + 16));
-    if (p.stages >= 3 || nslots == 2) break;
-    nslots = 2;
+  for (int wk = std::min(kMmaWarps / tr, S); wk >= 1; --wk) {
+    if (S % wk) continue;
+    // 8-scale and 32-block zero-point chunks one stage spans
+    const int nbs = kMmaSeg / block;
+    int sspan = 1, zspan = 1;
+    for (int st = 0; st < S / wk; ++st) {
+      const int b0 = st * wk * nbs, b1 = (st + 1) * wk * nbs - 1;
+      sspan = std::max(sspan, (b1 >> 3) - (b0 >> 3) + 1);
+      zspan = std::max(zspan, (b1 >> 5) - (b0 >> 5) + 1);
+    }
+    p.tr = tr;
+    p.wk = wk;
+    p.steps = S / wk;
+    p.wtc = wk * tr;
+    p.wpg = wk;                                      // partials per output for the epilogue
+    p.sc_sb = odd_at_least(sspan);
+    p.zp_zb = odd_at_least(zspan);
+    p.q_bytes = R * wk * 128;
+    p.sc_bytes = round_up(R * p.sc_sb * 16, 128);
+    p.zp_bytes = round_up(R * p.zp_zb * 16, 128);
+    p.sc_offset = p.q_bytes;
+    p.zp_offset = p.q_bytes + p.sc_bytes;
+    p.tx_bytes = R * (wk * 128 + p.sc_sb * 16 + p.zp_zb * 16);
+    p.stage_bytes = round_up(p.q_bytes + p.sc_bytes + p.zp_bytes, 1024);
+    // four reduction slots, or two when four would leave fewer than three stages
+    nslots = kSlotsPerGroup;
+    for (;;) {
+      red_bytes = round_up(nslots * wk * R * M * 4, 16);
+      const int fixed = x_bytes + red_bytes + 8 * 2 * nslots + 16;
+      p.stages = std::min(kMaxStages, (budget - fixed) / (p.stage_bytes + 16));
+      if (p.stages >= 3 || nslots == 2) break;
+      nslots = 2;
+    }
+    p.nslots = nslots;
+    if (p.stages >= 2) break;
   }
-  p.nslots = nslots;
   if (p.stages < 2) return fail(MNB_ERR_SHAPE, "shape needs more shared memory than one SM has");
   int off = p.stages * p.stage_bytes;
   p.xp_offset = off;
